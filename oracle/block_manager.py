@@ -1,0 +1,161 @@
+"""Block manager of the paged KV cache (oracle; test infrastructure only).
+
+Sources, in the order the rules are taken from them:
+
+* free list: "PagedAttention 内存管理深度解析" (deepinsea.top), "分页机制设计"
+  BlockManager sketch — the free list starts as the list of all block ids, a
+  request takes ceil(n/B) blocks by popping from the end, fails without side
+  effects when too few are free, and its blocks are appended back on release.
+  Here the initial list may be a seeded permutation ("seeded random block
+  placement"); popping from the end stays the rule.
+* reference counts, fork and copy-on-write: "079｜vLLM 与 PagedAttention"
+  (wq-win.github.io), §2 "共享与写时复制" (each physical block carries a
+  reference count; a branch that must write into a tail block still referenced
+  by others first copies it and remaps only its own table; a block is reclaimed
+  only when its count reaches zero), §2 "一次分叉什么时候真的要复制缓存块"
+  (full blocks stay shared; only the partly filled tail is ever copied) and the
+  §3 per-iteration algorithm box (check whether the next token needs a new
+  block; copy a shared tail before writing).
+* tail waste: same review, §2 "块大小决定有多少无法借给别人的尾部空间":
+  a sequence of L tokens holds B*ceil(L/B) slots.
+
+Readings (listed in the design notes): when several sequences share a tail and
+append in turn, each writer that still sees a count above one takes a copy;
+the last one (count one) writes in place. Freed blocks go back to the free list
+in the sequence's logical order. The GPU/CPU fallback allocation of the
+gitcode.csdn.net sketch is not the method (swap is a preemption path) and is
+not modelled: running out of blocks is an error.
+"""
+
+from __future__ import annotations
+
+
+class OutOfBlocks(RuntimeError):
+    """Too few free blocks; nothing was changed."""
+
+
+class BlockManagerStateError(RuntimeError):
+    """Unknown or duplicate sequence id, or a bad block id."""
+
+
+class BlockManager:
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        if num_blocks < 1 or block_size < 1:
+            raise ValueError("num_blocks and block_size must be positive")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        order = range(num_blocks) if free_order is None else [int(x) for x in free_order]
+        self.free = list(order)
+        if sorted(self.free) != list(range(num_blocks)):
+            raise ValueError("free_order must be a permutation of 0..num_blocks-1")
+        self.ref = [0] * num_blocks
+        self.tables: dict[int, list[int]] = {}
+        self.lens: dict[int, int] = {}
+
+    # -- queries ---------------------------------------------------------
+    def blocks_needed(self, num_tokens: int) -> int:
+        return -(-int(num_tokens) // self.block_size)
+
+    def num_free(self) -> int:
+        return len(self.free)
+
+    def table(self, seq: int) -> list[int]:
+        self._known(seq)
+        return list(self.tables[seq])
+
+    def length(self, seq: int) -> int:
+        self._known(seq)
+        return self.lens[seq]
+
+    def slot(self, seq: int, pos: int) -> int:
+        """Physical slot of position ``pos``: table[pos // B] * B + pos % B."""
+        t = self.tables[seq]
+        return t[pos // self.block_size] * self.block_size + pos % self.block_size
+
+    def slots(self, seq: int) -> list[int]:
+        return [self.slot(seq, p) for p in range(self.lens[seq])]
+
+    # -- operations ------------------------------------------------------
+    def allocate(self, seq: int, num_tokens: int) -> list[int]:
+        """Give a new sequence room for ``num_tokens`` tokens."""
+        if seq in self.tables:
+            raise BlockManagerStateError(f"sequence {seq} already allocated")
+        if num_tokens < 0:
+            raise ValueError("negative token count")
+        need = self.blocks_needed(num_tokens)
+        if need > len(self.free):
+            raise OutOfBlocks(f"need {need} blocks, {len(self.free)} free")
+        ids = [self.free.pop() for _ in range(need)]
+        for b in ids:
+            self.ref[b] = 1
+        self.tables[seq] = ids
+        self.lens[seq] = int(num_tokens)
+        return list(ids)
+
+    def fork(self, parent: int, child: int) -> None:
+        """``child`` shares every block of ``parent`` (reference count + 1)."""
+        self._known(parent)
+        if child in self.tables:
+            raise BlockManagerStateError(f"sequence {child} already allocated")
+        ids = list(self.tables[parent])
+        for b in ids:
+            self.ref[b] += 1
+        self.tables[child] = ids
+        self.lens[child] = self.lens[parent]
+
+    def append_slot(self, seq: int):
+        """Room for one more token of ``seq``.
+
+        Returns (slot, cow) where cow is None or the (src, dst) block pair whose
+        contents must be copied before the token is written.
+        """
+        self._known(seq)
+        L = self.lens[seq]
+        t = self.tables[seq]
+        cow = None
+        if L % self.block_size == 0:              # tail full (or no block yet)
+            if not self.free:
+                raise OutOfBlocks("no free block for the next token")
+            b = self.free.pop()
+            self.ref[b] = 1
+            t.append(b)
+        else:
+            tail = t[L // self.block_size]
+            if self.ref[tail] > 1:                # shared partial tail: copy on write
+                if not self.free:
+                    raise OutOfBlocks("no free block for copy-on-write")
+                b = self.free.pop()
+                self.ref[b] = 1
+                self.ref[tail] -= 1
+                t[L // self.block_size] = b
+                cow = (tail, b)
+        self.lens[seq] = L + 1
+        return self.slot(seq, L), cow
+
+    def free_seq(self, seq: int) -> None:
+        """Drop ``seq``'s references; blocks whose count reaches zero go back to
+        the free list, in the sequence's logical order."""
+        self._known(seq)
+        for b in self.tables[seq]:
+            if self.ref[b] < 1:
+                raise BlockManagerStateError(f"reference count of block {b} underflows")
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+        del self.tables[seq]
+        del self.lens[seq]
+
+    # -- helpers ---------------------------------------------------------
+    def padded_tables(self, seqs, width: int | None = None):
+        """int32 [len(seqs), width] tables padded with -1."""
+        import numpy as np
+        rows = [self.tables[s] for s in seqs]
+        w = max((len(r) for r in rows), default=0) if width is None else width
+        out = np.full((len(rows), max(w, 1)), -1, dtype=np.int32)
+        for i, r in enumerate(rows):
+            out[i, :len(r)] = r
+        return out
+
+    def _known(self, seq: int) -> None:
+        if seq not in self.tables:
+            raise BlockManagerStateError(f"unknown sequence {seq}")
