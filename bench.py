@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark: KV GB/s, fraction of HBM peak, decode tokens/s.
+
+Workload (default): the OPT-13B-shaped decode batch — 64 sequences, 40 heads
+(MHA), head_dim 128, block_size 16, fp16, lognormal context lengths (median
+600, sigma 0.8, clipped to [1, 2048], seed 0), block placement from a seeded
+permutation, pool sized 1.2x the demand. A step is one decode iteration of a
+40-layer model's attention: one batch append in the host block manager (new
+blocks / copy-on-write), the upload of slots, tables and lengths, then for
+every layer reshape_and_cache of the new token and paged decode attention over
+that layer's own pool. Every layer's pool is a separate 1.3 GB region, so each
+step reads ~42 GB of cache — far more than L2 (no flush needed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+on the host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s & fraction of GB300 HBM peak; decode tokens/s per config"
+FALLBACK_HBM_GBS = 6800.0
+CONFIGS = {
+    # name: (workload constructor kwargs, layers)
+    "opt13b": dict(layers=40),
+    "llama13b": dict(layers=40),
+    "longctx": dict(layers=8),
+}
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_src: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the kernel source as it is now (sha256 recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", "decode_partition_opt13b.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t:
+        return None
+    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(t.group(1)) if m.group(1) == cur else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = [r.split(", ") for r in open(self.path).read().strip().splitlines() if r]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": float(np.median(busy)) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def workload_shape(name, seed):
+    """Lengths and dimensions of a workload, without drawing its token data."""
+    import workloads as wl
+    if name == "opt13b":
+        return wl.opt13b_lengths(64, seed), 40, 40, 128, 16, "f16"
+    if name == "llama13b":
+        return wl.llama13b_lengths(128, seed), 40, 40, 128, 16, "f16"
+    if name == "longctx":
+        return np.array([n * 1024 for n in wl.LONGCTX_LENS_K], np.int32), 32, 8, 128, 16, "bf16"
+    raise ValueError(name)
+
+
+def make_workload(name, seed):
+    import workloads as wl
+    if name == "opt13b":
+        return wl.opt13b(seed)
+    if name == "llama13b":
+        return wl.llama13b(seed)
+    if name == "longctx":
+        return wl.longctx(seed)
+    raise ValueError(name)
+
+
+def decode_bytes(ctx, H, Hkv, D, out_bytes):
+    """Algorithmic bytes of one decode call: every cached key and value read
+    once, the queries read and the outputs written once."""
+    S = len(ctx)
+    return int(np.sum(ctx, dtype=np.int64)) * 2 * Hkv * D * 2 + S * H * D * 2 + S * H * D * out_bytes
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_118_gb300 as pk
+    import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    batch = make_workload(args.config, args.seed + rank)
+    S, H, Hkv, D, B = (batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_size,
+                       batch.block_size)
+    layers = args.layers or CONFIGS[args.config]["layers"]
+    tdt = torch.float16 if batch.dtype == "f16" else torch.bfloat16
+    pt = args.partition_tokens
+    total_steps = 2 * (args.warmup + args.steps) + 1
+    L0 = batch.context_lens.astype(np.int64)            # context at the first step
+    final = L0 + total_steps
+    demand = int(np.sum(-(-final // B)))
+    num_blocks = int(math.ceil(1.2 * demand))
+    width = int(np.max(-(-final // B)))
+    bm = pk.BlockManager(num_blocks, B, wl.free_order(num_blocks, args.seed + rank))
+    kc = torch.empty((layers, num_blocks, B, Hkv, D), dtype=tdt, device=dev)
+    vc = torch.empty_like(kc)
+
+    # prefill L-1 tokens of every sequence into every layer's pool
+    keep = np.ones(batch.total_tokens, bool)
+    keep[batch.offsets[1:] - 1] = False
+    slots = []
+    for s in range(S):
+        bm.allocate(s, int(L0[s]) - 1)
+        if L0[s] > 1:
+            slots.append(bm.slots(s))
+    d_slots = torch.from_numpy(np.concatenate(slots)).to(dev)
+    kp = torch.from_numpy(batch.k_tokens[keep].view(np.int16)).view(tdt).to(dev)
+    vp = torch.from_numpy(batch.v_tokens[keep].view(np.int16)).view(tdt).to(dev)
+    for l in range(layers):
+        pk.pkv_reshape_and_cache(kp, vp, kc[l], vc[l], d_slots)
+    del kp, vp, d_slots
+    torch.cuda.synchronize()
+
+    # per-layer step inputs (resident), and pinned host copies for the e2e run
+    qh = np.stack([wl.queries(S, H, D, batch.dtype, args.seed, l) for l in range(layers)])
+    nk, nv = zip(*[wl.new_tokens(S, Hkv, D, batch.dtype, args.seed, l) for l in range(layers)])
+    host = {n: torch.from_numpy(np.stack(a).view(np.int16) if n != "q" else a.view(np.int16))
+            .view(tdt).pin_memory() for n, a in (("q", qh), ("k", nk), ("v", nv))}
+    q = host["q"].to(dev)
+    knew, vnew = host["k"].to(dev), host["v"].to(dev)
+    out = torch.empty_like(q)
+    out_host = torch.empty(out.shape, dtype=tdt).pin_memory()
+    ws = pk.decode_workspace(S, H, D, width, B, pt, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    seq_ids = np.arange(S, dtype=np.int64)
+    d_tab = torch.empty((S, width), dtype=torch.int32, device=dev)
+    d_lens = torch.empty(S, dtype=torch.int32, device=dev)
+    d_new = torch.empty(S, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    launches = [0]
+    ctx_log = []
+    ev_pairs = []
+
+    def step(timed_kernels: bool):
+        new_slots, cow = bm.append_slots(seq_ids)                       # host block manager
+        tab, lens = bm.fill_tables(seq_ids, width)
+        d_new.copy_(torch.from_numpy(new_slots).pin_memory(), non_blocking=True)
+        d_tab.copy_(torch.from_numpy(tab).pin_memory(), non_blocking=True)
+        d_lens.copy_(torch.from_numpy(lens).pin_memory(), non_blocking=True)
+        ctx_log.append(lens.astype(np.int64))
+        for l in range(layers):
+            if len(cow):
+                pk.pkv_copy_blocks(kc[l], vc[l], cow)
+                launches[0] += -(-len(cow) // 1024)
+            pk.pkv_reshape_and_cache(knew[l], vnew[l], kc[l], vc[l], d_new, err)
+            if timed_kernels:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            pk.pkv_paged_attention_decode(out[l], q[l], kc[l], vc[l], d_tab, d_lens, B,
+                                          float(batch.scale), ws, pt, err)
+            if timed_kernels:
+                b.record(stream)
+                ev_pairs.append((a, b))
+            launches[0] += 3
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+
+    def barrier():
+        if dist:
+            td.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if not dist:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident run
+    for _ in range(args.warmup):
+        step(False)
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    ctx_log.clear()
+    ev_pairs.clear()
+    launches[0] = 0
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop() if rank == 0 else None
+    ms = max_over_ranks(t0.elapsed_time(t1))
+    out_bytes = 2
+    per_call = [decode_bytes(c, H, Hkv, D, out_bytes) for c in ctx_log]
+    step_bytes = sum(per_call) * layers
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    dec_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    achieved = (sum(per_call) * layers) / (sum(dec_ms) * 1e-3) / 1e9
+    n_launches = launches[0]
+    tokens_s = S * args.steps * world / (ms * 1e-3)
+    assert err.item() == 0, f"device error flag {err.item()}"
+
+    # ---- end-to-end: host inputs in, host outputs back, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(args.warmup):
+            step(False)
+        ctx_log.clear()
+        barrier()
+        w0 = time.perf_counter()
+        t0.record(stream)
+        for _ in range(args.steps):
+            q.copy_(host["q"], non_blocking=True)
+            knew.copy_(host["k"], non_blocking=True)
+            vnew.copy_(host["v"], non_blocking=True)
+            step(False)
+            out_host.copy_(out, non_blocking=True)
+        t1.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(max(t0.elapsed_time(t1), (time.perf_counter() - w0) * 1e3))
+        e_bytes = sum(decode_bytes(c, H, Hkv, D, out_bytes) for c in ctx_log) * layers
+        h2d = (q.numel() + knew.numel() + vnew.numel()) * 2 + S * (8 + 4 + 4 * width)
+        e2e = {"value": round(e_bytes * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2)}
+
+    peak, peak_kind = load_peaks()
+    src = os.path.join(ROOT, "paged_kv_cache_118_gb300", "csrc", "decode_attention.cu")
+    traffic = profile_traffic(src)
+    ctx_mean = float(np.mean([c.sum() for c in ctx_log])) if ctx_log else float(L0.sum())
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": batch.dtype, "data": "synthetic",
+        "config": {"workload": f"{args.config}_decode", "num_seqs": S, "num_heads": H,
+                   "num_kv_heads": Hkv, "head_size": D, "block_size": B, "layers": layers,
+                   "context_tokens_first_step": int(L0.sum()), "partition_tokens": pt or 512,
+                   "num_blocks": num_blocks, "seed": args.seed,
+                   "l2": "inputs larger than L2 (each step reads every layer's pool)"},
+        "decode_tokens_per_s": round(tokens_s, 1),
+        "frac_of_hbm_peak": round(value / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "paged decode attention (partition + reduce)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": traffic,
+                     "bytes_per_launch": int(np.mean(per_call)),
+                     "launch_us": round(1e3 * float(np.mean(dec_ms)), 2)},
+        "e2e": e2e, "gpu_launches": n_launches, "clocks": clk,
+    }
+    del kc, vc
+    return line
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+
+def _oracle_worker(args):
+    """Spawned process: build the oracle's state for a share of the sequences
+    (untimed), then time oracle decode steps (append + scatter + attention)
+    until the time budget is used."""
+    cfg, seed, seqs, budget_s, min_reps = args
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    sys.path.insert(0, ROOT)
+    import workloads as wl
+    from oracle.attention import paged_attention_decode
+    from oracle.cache_ops import reshape_and_cache
+    from oracle.pipeline import build_decode_state, pool_demand
+    all_lens, H, Hkv, D, B, dtype = workload_shape(cfg, seed)
+    lens = all_lens[seqs]
+    sub = wl.decode_batch("sample", lens, H, Hkv, D, B, dtype, seed + 1000 * seqs[0],
+                          outlier_frac=0.01 if cfg == "longctx" else 0.0)
+    n = pool_demand(lens + 64, sub.block_size) + 8
+    st = build_decode_state(sub, n, wl.free_order(n, seed), wl.poison_bits(sub.dtype))
+    bm, kc, vc = st["bm"], st["k_cache"], st["v_cache"]
+    nk, nv = wl.new_tokens(len(seqs), sub.num_kv_heads, sub.head_size, sub.dtype, seed, 0)
+    done_bytes, reps, t0 = 0, 0, time.perf_counter()
+    while reps < min_reps or time.perf_counter() - t0 < budget_s:
+        new_slots = np.array([bm.append_slot(s)[0] for s in range(len(seqs))], np.int64)
+        reshape_and_cache(nk, nv, kc, vc, new_slots)
+        ctx = np.array([bm.length(s) for s in range(len(seqs))], np.int64)
+        tables = bm.padded_tables(range(len(seqs)))
+        paged_attention_decode(sub.q, kc, vc, tables, ctx, sub.block_size, sub.scale, sub.dtype)
+        done_bytes += decode_bytes(ctx, sub.num_heads, sub.num_kv_heads, sub.head_size, 2)
+        reps += 1
+    return done_bytes, time.perf_counter() - t0, reps
+
+
+def oracle_throughput(cfg, seed, budget_s, min_reps=1):
+    """Oracle GB/s on all host cores: the batch's sequences dealt round-robin
+    to one spawned worker per core; each times whole oracle decode steps of
+    its share for about ``budget_s`` seconds."""
+    n_seqs = len(workload_shape(cfg, seed)[0])
+    cores = os.cpu_count() or 1
+    workers = min(cores, n_seqs)
+    shares = [list(range(w, n_seqs, workers)) for w in range(workers)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        res = pool.map(_oracle_worker, [(cfg, seed, s, budget_s, min_reps) for s in shares])
+    total = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    reps = min(r[2] for r in res)
+    return total / wall / 1e9, workers, reps, wall
+
+
+def run_reference(args, rank):
+    """The oracle as it stands, timed on the host cores: each step is one
+    bounded sample — a single layer's decode step of the whole batch."""
+    gbs, cores, reps, wall = oracle_throughput(args.config, args.seed, budget_s=0.0,
+                                               min_reps=args.warmup + args.steps)
+    sample = (f"{args.config} batch, one layer per step, {reps} oracle decode steps "
+              f"(append + reshape_and_cache + fp64 attention) over {cores} spawn workers")
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * wall / max(reps, 1), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.config}_decode", "seed": args.seed},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="opt13b")
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank)), flush=True)
+        return
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # before the first GPU call: the oracle pool is spawned, not forked
+        gbs, cores, reps, wall = oracle_throughput(args.config, args.seed, args.cpu_budget)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{args.config} batch, one layer, {reps}+ oracle decode steps per "
+                         f"worker (append + reshape_and_cache + fp64 attention), "
+                         f"{wall:.1f} s on {cores} spawn workers"}
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        torch.cuda.set_device(local_rank)
+        td.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as td
+        td.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * pagedkv — paged KV-cache decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libpagedkv.so. Plain pointers and sizes only; no CUDA or framework
+ * types appear in the signatures. A CUDA stream is passed as `void*`
+ * (a cudaStream_t; NULL is the legacy default stream).
+ *
+ * Sources of the operations (web pages on vLLM's PagedAttention):
+ *  [R]  "079｜vLLM 与 PagedAttention：不改变模型，也能让更多请求同时运行",
+ *       wq-win.github.io — review of Kwon et al., SOSP 2023.
+ *  [G]  "vLLM 推理引擎：PagedAttention 与 KVCache 管理", gitcode.csdn.net.
+ *  [D]  "PagedAttention 内存管理深度解析", deepinsea.top.
+ *
+ * Conventions shared by every call:
+ *  - dtype codes: PKV_F16 = IEEE binary16, PKV_BF16 = bfloat16, PKV_F32 = binary32.
+ *  - KV cache layout ([G] §3, PagedAttention.forward comments):
+ *        k_cache, v_cache: [num_blocks][block_size][num_kv_heads][head_size]
+ *    a "slot" is block * block_size + row; row-major, contiguous.
+ *  - Device buffers are owned by the caller and must stay valid until the work
+ *    queued on `stream` has finished. The library allocates no device memory;
+ *    the decode call takes a caller-provided workspace.
+ *  - Host-side validation is synchronous and happens before anything is queued:
+ *    on an error status nothing was launched and nothing was written.
+ *  - Device-side checks: a kernel that finds an out-of-range index in device
+ *    data skips the access and ORs a PKV_DEVERR_* bit into *err_flag (a device
+ *    int32 the caller zeroes and reads; may be NULL). Kernels never trap.
+ *  - All GPU calls are asynchronous with respect to the host.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_EINVAL = 1,     /* null pointer, bad shape, unsupported size or dtype, misaligned pointer */
+  PKV_ENOMEM = 2,     /* block manager: too few free blocks; nothing was changed */
+  PKV_ERANGE = 3,     /* host-visible index out of range (block id, copy pair) */
+  PKV_ECUDA = 4,      /* a CUDA runtime or launch error */
+  PKV_ESTATE = 5,     /* block manager: unknown or duplicate sequence id, reference-count underflow */
+  PKV_EWORKSPACE = 6  /* decode workspace smaller than pkv_decode_workspace_size() */
+} pkv_status;
+
+enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 };
+
+/* Bits a kernel ORs into *err_flag. */
+#define PKV_DEVERR_BLOCK_ID 0x1 /* block-table entry outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT 0x2  /* context length outside [1, max_blocks_per_seq * block_size] */
+#define PKV_DEVERR_SLOT 0x4     /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_TIMEOUT 0x8  /* a pipeline wait gave up (the kernel returned early) */
+
+/* Human-readable name of a status code; never NULL. */
+const char* pkv_status_string(int status);
+/* Library version string. */
+const char* pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Decode attention over the paged cache.
+ *
+ * Defines ([R] §2 "分块以后，注意力仍需对整个历史归一化"): for each sequence s
+ * and query head h, with L = context_lens[s] tokens stored in the blocks
+ * block_tables[s][0 .. ceil(L/B)-1] in position order,
+ *     o[s][h] = sum_u exp(scale * q.k_u) v_u / sum_u exp(scale * q.k_u)
+ * over all L positions u — one softmax denominator for the whole history, the
+ * unfilled rows of the last block excluded. Query head h reads KV head
+ * h / (num_heads / num_kv_heads).
+ *
+ * The context is processed in partitions of `partition_tokens` tokens (0 picks
+ * 512; otherwise a positive multiple of 32, at most 4096): one CTA per
+ * (sequence, KV head, partition) produces an unnormalised partial, and a second
+ * kernel merges the partials of each (sequence, head) with the global
+ * denominator.
+ *
+ *   out          device, [num_seqs][num_heads][head_size] of out_dtype (F16, BF16 or F32)
+ *   q            device, [num_seqs][num_heads][head_size] of kv_dtype
+ *   k_cache,
+ *   v_cache      device, [num_blocks][block_size][num_kv_heads][head_size] of kv_dtype
+ *   kv_dtype     PKV_F16 or PKV_BF16
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                ceil(L/B) are never read (pad with -1)
+ *   context_lens device int32 [num_seqs]; 1 <= L <= max_blocks_per_seq * block_size
+ *                (the newest token counts)
+ *   head_size    64 or 128; num_heads a multiple of num_kv_heads
+ *   block_size   8, 16, 32, 64 or 128
+ *   scale        multiplies q.k (typically 1/sqrt(head_size))
+ *   workspace    device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned;
+ *                scratch owned by the caller, contents on entry irrelevant
+ *   err_flag     device int32 or NULL (see PKV_DEVERR_*); a sequence whose length
+ *                is out of range gets an all-zero output row
+ * q, out, k_cache and v_cache must be 16-byte aligned.
+ * Errors: PKV_EINVAL (shape/dtype/alignment), PKV_EWORKSPACE, PKV_ECUDA.
+ * ------------------------------------------------------------------------ */
+size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_size,
+                                 int max_blocks_per_seq, int block_size, int partition_tokens);
+
+pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
+                                      const void* k_cache, const void* v_cache, int kv_dtype,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                      int num_blocks, int block_size, int max_blocks_per_seq,
+                                      float scale, int partition_tokens, void* workspace,
+                                      size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/* ------------------------------------------------------------------------
+ * reshape_and_cache: write new tokens' keys and values into their slots.
+ *
+ * Defines ([R] §2 "共享与写时复制" and the §3 per-iteration algorithm box: the
+ * new token goes into the sequence's tail block): for every token t with
+ * slot = slot_mapping[t] >= 0,
+ *     k_cache[slot / B][slot % B][h][:] = k[t][h][:]   (same for v), bitwise.
+ * A negative slot means "skip". A slot >= num_blocks * B is skipped and sets
+ * PKV_DEVERR_SLOT.
+ *
+ *   k, v          device, [num_tokens][num_kv_heads][head_size] of dtype
+ *   k_cache, ...  device, layout above
+ *   slot_mapping  device int64 [num_tokens]
+ *   dtype         PKV_F16 or PKV_BF16; head_size * 2 a multiple of 16
+ * All four data pointers 16-byte aligned. num_tokens == 0 is a no-op.
+ * Two tokens with the same slot race (one of them wins).
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                 int head_size, int num_blocks, int block_size, int dtype,
+                                 int32_t* err_flag, void* stream);
+
+/* ------------------------------------------------------------------------
+ * copy_blocks: copy-on-write block copies.
+ *
+ * Defines ([R] §2 "共享与写时复制" and "一次分叉什么时候真的要复制缓存块"):
+ * before a branch writes into a block another branch still references, the
+ * block is copied and only this branch is remapped. For every pair i,
+ *     K[dst_i] = K[src_i], V[dst_i] = V[src_i]      (block_bytes bytes each).
+ *
+ *   src_dst_pairs  HOST int32 [num_pairs][2] = {src, dst}; read before the call
+ *                  returns (the ids travel in the kernel's parameters, so the
+ *                  host buffer may be reused at once)
+ *   block_bytes    bytes of one block of one cache:
+ *                  block_size * num_kv_heads * head_size * element size;
+ *                  a multiple of 16; caches 16-byte aligned
+ * Ids must lie in [0, num_blocks) (else PKV_ERANGE); destinations must be
+ * distinct and no destination may also be a source (else PKV_EINVAL).
+ * num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
+                           int num_pairs, int num_blocks, size_t block_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host block manager: free list, reference counts, fork, copy-on-write.
+ *
+ * Defines: [D] "分页机制设计" (a free list of block ids; a request takes
+ * ceil(n/B) blocks popped from the end of the list and fails with no side
+ * effect when too few are free; released blocks are appended back) and [R] §2
+ * "共享与写时复制" (per-block reference counts; a fork shares every block; a
+ * block is reclaimed only when its count reaches zero; writing into a tail
+ * block still shared copies it first), [R] §2 "一次分叉什么时候真的要复制缓存块"
+ * (full blocks are never copied) and the §3 algorithm box (check whether the
+ * next token needs a new block; copy-on-write a shared tail).
+ *
+ * The handle is owned by the library: create with pkv_bm_create, release with
+ * pkv_bm_destroy. Not thread-safe: one thread at a time per handle.
+ * Sequence ids are arbitrary int64 keys chosen by the caller.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_bm pkv_bm;
+
+/* free_order: NULL, or a permutation of 0..num_blocks-1 that becomes the
+ * initial free list (blocks are handed out from its end). NULL means the list
+ * 0, 1, ..., num_blocks-1. Returns NULL on bad arguments. */
+pkv_bm* pkv_bm_create(int num_blocks, int block_size, const int32_t* free_order);
+void pkv_bm_destroy(pkv_bm* bm);
+
+/* A new sequence holding num_tokens >= 0 tokens (ceil(n/B) blocks, count 1).
+ * PKV_ESTATE if seq exists; PKV_ENOMEM (no change) if too few blocks are free. */
+pkv_status pkv_bm_allocate(pkv_bm* bm, int64_t seq, int64_t num_tokens);
+/* child shares all of parent's blocks (each count + 1) and its length. */
+pkv_status pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child);
+/* Room for one more token of seq. *slot receives its slot. If the tail block
+ * was shared, a fresh block replaces it in seq's table and (*cow_src, *cow_dst)
+ * receive the pair to copy before writing; otherwise both are set to -1.
+ * PKV_ENOMEM (no change) when a block is needed and none is free. */
+pkv_status pkv_bm_append_slot(pkv_bm* bm, int64_t seq, int64_t* slot, int32_t* cow_src,
+                              int32_t* cow_dst);
+/* append_slot for n sequences in order, all or nothing: on PKV_ENOMEM /
+ * PKV_ESTATE nothing changed. slots: int64 [n]; cow_pairs: int32 [n][2] (room
+ * for n pairs); *num_cow receives the number of pairs written. */
+pkv_status pkv_bm_append_slots(pkv_bm* bm, const int64_t* seqs, int n, int64_t* slots,
+                               int32_t* cow_pairs, int* num_cow);
+/* Drop seq; blocks whose count reaches zero return to the free list in the
+ * sequence's logical order. */
+pkv_status pkv_bm_free(pkv_bm* bm, int64_t seq);
+
+/* Queries. */
+int pkv_bm_num_free(const pkv_bm* bm);
+int pkv_bm_refcount(const pkv_bm* bm, int32_t block); /* -1 if out of range */
+int64_t pkv_bm_length(const pkv_bm* bm, int64_t seq); /* -1 if unknown */
+/* seq's table into out[0..cap); *n receives its length (PKV_ERANGE if > cap). */
+pkv_status pkv_bm_block_table(const pkv_bm* bm, int64_t seq, int32_t* out, int cap, int* n);
+/* Tables of n sequences into out[n][width], padded with -1, and their lengths
+ * into context_lens[n] (may be NULL). PKV_ERANGE if a table is wider. */
+pkv_status pkv_bm_fill_tables(const pkv_bm* bm, const int64_t* seqs, int n, int32_t* out,
+                              int width, int32_t* context_lens);
+/* Slots of positions first .. first+count-1 of seq into out[count]. */
+pkv_status pkv_bm_slots(const pkv_bm* bm, int64_t seq, int64_t first, int64_t count,
+                        int64_t* out);
+/* The free list, bottom to top (the next block handed out is the last one);
+ * returns its length, writes at most cap entries. */
+int pkv_bm_free_list(const pkv_bm* bm, int32_t* out, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,262 @@
+"""pagedkv — paged KV-cache decode attention on GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libpagedkv.so`` (declared in
+``include/pagedkv.h``). The functions here keep the C names and only marshal
+arguments: torch tensors become device pointers and sizes, the current torch
+stream becomes the CUDA stream. Every step of the computation runs in the
+library's CUDA kernels (or, for the block manager, its C++ host code).
+
+Importing this package loads the library and raises if it has not been built
+(``python -m paged_kv_cache_118_gb300.build``); there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+PKV_OK, PKV_EINVAL, PKV_ENOMEM, PKV_ERANGE, PKV_ECUDA, PKV_ESTATE, PKV_EWORKSPACE = range(7)
+PKV_F16, PKV_BF16, PKV_F32 = 0, 1, 2
+PKV_DEVERR_BLOCK_ID, PKV_DEVERR_CONTEXT, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_DTYPE = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32}
+
+_c_int, _c_i64, _c_sz, _c_f, _vp = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                                     ctypes.c_float, ctypes.c_void_p)
+
+# name -> (restype, argtypes); the exported symbols of include/pagedkv.h
+SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [_c_int]),
+    "pkv_version": (ctypes.c_char_p, []),
+    "pkv_decode_workspace_size": (_c_sz, [_c_int] * 6),
+    "pkv_paged_attention_decode": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
+                                            _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                            _c_int, _c_f, _c_int, _vp, _c_sz, _vp, _vp]),
+    "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _vp, _vp]),
+    "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_sz, _vp]),
+    "pkv_bm_create": (_vp, [_c_int, _c_int, _vp]),
+    "pkv_bm_destroy": (None, [_vp]),
+    "pkv_bm_allocate": (_c_int, [_vp, _c_i64, _c_i64]),
+    "pkv_bm_fork": (_c_int, [_vp, _c_i64, _c_i64]),
+    "pkv_bm_append_slot": (_c_int, [_vp, _c_i64, _vp, _vp, _vp]),
+    "pkv_bm_append_slots": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp]),
+    "pkv_bm_free": (_c_int, [_vp, _c_i64]),
+    "pkv_bm_num_free": (_c_int, [_vp]),
+    "pkv_bm_refcount": (_c_int, [_vp, ctypes.c_int32]),
+    "pkv_bm_length": (_c_i64, [_vp, _c_i64]),
+    "pkv_bm_block_table": (_c_int, [_vp, _c_i64, _vp, _c_int, _vp]),
+    "pkv_bm_fill_tables": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _vp]),
+    "pkv_bm_slots": (_c_int, [_vp, _c_i64, _c_i64, _c_i64, _vp]),
+    "pkv_bm_free_list": (_c_int, [_vp, _vp, _c_int]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m paged_kv_cache_118_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.pkv_status_string(status).decode()} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != PKV_OK:
+        raise PagedKVError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("pagedkv kernels take CUDA tensors")
+
+
+# ---------------------------------------------------------------- kernels
+
+def pkv_decode_workspace_size(num_seqs: int, num_heads: int, head_size: int,
+                              max_blocks_per_seq: int, block_size: int,
+                              partition_tokens: int = 0) -> int:
+    return int(lib.pkv_decode_workspace_size(num_seqs, num_heads, head_size,
+                                             max_blocks_per_seq, block_size, partition_tokens))
+
+
+def decode_workspace(num_seqs, num_heads, head_size, max_blocks_per_seq, block_size,
+                     partition_tokens=0, device="cuda") -> torch.Tensor:
+    """A caller-owned scratch buffer of the size the decode call needs."""
+    n = pkv_decode_workspace_size(num_seqs, num_heads, head_size, max_blocks_per_seq,
+                                  block_size, partition_tokens)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def pkv_paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                               v_cache: torch.Tensor, block_tables: torch.Tensor,
+                               context_lens: torch.Tensor, block_size: int, scale: float,
+                               workspace: torch.Tensor, partition_tokens: int = 0,
+                               err_flag: torch.Tensor | None = None, stream=None) -> None:
+    """out[s, h] = softmax attention of q[s, h] over sequence s's paged history.
+
+    q, out: [num_seqs, num_heads, head_size]; caches: [num_blocks, block_size,
+    num_kv_heads, head_size]; block_tables: int32 [num_seqs, max_blocks_per_seq];
+    context_lens: int32 [num_seqs]; workspace: bytes from decode_workspace().
+    """
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, err_flag)
+    S, H, D = q.shape
+    nb, B, Hkv, D2 = k_cache.shape
+    st = lib.pkv_paged_attention_decode(
+        _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
+        _ptr(block_tables), _ptr(context_lens), S, H, Hkv, D, nb, block_size,
+        block_tables.shape[1], float(scale), partition_tokens, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream))
+    _check(st, "pkv_paged_attention_decode")
+
+
+def pkv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          err_flag: torch.Tensor | None = None, stream=None) -> None:
+    """k_cache[slot // B, slot % B] = k[t] (and v) for every token t with slot >= 0."""
+    _need_cuda(k, v, k_cache, v_cache, slot_mapping, err_flag)
+    T, Hkv, D = k.shape
+    nb, B = k_cache.shape[:2]
+    st = lib.pkv_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(slot_mapping), T, Hkv, D, nb, B, _DTYPE[k.dtype],
+                                   _ptr(err_flag), _stream(stream))
+    _check(st, "pkv_reshape_and_cache")
+
+
+def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
+                    stream=None) -> None:
+    """Copy-on-write: block dst of both caches becomes a copy of block src.
+
+    src_dst_pairs: host int32 array-like [n, 2]."""
+    import numpy as np
+    _need_cuda(k_cache, v_cache)
+    pairs = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int32).reshape(-1, 2))
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    st = lib.pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), pairs.ctypes.data, pairs.shape[0],
+                             k_cache.shape[0], block_bytes, _stream(stream))
+    _check(st, "pkv_copy_blocks")
+
+
+# ---------------------------------------------------------------- block manager
+
+class BlockManager:
+    """Handle on the library's host block manager (pkv_bm_*)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        import numpy as np
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must hold num_blocks ids")
+        self._h = lib.pkv_bm_create(num_blocks, block_size,
+                                    None if order is None else order.ctypes.data)
+        if not self._h:
+            raise PagedKVError(PKV_EINVAL, "pkv_bm_create")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib.pkv_bm_destroy(h)
+            self._h = None
+
+    def allocate(self, seq: int, num_tokens: int) -> None:
+        _check(lib.pkv_bm_allocate(self._h, seq, num_tokens), "pkv_bm_allocate")
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(lib.pkv_bm_fork(self._h, parent, child), "pkv_bm_fork")
+
+    def append_slot(self, seq: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib.pkv_bm_append_slot(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                      ctypes.byref(dst)), "pkv_bm_append_slot")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def append_slots(self, seqs):
+        """Batch append (all or nothing): returns (slots int64 [n], cow int32 [k, 2])."""
+        import numpy as np
+        seqs = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        n = seqs.shape[0]
+        slots = np.empty(n, np.int64)
+        cow = np.empty((max(n, 1), 2), np.int32)
+        k = ctypes.c_int()
+        _check(lib.pkv_bm_append_slots(self._h, seqs.ctypes.data, n, slots.ctypes.data,
+                                       cow.ctypes.data, ctypes.byref(k)), "pkv_bm_append_slots")
+        return slots, cow[:k.value]
+
+    def free_seq(self, seq: int) -> None:
+        _check(lib.pkv_bm_free(self._h, seq), "pkv_bm_free")
+
+    def num_free(self) -> int:
+        return int(lib.pkv_bm_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(lib.pkv_bm_refcount(self._h, block))
+
+    def length(self, seq: int) -> int:
+        return int(lib.pkv_bm_length(self._h, seq))
+
+    def table(self, seq: int):
+        import numpy as np
+        n = ctypes.c_int()
+        lib.pkv_bm_block_table(self._h, seq, None, 0, ctypes.byref(n))
+        out = np.empty(max(n.value, 1), np.int32)
+        _check(lib.pkv_bm_block_table(self._h, seq, out.ctypes.data, out.shape[0],
+                                      ctypes.byref(n)), "pkv_bm_block_table")
+        return out[:n.value]
+
+    def fill_tables(self, seqs, width: int):
+        """(tables int32 [n, width] padded with -1, context_lens int32 [n])."""
+        import numpy as np
+        seqs = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        n = seqs.shape[0]
+        out = np.empty((n, width), np.int32)
+        lens = np.empty(n, np.int32)
+        _check(lib.pkv_bm_fill_tables(self._h, seqs.ctypes.data, n, out.ctypes.data, width,
+                                      lens.ctypes.data), "pkv_bm_fill_tables")
+        return out, lens
+
+    def slots(self, seq: int, first: int = 0, count: int | None = None):
+        import numpy as np
+        if count is None:
+            count = self.length(seq) - first
+        out = np.empty(max(count, 1), np.int64)
+        _check(lib.pkv_bm_slots(self._h, seq, first, count, out.ctypes.data), "pkv_bm_slots")
+        return out[:count]
+
+    def free_list(self):
+        import numpy as np
+        n = lib.pkv_bm_free_list(self._h, None, 0)
+        out = np.empty(max(n, 1), np.int32)
+        lib.pkv_bm_free_list(self._h, out.ctypes.data, n)
+        return out[:n]

@@ -1,0 +1,61 @@
+"""Shared pieces of the GPU parity tests: moving the generator's bit patterns
+to the device, running a decode step through the library, and the tolerance.
+
+Tolerance (attention outputs): the kernels accumulate in fp32; the stated
+bound is a max-abs error of 2e-3 (fp16) / 8e-3 (bf16) against the fp64
+oracle. An fp32 output is held to that bound as it is. An output rounded to
+fp16/bf16 also carries the rounding of the result itself, up to half an ulp
+of the format at the value's magnitude, which for bf16 outputs above 2 alone
+exceeds 8e-3; so those are held to bound + half an ulp of |oracle|.
+"""
+
+import numpy as np
+import torch
+
+from paged_kv_cache_118_gb300.cache import PagedKVCache
+
+TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
+BOUND = {"f16": 2e-3, "bf16": 8e-3}
+MANT = {torch.float16: (10, -14), torch.bfloat16: (7, -126)}
+
+
+def dev(bits: np.ndarray, dtype: str) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        TORCH_DTYPE[dtype]).cuda()
+
+
+def half_ulp(x: np.ndarray, tdtype) -> np.ndarray:
+    mant, emin = MANT[tdtype]
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** emin)))
+    return 0.5 * np.exp2(e - mant)
+
+
+def assert_close(gpu: torch.Tensor, ref: np.ndarray, dtype: str):
+    """Element-wise check of a GPU attention output against the oracle."""
+    got = gpu.float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape
+    mask = ~np.isnan(ref)
+    assert np.all(np.isfinite(got[mask])), "non-finite output"
+    err = np.abs(got - ref)[mask]
+    tol = BOUND[dtype] + (0.0 if gpu.dtype == torch.float32 else half_ulp(ref, gpu.dtype)[mask])
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} elements off, max err {err.max():.3e}"
+    return float(err.max()) if err.size else 0.0
+
+
+def gpu_decode_state(batch, num_blocks, order, poison=True):
+    """Prefill L-1 tokens per sequence, append the newest token of each, build
+    the device tables — all through the library (block manager + kernels)."""
+    cache = PagedKVCache(num_blocks, batch.block_size, batch.num_kv_heads, batch.head_size,
+                         TORCH_DTYPE[batch.dtype], free_order=order, poison=poison)
+    S = batch.num_seqs
+    lens = batch.context_lens.astype(np.int64)
+    last = batch.offsets[1:] - 1
+    keep = np.ones(batch.total_tokens, bool)
+    keep[last] = False
+    cache.prefill(range(S), lens - 1, dev(batch.k_tokens[keep], batch.dtype),
+                  dev(batch.v_tokens[keep], batch.dtype))
+    cache.append(list(range(S)), dev(batch.k_tokens[last], batch.dtype),
+                 dev(batch.v_tokens[last], batch.dtype))
+    tables, ctx = cache.tables(range(S))
+    return cache, tables, ctx

@@ -1,0 +1,91 @@
+"""The C ABI: libpagedkv.so loads, exports every function include/pagedkv.h
+declares, and refuses bad arguments on the host before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_118_gb300 as pk
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pagedkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 20
+    raw = ctypes.CDLL(pk.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) == set(pk.SIGNATURES), set(names) ^ set(pk.SIGNATURES)
+
+
+def test_status_strings_and_version():
+    for s in range(7):
+        assert pk.lib.pkv_status_string(s)
+    assert b"unknown" in pk.lib.pkv_status_string(99)
+    assert b"sm_103a" in pk.lib.pkv_version()
+
+
+def test_workspace_size_formula():
+    # rows = S * H * ceil(max_blocks * B / partition); each row holds D floats + (m, l)
+    for S, H, D, mb, B, pt in [(64, 40, 128, 128, 16, 512), (8, 32, 128, 8192, 16, 512),
+                               (3, 4, 64, 5, 4, 32), (1, 1, 64, 1, 8, 0)]:
+        parts = -(-(mb * B) // (pt or 512))
+        rows = S * H * parts
+        assert pk.pkv_decode_workspace_size(S, H, D, mb, B, pt) == rows * D * 4 + rows * 8 + 16
+
+
+def _decode_status(**over):
+    a = dict(out=16, out_dtype=0, q=16, k=16, v=16, kv_dtype=0, bt=16, cl=16, S=2, H=4, Hkv=4,
+             D=64, nb=8, B=16, mb=4, scale=0.125, pt=0, ws=16, wsb=1 << 20, err=None)
+    a.update(over)
+    return pk.lib.pkv_paged_attention_decode(a["out"], a["out_dtype"], a["q"], a["k"], a["v"],
+                                             a["kv_dtype"], a["bt"], a["cl"], a["S"], a["H"],
+                                             a["Hkv"], a["D"], a["nb"], a["B"], a["mb"],
+                                             a["scale"], a["pt"], a["ws"], a["wsb"], a["err"],
+                                             None)
+
+
+@pytest.mark.parametrize("over", [
+    dict(q=None), dict(out=None), dict(ws=None), dict(kv_dtype=2), dict(out_dtype=7),
+    dict(D=96), dict(D=256), dict(H=6, Hkv=4), dict(B=12), dict(B=256), dict(pt=48),
+    dict(pt=8192), dict(S=-1), dict(nb=0), dict(mb=0), dict(q=24), dict(k=8),
+    dict(scale=float("nan")), dict(S=70000)])
+def test_decode_rejects_bad_arguments_on_host(over):
+    assert _decode_status(**over) == pk.PKV_EINVAL
+
+
+def test_decode_rejects_small_workspace_and_accepts_empty_batch():
+    assert _decode_status(wsb=100) == pk.PKV_EWORKSPACE
+    assert _decode_status(S=0, q=None) == pk.PKV_OK
+
+
+def test_copy_blocks_host_validation():
+    import numpy as np
+    def st(pairs, nb=10, bb=4096, k=16, v=16):
+        p = np.asarray(pairs, np.int32).reshape(-1, 2)
+        return pk.lib.pkv_copy_blocks(k, v, p.ctypes.data, p.shape[0], nb, bb, None)
+    assert st([(1, 10)]) == pk.PKV_ERANGE
+    assert st([(-1, 2)]) == pk.PKV_ERANGE
+    assert st([(1, 2), (3, 2)]) == pk.PKV_EINVAL      # duplicate destination
+    assert st([(1, 2), (2, 3)]) == pk.PKV_EINVAL      # a destination is also a source
+    assert st([(1, 2)], bb=100) == pk.PKV_EINVAL
+    assert st([(1, 2)], k=8) == pk.PKV_EINVAL
+    assert pk.lib.pkv_copy_blocks(16, 16, None, 0, 10, 4096, None) == pk.PKV_OK
+
+
+def test_reshape_and_cache_host_validation():
+    f = pk.lib.pkv_reshape_and_cache
+    assert f(16, 16, 16, 16, 16, 0, 4, 64, 8, 16, 0, None, None) == pk.PKV_OK
+    assert f(16, 16, 16, 16, None, 3, 4, 64, 8, 16, 0, None, None) == pk.PKV_EINVAL
+    assert f(16, 16, 16, 16, 16, 3, 4, 60, 8, 16, 0, None, None) == pk.PKV_EINVAL
+    assert f(16, 16, 16, 16, 16, 3, 4, 64, 8, 16, 2, None, None) == pk.PKV_EINVAL
+    assert f(16, 24, 16, 16, 16, 3, 4, 64, 8, 16, 0, None, None) == pk.PKV_EINVAL

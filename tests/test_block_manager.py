@@ -1,0 +1,122 @@
+"""The library's C++ block manager against the oracle's Python one: identical
+tables, slots, copy-on-write pairs, reference counts and free lists for the
+same operation sequence, bit for bit; and its own error behaviour."""
+
+import random
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_118_gb300 as pk
+from oracle.block_manager import BlockManager as RefBM
+from oracle.block_manager import BlockManagerStateError, OutOfBlocks
+from workloads import free_order, gqa_prefix
+
+
+def same_state(bm, ref, live):
+    assert bm.num_free() == ref.num_free()
+    assert list(bm.free_list()) == ref.free
+    for b in range(ref.num_blocks):
+        assert bm.refcount(b) == ref.ref[b]
+    for s in live:
+        assert list(bm.table(s)) == ref.table(s)
+        assert bm.length(s) == ref.length(s)
+        assert list(bm.slots(s)) == ref.slots(s)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_operations_match_oracle(seed):
+    rng = random.Random(seed)
+    N, B = rng.randint(4, 80), rng.choice([1, 2, 4, 8, 16, 32])
+    order = free_order(N, seed)
+    bm, ref = pk.BlockManager(N, B, order), RefBM(N, B, order)
+    live, nxt = [], 0
+    for _ in range(400):
+        op = rng.random()
+        if op < 0.25 or not live:
+            n = rng.randint(0, 3 * B)
+            try:
+                ref.allocate(nxt, n)
+                ok = True
+            except OutOfBlocks:
+                ok = False
+            if ok:
+                bm.allocate(nxt, n)
+                live.append(nxt)
+            else:
+                with pytest.raises(pk.PagedKVError) as e:
+                    bm.allocate(nxt, n)
+                assert e.value.status == pk.PKV_ENOMEM
+            nxt += 1
+        elif op < 0.4:
+            p = rng.choice(live)
+            ref.fork(p, nxt); bm.fork(p, nxt); live.append(nxt); nxt += 1
+        elif op < 0.7:
+            s = rng.choice(live)
+            try:
+                want = ref.append_slot(s)
+            except OutOfBlocks:
+                with pytest.raises(pk.PagedKVError) as e:
+                    bm.append_slot(s)
+                assert e.value.status == pk.PKV_ENOMEM
+            else:
+                assert bm.append_slot(s) == want
+        elif op < 0.85:
+            batch = [rng.choice(live) for _ in range(rng.randint(1, 6))]
+            snap = (list(ref.free), list(ref.ref), {k: list(v) for k, v in ref.tables.items()},
+                    dict(ref.lens))
+            try:
+                want = [ref.append_slot(s) for s in batch]
+            except OutOfBlocks:
+                ref.free, ref.ref, ref.tables, ref.lens = snap   # all or nothing
+                with pytest.raises(pk.PagedKVError) as e:
+                    bm.append_slots(batch)
+                assert e.value.status == pk.PKV_ENOMEM
+            else:
+                slots, cow = bm.append_slots(batch)
+                assert list(slots) == [w[0] for w in want]
+                assert [tuple(c) for c in cow] == [w[1] for w in want if w[1] is not None]
+        else:
+            s = rng.choice(live)
+            ref.free_seq(s); bm.free_seq(s); live.remove(s)
+        same_state(bm, ref, live)
+
+
+def test_beam_groups_match_oracle_and_copy_three_of_four():
+    pb = gqa_prefix(seed=1, groups=5, beams=4, prefix_tokens=48, max_tail=20)
+    N = 120
+    order = free_order(N, 4)
+    bm, ref = pk.BlockManager(N, 16, order), RefBM(N, 16, order)
+    for g in range(pb.num_groups):
+        for m in (bm, ref):
+            m.allocate(4 * g, int(pb.prefix_lens[g]))
+            for b in range(1, 4):
+                m.fork(4 * g, 4 * g + b)
+    seqs = list(range(pb.num_seqs))
+    slots, cow = bm.append_slots(seqs)
+    want = [ref.append_slot(s) for s in seqs]
+    assert list(slots) == [w[0] for w in want]
+    assert len(cow) == 3 * pb.num_groups
+    same_state(bm, ref, seqs)
+
+
+def test_error_statuses():
+    bm = pk.BlockManager(4, 4)
+    bm.allocate(1, 5)
+    for fn, args, status in [(bm.allocate, (1, 1), pk.PKV_ESTATE),
+                             (bm.allocate, (2, 9), pk.PKV_ENOMEM),
+                             (bm.fork, (7, 8), pk.PKV_ESTATE),
+                             (bm.fork, (1, 1), pk.PKV_ESTATE),
+                             (bm.append_slot, (9,), pk.PKV_ESTATE),
+                             (bm.free_seq, (9,), pk.PKV_ESTATE)]:
+        with pytest.raises(pk.PagedKVError) as e:
+            fn(*args)
+        assert e.value.status == status
+    assert bm.length(9) == -1 and bm.refcount(99) == -1
+    with pytest.raises(pk.PagedKVError):
+        pk.BlockManager(4, 4, free_order=[0, 1, 1, 2])
+    tabs, lens = bm.fill_tables([1], 4)
+    assert list(tabs[0]) == [3, 2, -1, -1] and list(lens) == [5]
+    with pytest.raises(pk.PagedKVError) as e:
+        bm.fill_tables([1], 1)
+    assert e.value.status == pk.PKV_ERANGE

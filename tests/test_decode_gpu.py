@@ -1,0 +1,207 @@
+"""GPU parity: the library's kernels against the fp64 oracle, element by
+element, on seeded inputs that span several tiles, partitions and ragged
+tails; invariances that must hold bitwise; device-side error reporting."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_118_gb300 as pk
+from oracle.attention import paged_attention_decode as oracle_decode
+from oracle.cache_ops import copy_blocks as oracle_copy
+from oracle.pipeline import build_decode_state, build_shared_prefix_state, pool_demand
+from parity import TORCH_DTYPE, assert_close, dev, gpu_decode_state
+from workloads import decode_batch, free_order, gqa_prefix, poison_bits, tiny
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(batch, pt=0, extra=13, seed=1, out_dtypes=("same", "f32")):
+    n = pool_demand(batch.context_lens, batch.block_size) + extra
+    order = free_order(n, seed)
+    ref = build_decode_state(batch, n, order, poison_bits(batch.dtype))
+    cache, tables, ctx = gpu_decode_state(batch, n, order)
+    # the block manager and both scatters agree bit for bit
+    assert np.array_equal(tables.cpu().numpy(), ref["block_tables"])
+    assert np.array_equal(ctx.cpu().numpy(), batch.context_lens)
+    assert np.array_equal(cache.k_cache.view(torch.int16).cpu().numpy().view(np.uint16),
+                          ref["k_cache"])
+    assert np.array_equal(cache.v_cache.view(torch.int16).cpu().numpy().view(np.uint16),
+                          ref["v_cache"])
+    want = oracle_decode(batch.q, ref["k_cache"], ref["v_cache"], ref["block_tables"],
+                         batch.context_lens, batch.block_size, batch.scale, batch.dtype)
+    q = dev(batch.q, batch.dtype)
+    outs = {}
+    for od in out_dtypes:
+        out = torch.empty(q.shape, dtype=q.dtype if od == "same" else torch.float32,
+                          device="cuda")
+        cache.attend(q, tables, ctx, float(batch.scale), out=out, partition_tokens=pt)
+        torch.cuda.synchronize()
+        assert_close(out, want, batch.dtype)
+        outs[od] = out
+    assert cache.err.item() == 0
+    return outs, cache, tables, ctx
+
+
+def test_tiny_config():
+    batch = tiny(0)
+    outs, *_ = run_case(batch, extra=64 - 18)
+
+
+CASES = [
+    # lens, H, H_kv, D, B, dtype, partition_tokens
+    ((1, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1000, 2048), 40, 40, 128, 16, "f16", 512),
+    ((1, 100, 513, 1537, 3000), 32, 8, 128, 16, "bf16", 512),
+    ((3, 64, 65, 700), 8, 8, 64, 8, "f16", 64),
+    ((2, 33, 95, 250), 6, 2, 64, 32, "bf16", 32),
+    ((1, 300, 257, 1024), 16, 2, 128, 64, "f16", 256),
+    ((7, 900, 4097), 10, 2, 128, 128, "bf16", 4096),
+    ((95, 96, 97, 300), 4, 2, 128, 8, "f16", 96),
+    ((129, 300, 64), 4, 4, 64, 128, "bf16", 32),
+    ((5000,), 8, 1, 128, 16, "bf16", 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_against_oracle(case):
+    lens, H, Hkv, D, B, dt, pt = case
+    batch = decode_batch("t", lens, H, Hkv, D, B, dt, seed=len(lens) + H)
+    run_case(batch, pt=pt)
+
+
+def test_outlier_keys_long_context():
+    """1% of the keys x8: softmax weights nearly one-hot in places."""
+    batch = decode_batch("t", (2500, 6000, 700), 32, 8, 128, 16, "bf16", seed=3,
+                         outlier_frac=0.01)
+    run_case(batch)
+
+
+def test_block_size_sweep_identical_outputs():
+    """Same token data placed in pools of block size 8..128: the outputs agree
+    bit for bit (tiles of 32 tokens and 512-token partitions do not depend on
+    the block size) and each matches the oracle."""
+    outs = []
+    for B in (8, 16, 32, 64, 128):
+        batch = decode_batch("t", (1, 77, 513, 1400, 2049), 40, 40, 128, B, "f16", seed=11)
+        o, *_ = run_case(batch, seed=B)
+        outs.append(o["f32"].cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_physical_placement_does_not_matter():
+    batch = decode_batch("t", (40, 555, 1111), 8, 2, 128, 16, "bf16", seed=12)
+    a, *_ = run_case(batch, seed=1, extra=40)
+    b, *_ = run_case(batch, seed=2, extra=40)
+    assert torch.equal(a["same"], b["same"]) and torch.equal(a["f32"], b["f32"])
+
+
+def test_shared_prefix_copy_on_write_pipeline():
+    """Beam groups: prefill once, fork, append tails step by step with
+    copy-on-write; tables, copy pairs and pools match the oracle's pipeline
+    bit for bit; outputs match the oracle and equal private copies bitwise."""
+    pb = gqa_prefix(seed=5, groups=6, beams=4, prefix_tokens=256, max_tail=70)
+    n = 400
+    order = free_order(n, 9)
+    ref = build_shared_prefix_state(pb, n, order, poison_bits(pb.dtype))
+    from paged_kv_cache_118_gb300.cache import PagedKVCache
+    cache = PagedKVCache(n, pb.block_size, pb.num_kv_heads, pb.head_size, torch.bfloat16,
+                         free_order=order)
+    for g in range(pb.num_groups):
+        a, b = pb.prefix_offsets[g], pb.prefix_offsets[g + 1]
+        cache.prefill([g * pb.beams], [b - a], dev(pb.prefix_k[a:b], "bf16"),
+                      dev(pb.prefix_v[a:b], "bf16"))
+        for j in range(1, pb.beams):
+            cache.fork(g * pb.beams, g * pb.beams + j)
+    cows = []
+    for i in range(int(pb.tail_lens.max())):
+        seqs = [s for s in range(pb.num_seqs) if pb.tail_lens[s] > i]
+        rows = pb.tail_offsets[seqs] + i
+        _, cow = cache.append(seqs, dev(pb.tail_k[rows], "bf16"), dev(pb.tail_v[rows], "bf16"))
+        cows += [tuple(c) for c in cow]
+    assert cows == [tuple(c) for c in ref["cow_pairs"]]
+    assert len(cows) == 3 * pb.num_groups
+    tables, ctx = cache.tables(range(pb.num_seqs))
+    assert np.array_equal(tables.cpu().numpy(), ref["block_tables"])
+    assert np.array_equal(ctx.cpu().numpy(), ref["context_lens"])
+    assert np.array_equal(cache.k_cache.view(torch.int16).cpu().numpy().view(np.uint16),
+                          ref["k_cache"])
+    want = oracle_decode(pb.q, ref["k_cache"], ref["v_cache"], ref["block_tables"],
+                         ref["context_lens"], 16, pb.scale, "bf16")
+    q = dev(pb.q, "bf16")
+    shared = cache.attend(q, tables, ctx, float(pb.scale))
+    torch.cuda.synchronize()
+    assert_close(shared, want, "bf16")
+    # private copies of the same tokens
+    lens, ks, vs = [], [], []
+    for s in range(pb.num_seqs):
+        g = s // pb.beams
+        pa, pz = pb.prefix_offsets[g], pb.prefix_offsets[g + 1]
+        ta, tz = pb.tail_offsets[s], pb.tail_offsets[s + 1]
+        ks.append(np.concatenate([pb.prefix_k[pa:pz], pb.tail_k[ta:tz]]))
+        vs.append(np.concatenate([pb.prefix_v[pa:pz], pb.tail_v[ta:tz]]))
+        lens.append(len(ks[-1]))
+    priv = PagedKVCache(sum(-(-L // 16) for L in lens) + 3, 16, 8, 128, torch.bfloat16,
+                        free_order=free_order(sum(-(-L // 16) for L in lens) + 3, 4))
+    priv.prefill(range(pb.num_seqs), lens, dev(np.concatenate(ks), "bf16"),
+                 dev(np.concatenate(vs), "bf16"))
+    pt, pc = priv.tables(range(pb.num_seqs))
+    private = priv.attend(q, pt, pc, float(pb.scale))
+    torch.cuda.synchronize()
+    assert torch.equal(shared, private)
+    assert cache.err.item() == 0 and priv.err.item() == 0
+
+
+def test_no_partial_prefix_means_no_copies():
+    pb = gqa_prefix(seed=6, groups=3, beams=4, prefix_tokens=64, max_tail=5, partial=False)
+    ref = build_shared_prefix_state(pb, 100, free_order(100, 1), poison_bits("bf16"))
+    assert len(ref["cow_pairs"]) == 0
+
+
+def test_reshape_and_cache_padding_and_range_errors():
+    kc = torch.zeros(4, 8, 2, 64, dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k = torch.randn(3, 2, 64, dtype=torch.float16, device="cuda")
+    v = torch.randn_like(k)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.tensor([5, -1, 32], dtype=torch.int64, device="cuda")
+    pk.pkv_reshape_and_cache(k, v, kc, vc, slots, err)
+    torch.cuda.synchronize()
+    assert torch.equal(kc.view(-1, 2, 64)[5], k[0]) and torch.equal(vc.view(-1, 2, 64)[5], v[0])
+    assert int((kc != 0).any(dim=(1, 2, 3)).sum()) == 1
+    assert err.item() & pk.PKV_DEVERR_SLOT
+
+
+@pytest.mark.parametrize("n_pairs", [1, 7, 1500])
+def test_copy_blocks_bitwise(n_pairs):
+    rng = np.random.default_rng(n_pairs)
+    nb = 2 * n_pairs + 5
+    kc_h = rng.integers(0, 1 << 16, (nb, 16, 8, 128), dtype=np.uint16)
+    vc_h = rng.integers(0, 1 << 16, (nb, 16, 8, 128), dtype=np.uint16)
+    perm = rng.permutation(nb)
+    pairs = np.stack([perm[:n_pairs], perm[n_pairs:2 * n_pairs]], 1)
+    kc, vc = dev(kc_h, "bf16"), dev(vc_h, "bf16")
+    pk.pkv_copy_blocks(kc, vc, pairs)
+    oracle_copy(kc_h, vc_h, pairs)
+    torch.cuda.synchronize()
+    assert np.array_equal(kc.view(torch.int16).cpu().numpy().view(np.uint16), kc_h)
+    assert np.array_equal(vc.view(torch.int16).cpu().numpy().view(np.uint16), vc_h)
+
+
+def test_decode_flags_bad_block_ids_and_lengths():
+    batch = decode_batch("t", (40, 70, 20), 4, 4, 64, 16, "f16", seed=21)
+    n = 20
+    cache, tables, ctx = gpu_decode_state(batch, n, free_order(n, 0))
+    q = dev(batch.q, "f16")
+    good = cache.attend(q, tables, ctx, float(batch.scale)).clone()
+    bad_tab = tables.clone()
+    bad_tab[1, 2] = n + 5                       # outside the pool
+    bad_ctx = ctx.clone()
+    bad_ctx[2] = tables.shape[1] * 16 + 1       # longer than its table
+    cache.err.zero_()
+    out = cache.attend(q, bad_tab, bad_ctx, float(batch.scale))
+    torch.cuda.synchronize()
+    e = cache.err.item()
+    assert e & pk.PKV_DEVERR_BLOCK_ID and e & pk.PKV_DEVERR_CONTEXT and not e & pk.PKV_DEVERR_TIMEOUT
+    assert torch.equal(out[0], good[0])         # untouched sequence
+    assert torch.all(out[2] == 0)               # invalid length -> zeros
