@@ -10,8 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     # Build libpagedkv.so in-tree when it is missing or older than its sources.
-    from paged_kv_cache_118_gb300 import build as _build
-    _build.build()
+    import importlib.util
+    path = os.path.join(ROOT, "paged_kv_cache_118_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("pkv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: large inputs; minutes of host work")
 
