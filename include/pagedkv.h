@@ -86,7 +86,7 @@ const char* pkv_version(void);
  *   context_lens device int32 [num_seqs]; 1 <= L <= max_blocks_per_seq * block_size
  *                (the newest token counts)
  *   head_size    64 or 128; num_heads a multiple of num_kv_heads
- *   block_size   8, 16, 32, 64 or 128
+ *   block_size   a power of two from 1 to 256
  *   scale        multiplies q.k (typically 1/sqrt(head_size))
  *   workspace    device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned;
  *                scratch owned by the caller, contents on entry irrelevant

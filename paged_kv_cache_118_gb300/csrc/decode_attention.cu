@@ -490,7 +490,8 @@ static int effective_partition(int partition_tokens) {
   return partition_tokens == 0 ? 512 : partition_tokens;
 }
 
-static bool block_size_ok(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
+// A 32-token tile is a whole number of blocks, or a whole number of tiles is a block.
+static bool block_size_ok(int b) { return b >= 1 && b <= 256 && (b & (b - 1)) == 0; }
 
 extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_size,
                                             int max_blocks_per_seq, int block_size,

@@ -56,7 +56,7 @@ def _decode_status(**over):
 
 @pytest.mark.parametrize("over", [
     dict(q=None), dict(out=None), dict(ws=None), dict(kv_dtype=2), dict(out_dtype=7),
-    dict(D=96), dict(D=256), dict(H=6, Hkv=4), dict(B=12), dict(B=256), dict(pt=48),
+    dict(D=96), dict(D=256), dict(H=6, Hkv=4), dict(B=12), dict(B=512), dict(pt=48),
     dict(pt=8192), dict(S=-1), dict(nb=0), dict(mb=0), dict(q=24), dict(k=8),
     dict(scale=float("nan")), dict(S=70000)])
 def test_decode_rejects_bad_arguments_on_host(over):

@@ -59,6 +59,9 @@ CASES = [
     ((95, 96, 97, 300), 4, 2, 128, 8, "f16", 96),
     ((129, 300, 64), 4, 4, 64, 128, "bf16", 32),
     ((5000,), 8, 1, 128, 16, "bf16", 0),
+    ((1, 2, 3, 70), 4, 2, 64, 1, "f16", 64),
+    ((33, 257, 600), 8, 8, 128, 256, "bf16", 512),
+    ((6, 45), 4, 4, 128, 2, "bf16", 32),
 ]
 
 
