@@ -60,19 +60,24 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(kernel_src: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the kernel source as it is now (sha256 recorded in the summary)."""
+def profile_traffic(kernel_src: str, bytes_per_launch: float):
+    """DRAM bytes per decode launch, from the committed ncu summary, if it was
+    taken on the kernel source as it is now (its sha256 is recorded there).
+    The captured launch's traffic is scaled to this run's launch by the ratio
+    of algorithmic bytes (same batch, a few tokens longer or shorter)."""
     path = os.path.join(ROOT, "profiles", "decode_partition_opt13b.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m or not t:
+    t = re.search(r"captured_traffic_bytes:\s*([0-9]+)", text)
+    a = re.search(r"captured_algorithmic_bytes:\s*([0-9]+)", text)
+    if not (m and t and a):
         return None
     cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return float(t.group(1)) if m.group(1) == cur else None
+    if m.group(1) != cur:
+        return None
+    return round(float(t.group(1)) * bytes_per_launch / float(a.group(1)))
 
 
 class ClockSampler:
@@ -307,7 +312,7 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = load_peaks()
     src = os.path.join(ROOT, "paged_kv_cache_118_gb300", "csrc", "decode_attention.cu")
-    traffic = profile_traffic(src)
+    traffic = profile_traffic(src, float(np.mean(per_call))) if args.config == "opt13b" else None
     ctx_mean = float(np.mean([c.sum() for c in ctx_log])) if ctx_log else float(L0.sum())
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
