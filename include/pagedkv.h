@@ -107,6 +107,43 @@ pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
                                       size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Decode attention without a caller workspace.
+ *
+ * No counterpart on the pages: this is a convenience of this library. It is
+ * for callers that cannot allocate device memory — a plugin that its host
+ * application gives only input and output buffers, or a serving loop that
+ * reserved all memory up front and must not call cudaMalloc (which can stall
+ * the device) while decoding. It computes exactly what
+ * pkv_paged_attention_decode computes, with the same arguments minus the
+ * workspace; the partition partials go to a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library keeps until the process exits. It allocates nothing.
+ *
+ *  - Limit: PKV_EWORKSPACE (nothing launched) when
+ *    pkv_decode_workspace_size(num_seqs, num_heads, head_size,
+ *    max_blocks_per_seq, block_size, partition_tokens) > PKV_NOALLOC_SCRATCH_BYTES.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture. A failed lookup returns PKV_ECUDA.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero (each call writes every partial it
+ *    reads), but calls whose GPU work overlaps — on different streams, or from
+ *    different host threads — race on it and corrupt each other's outputs:
+ *    issue them on one stream.
+ * ------------------------------------------------------------------------ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+
+pkv_status pkv_paged_attention_decode_noalloc(void* out, int out_dtype, const void* q,
+                                              const void* k_cache, const void* v_cache,
+                                              int kv_dtype, const int32_t* block_tables,
+                                              const int32_t* context_lens, int num_seqs,
+                                              int num_heads, int num_kv_heads, int head_size,
+                                              int num_blocks, int block_size,
+                                              int max_blocks_per_seq, float scale,
+                                              int partition_tokens, int32_t* err_flag,
+                                              void* stream);
+
+/* ------------------------------------------------------------------------
  * reshape_and_cache: write new tokens' keys and values into their slots.
  *
  * Defines ([R] §2 "共享与写时复制" and the §3 per-iteration algorithm box: the

@@ -7,7 +7,7 @@ stream becomes the CUDA stream. Every step of the computation runs in the
 library's CUDA kernels (or, for the block manager, its C++ host code).
 
 Importing this package loads the library and raises if it has not been built
-(``python -m paged_kv_cache_118_gb300.build``); there is no fallback.
+(``python paged_kv_cache_118_gb300/build.py``); there is no fallback.
 """
 
 from __future__ import annotations
@@ -37,6 +37,9 @@ SIGNATURES = {
     "pkv_paged_attention_decode": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                             _c_int, _c_f, _c_int, _vp, _c_sz, _vp, _vp]),
+    "pkv_paged_attention_decode_noalloc": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp,
+                                                    _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                                    _c_int, _c_int, _c_f, _c_int, _vp, _vp]),
     "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _vp, _vp]),
     "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_sz, _vp]),
@@ -60,7 +63,7 @@ SIGNATURES = {
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m paged_kv_cache_118_gb300.build` (needs nvcc)")
+                          "`python paged_kv_cache_118_gb300/build.py` (needs nvcc)")
     lib = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
@@ -136,6 +139,27 @@ def pkv_paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torc
         block_tables.shape[1], float(scale), partition_tokens, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream(stream))
     _check(st, "pkv_paged_attention_decode")
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def pkv_paged_attention_decode_noalloc(out: torch.Tensor, q: torch.Tensor,
+                                       k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                       block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                       block_size: int, scale: float, partition_tokens: int = 0,
+                                       err_flag: torch.Tensor | None = None, stream=None) -> None:
+    """pkv_paged_attention_decode without a workspace argument, for callers that
+    cannot allocate device memory: the partials go to the library's built-in
+    NOALLOC_SCRATCH_BYTES array (shared by all calls; keep calls on one stream)."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, err_flag)
+    S, H, D = q.shape
+    nb, B, Hkv, _ = k_cache.shape
+    st = lib.pkv_paged_attention_decode_noalloc(
+        _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
+        _ptr(block_tables), _ptr(context_lens), S, H, Hkv, D, nb, block_size,
+        block_tables.shape[1], float(scale), partition_tokens, _ptr(err_flag), _stream(stream))
+    _check(st, "pkv_paged_attention_decode_noalloc")
 
 
 def pkv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,

@@ -7,7 +7,7 @@ statically (the driver library is reached at run time). Objects go to
 ``paged_kv_cache_118_gb300/_build/``. A rebuild happens only when a source or
 header is newer than the library.
 
-    python -m paged_kv_cache_118_gb300.build [--force] [--verbose]
+    python paged_kv_cache_118_gb300/build.py [--force] [--verbose]
 """
 
 from __future__ import annotations

@@ -586,3 +586,64 @@ extern "C" pkv_status pkv_paged_attention_decode(
                        : launch_reduce<64>(out, out_dtype, rp, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the decode call.
+//
+// Some callers cannot hand the decode call a workspace: for example a plugin
+// that a host application gives only its input and output buffers while the
+// application owns every byte of device memory, or a serving loop that has
+// reserved the whole pool up front and must not call cudaMalloc (which can
+// stall the device) once decoding runs. For them, the partition partials live
+// in this fixed array, part of the library's image: every GPU that loads the
+// library holds its PKV_NOALLOC_SCRATCH_BYTES until the process exits. The
+// kernels are the same as those of pkv_paged_attention_decode; only the place
+// of the partials differs.
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of g_noalloc_scratch on the current device. Host code only
+// sees a host-side stand-in under the array's name, so the address is looked
+// up once per device (with that device current) and remembered.
+static pkv_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return PKV_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_noalloc(
+    void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+    int kv_dtype, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_heads, int num_kv_heads, int head_size, int num_blocks, int block_size,
+    int max_blocks_per_seq, float scale, int partition_tokens, int32_t* err_flag, void* stream) {
+  if (num_seqs == 0) return PKV_OK;
+  const size_t need = pkv_decode_workspace_size(num_seqs, num_heads, head_size,
+                                                max_blocks_per_seq, block_size, partition_tokens);
+  if (need == 0) return PKV_EINVAL;
+  if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_EWORKSPACE;
+  void* scratch = nullptr;
+  const pkv_status st = noalloc_scratch(&scratch);
+  if (st != PKV_OK) return st;
+  // Nothing in the array has to start at zero: the merge reads only partials
+  // that the same call wrote first, in stream order.
+  return pkv_paged_attention_decode(out, out_dtype, q, k_cache, v_cache, kv_dtype, block_tables,
+                                    context_lens, num_seqs, num_heads, num_kv_heads, head_size,
+                                    num_blocks, block_size, max_blocks_per_seq, scale,
+                                    partition_tokens, scratch, PKV_NOALLOC_SCRATCH_BYTES, err_flag,
+                                    stream);
+}
