@@ -38,9 +38,10 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode KV GB/s & fraction of GB300 HBM peak; decode tokens/s per config"
 FALLBACK_HBM_GBS = 6800.0
 CONFIGS = {
-    # name: (workload constructor kwargs, layers)
+    # name: layers of the model whose decode iteration one step runs
     "opt13b": dict(layers=40),
     "llama13b": dict(layers=40),
+    "gqa_prefix": dict(layers=16),
     "longctx": dict(layers=8),
 }
 
@@ -139,6 +140,11 @@ def workload_shape(name, seed):
         return wl.llama13b_lengths(128, seed), 40, 40, 128, 16, "f16"
     if name == "longctx":
         return np.array([n * 1024 for n in wl.LONGCTX_LENS_K], np.int32), 32, 8, 128, 16, "bf16"
+    if name == "gqa_prefix":
+        pb = wl.gqa_prefix(seed)
+        lens = np.array([int(pb.prefix_lens[s // 4]) + int(pb.tail_lens[s]) for s in range(256)],
+                        np.int32)
+        return lens, 32, 8, 128, 16, "bf16"
     raise ValueError(name)
 
 
@@ -160,6 +166,88 @@ def decode_bytes(ctx, H, Hkv, D, out_bytes):
     return int(np.sum(ctx, dtype=np.int64)) * 2 * Hkv * D * 2 + S * H * D * 2 + S * H * D * out_bytes
 
 
+def setup_pools(args, rank, dev, layers, total_steps):
+    """Pools of every layer filled with the workload's cached tokens through the
+    library (block manager + reshape_and_cache [+ copy_blocks]); returns the
+    state the timed decode steps start from."""
+    import torch
+    import paged_kv_cache_118_gb300 as pk
+    import workloads as wl
+
+    seed = args.seed + rank
+    if args.config == "gqa_prefix":
+        pb = wl.gqa_prefix(seed)
+        S, H, Hkv, D, B = pb.num_seqs, pb.num_heads, pb.num_kv_heads, pb.head_size, pb.block_size
+        tdt = torch.bfloat16
+        L0 = np.array([int(pb.prefix_lens[s // pb.beams]) + int(pb.tail_lens[s]) + 1
+                       for s in range(S)], np.int64)
+        unique = int(np.sum(-(-pb.prefix_lens // B))) + int(np.sum(-(-(pb.tail_lens + B + total_steps) // B)))
+        num_blocks = int(math.ceil(1.2 * unique))
+        bm = pk.BlockManager(num_blocks, B, wl.free_order(num_blocks, seed))
+        pre = []
+        for g in range(pb.num_groups):
+            bm.allocate(g * pb.beams, int(pb.prefix_lens[g]))
+            pre.append(bm.slots(g * pb.beams))
+            for j in range(1, pb.beams):
+                bm.fork(g * pb.beams, g * pb.beams + j)
+        tail_slots = np.full(int(pb.tail_offsets[-1]), -1, np.int64)
+        cows = []
+        for i in range(int(pb.tail_lens.max())):
+            seqs = np.nonzero(pb.tail_lens > i)[0]
+            sl, cow = bm.append_slots(seqs)
+            tail_slots[pb.tail_offsets[seqs] + i] = sl
+            cows.append(cow)
+        cows = np.concatenate(cows)
+        kc = torch.empty((layers, num_blocks, B, Hkv, D), dtype=tdt, device=dev)
+        vc = torch.empty_like(kc)
+        parts = [(np.concatenate(pre), pb.prefix_k, pb.prefix_v), (tail_slots, pb.tail_k, pb.tail_v)]
+        for i, (sl, kk, vv) in enumerate(parts):
+            d_sl = torch.from_numpy(sl).to(dev)
+            kt = torch.from_numpy(kk.view(np.int16)).view(tdt).to(dev)
+            vt = torch.from_numpy(vv.view(np.int16)).view(tdt).to(dev)
+            for l in range(layers):
+                if i == 1:
+                    pk.pkv_copy_blocks(kc[l], vc[l], cows)
+                pk.pkv_reshape_and_cache(kt, vt, kc[l], vc[l], d_sl)
+            del kt, vt, d_sl
+        # tokens of shared (full) blocks are read by several beams but stored once
+        refs = np.array([bm.refcount(b) for b in range(num_blocks)])
+        shared_extra = int(np.sum(np.maximum(refs - 1, 0))) * B
+        info = dict(dtype="bf16", scale=float(pb.scale), cow_pairs=int(len(cows)),
+                    groups=pb.num_groups, beams=pb.beams)
+    else:
+        batch = make_workload(args.config, seed)
+        S, H, Hkv, D, B = (batch.num_seqs, batch.num_heads, batch.num_kv_heads,
+                           batch.head_size, batch.block_size)
+        tdt = torch.float16 if batch.dtype == "f16" else torch.bfloat16
+        L0 = batch.context_lens.astype(np.int64)            # context at the first step
+        final = L0 + total_steps
+        num_blocks = int(math.ceil(1.2 * int(np.sum(-(-final // B)))))
+        bm = pk.BlockManager(num_blocks, B, wl.free_order(num_blocks, seed))
+        kc = torch.empty((layers, num_blocks, B, Hkv, D), dtype=tdt, device=dev)
+        vc = torch.empty_like(kc)
+        # prefill L-1 tokens of every sequence into every layer's pool
+        keep = np.ones(batch.total_tokens, bool)
+        keep[batch.offsets[1:] - 1] = False
+        slots = []
+        for s in range(S):
+            bm.allocate(s, int(L0[s]) - 1)
+            if L0[s] > 1:
+                slots.append(bm.slots(s))
+        d_slots = torch.from_numpy(np.concatenate(slots)).to(dev)
+        kp = torch.from_numpy(batch.k_tokens[keep].view(np.int16)).view(tdt).to(dev)
+        vp = torch.from_numpy(batch.v_tokens[keep].view(np.int16)).view(tdt).to(dev)
+        for l in range(layers):
+            pk.pkv_reshape_and_cache(kp, vp, kc[l], vc[l], d_slots)
+        del kp, vp, d_slots
+        shared_extra = 0
+        info = dict(dtype=batch.dtype, scale=float(batch.scale))
+    torch.cuda.synchronize()
+    width = int(np.max(-(-(L0 + total_steps) // B)))
+    return dict(bm=bm, kc=kc, vc=vc, S=S, H=H, Hkv=Hkv, D=D, B=B, tdt=tdt, L0=L0,
+                width=width, num_blocks=num_blocks, shared_extra=shared_extra, **info)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import paged_kv_cache_118_gb300 as pk
@@ -167,41 +255,20 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    batch = make_workload(args.config, args.seed + rank)
-    S, H, Hkv, D, B = (batch.num_seqs, batch.num_heads, batch.num_kv_heads, batch.head_size,
-                       batch.block_size)
     layers = args.layers or CONFIGS[args.config]["layers"]
-    tdt = torch.float16 if batch.dtype == "f16" else torch.bfloat16
     pt = args.partition_tokens
     total_steps = 2 * (args.warmup + args.steps) + 1
-    L0 = batch.context_lens.astype(np.int64)            # context at the first step
-    final = L0 + total_steps
-    demand = int(np.sum(-(-final // B)))
-    num_blocks = int(math.ceil(1.2 * demand))
-    width = int(np.max(-(-final // B)))
-    bm = pk.BlockManager(num_blocks, B, wl.free_order(num_blocks, args.seed + rank))
-    kc = torch.empty((layers, num_blocks, B, Hkv, D), dtype=tdt, device=dev)
-    vc = torch.empty_like(kc)
-
-    # prefill L-1 tokens of every sequence into every layer's pool
-    keep = np.ones(batch.total_tokens, bool)
-    keep[batch.offsets[1:] - 1] = False
-    slots = []
-    for s in range(S):
-        bm.allocate(s, int(L0[s]) - 1)
-        if L0[s] > 1:
-            slots.append(bm.slots(s))
-    d_slots = torch.from_numpy(np.concatenate(slots)).to(dev)
-    kp = torch.from_numpy(batch.k_tokens[keep].view(np.int16)).view(tdt).to(dev)
-    vp = torch.from_numpy(batch.v_tokens[keep].view(np.int16)).view(tdt).to(dev)
-    for l in range(layers):
-        pk.pkv_reshape_and_cache(kp, vp, kc[l], vc[l], d_slots)
-    del kp, vp, d_slots
-    torch.cuda.synchronize()
+    st = setup_pools(args, rank, dev, layers, total_steps)
+    bm, kc, vc = st["bm"], st["kc"], st["vc"]
+    S, H, Hkv, D, B, tdt, L0, width = (st[k] for k in ("S", "H", "Hkv", "D", "B", "tdt", "L0",
+                                                       "width"))
+    num_blocks = st["num_blocks"]
+    dtype_name = st["dtype"]
+    scale = st["scale"]
 
     # per-layer step inputs (resident), and pinned host copies for the e2e run
-    qh = np.stack([wl.queries(S, H, D, batch.dtype, args.seed, l) for l in range(layers)])
-    nk, nv = zip(*[wl.new_tokens(S, Hkv, D, batch.dtype, args.seed, l) for l in range(layers)])
+    qh = np.stack([wl.queries(S, H, D, dtype_name, args.seed, l) for l in range(layers)])
+    nk, nv = zip(*[wl.new_tokens(S, Hkv, D, dtype_name, args.seed, l) for l in range(layers)])
     host = {n: torch.from_numpy(np.stack(a).view(np.int16) if n != "q" else a.view(np.int16))
             .view(tdt).pin_memory() for n, a in (("q", qh), ("k", nk), ("v", nv))}
     q = host["q"].to(dev)
@@ -236,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
             pk.pkv_paged_attention_decode(out[l], q[l], kc[l], vc[l], d_tab, d_lens, B,
-                                          float(batch.scale), ws, pt, err)
+                                          scale, ws, pt, err)
             if timed_kernels:
                 b.record(stream)
                 ev_pairs.append((a, b))
@@ -278,7 +345,10 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop() if rank == 0 else None
     ms = max_over_ranks(t0.elapsed_time(t1))
     out_bytes = 2
-    per_call = [decode_bytes(c, H, Hkv, D, out_bytes) for c in ctx_log]
+    # unique bytes: a token stored once but read by several beams counts once
+    shared_bytes = st["shared_extra"] * 2 * Hkv * D * 2
+    logical_call = [decode_bytes(c, H, Hkv, D, out_bytes) for c in ctx_log]
+    per_call = [b - shared_bytes for b in logical_call]
     step_bytes = sum(per_call) * layers
     value = step_bytes * world / (ms * 1e-3) / 1e9
     dec_ms = [a.elapsed_time(b) for a, b in ev_pairs]
@@ -305,7 +375,8 @@ def run_ours(args, rank, world, local_rank):
         t1.record(stream)
         barrier()
         ms_e2e = max_over_ranks(max(t0.elapsed_time(t1), (time.perf_counter() - w0) * 1e3))
-        e_bytes = sum(decode_bytes(c, H, Hkv, D, out_bytes) for c in ctx_log) * layers
+        e_bytes = sum(decode_bytes(c, H, Hkv, D, out_bytes) - shared_bytes
+                      for c in ctx_log) * layers
         h2d = (q.numel() + knew.numel() + vnew.numel()) * 2 + S * (8 + 4 + 4 * width)
         e2e = {"value": round(e_bytes * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2)}
@@ -313,18 +384,20 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = load_peaks()
     src = os.path.join(ROOT, "paged_kv_cache_118_gb300", "csrc", "decode_attention.cu")
     traffic = profile_traffic(src, float(np.mean(per_call))) if args.config == "opt13b" else None
-    ctx_mean = float(np.mean([c.sum() for c in ctx_log])) if ctx_log else float(L0.sum())
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": batch.dtype, "data": "synthetic",
+        "dtype": dtype_name, "data": "synthetic",
         "config": {"workload": f"{args.config}_decode", "num_seqs": S, "num_heads": H,
                    "num_kv_heads": Hkv, "head_size": D, "block_size": B, "layers": layers,
                    "context_tokens_first_step": int(L0.sum()), "partition_tokens": pt or 512,
                    "num_blocks": num_blocks, "seed": args.seed,
-                   "l2": "inputs larger than L2 (each step reads every layer's pool)"},
+                   "l2": "inputs larger than L2 (each step reads every layer's pool)",
+                   **({"groups": st["groups"], "beams": st["beams"],
+                       "cow_pairs": st["cow_pairs"]} if "groups" in st else {})},
         "decode_tokens_per_s": round(tokens_s, 1),
+        "logical_GBps": round(sum(logical_call) * layers * world / (ms * 1e-3) / 1e9, 2),
         "frac_of_hbm_peak": round(value / peak, 4),
         "roofline": {"bound": "hbm", "kernel": "paged decode attention (partition + reduce)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",

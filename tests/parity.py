@@ -59,3 +59,40 @@ def gpu_decode_state(batch, num_blocks, order, poison=True):
                  dev(batch.v_tokens[last], batch.dtype))
     tables, ctx = cache.tables(range(S))
     return cache, tables, ctx
+
+
+def sub_batch(batch, s):
+    """Sequence s of a DecodeBatch as a batch of its own (same bits)."""
+    from workloads import DecodeBatch
+    a, b = int(batch.offsets[s]), int(batch.offsets[s + 1])
+    return DecodeBatch(batch.name, batch.dtype, batch.num_heads, batch.num_kv_heads,
+                       batch.head_size, batch.block_size, batch.scale,
+                       batch.context_lens[s:s + 1].copy(), batch.q[s:s + 1],
+                       batch.k_tokens[a:b], batch.v_tokens[a:b],
+                       np.array([0, b - a], np.int64), batch.seed)
+
+
+def oracle_sampled(batch, seqs):
+    """Oracle outputs [H, D] for the sampled sequences, each computed from a
+    pool of its own (placement does not change the result)."""
+    from oracle.attention import paged_attention_decode
+    from oracle.pipeline import build_decode_state, pool_demand
+    from workloads import free_order, poison_bits
+    out = {}
+    for s in seqs:
+        sb = sub_batch(batch, s)
+        n = pool_demand(sb.context_lens, sb.block_size) + 2
+        st = build_decode_state(sb, n, free_order(n, s), poison_bits(sb.dtype))
+        out[s] = paged_attention_decode(sb.q, st["k_cache"], st["v_cache"], st["block_tables"],
+                                        sb.context_lens, sb.block_size, sb.scale, sb.dtype)[0]
+    return out
+
+
+def sample_seqs(lens, k, seed):
+    """Shortest, longest, median and k-3 seeded others."""
+    order = np.argsort(lens, kind="stable")
+    pick = {int(order[0]), int(order[-1]), int(order[len(order) // 2])}
+    rng = np.random.default_rng(seed)
+    while len(pick) < min(k, len(lens)):
+        pick.add(int(rng.integers(len(lens))))
+    return sorted(pick)
