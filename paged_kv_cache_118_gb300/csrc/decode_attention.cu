@@ -47,23 +47,37 @@ constexpr int kGroups = kConsumerWarps * 32 / kGroupLanes;  // token groups per 
 constexpr int kStages = 4;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 growth of the max that forces a rescale
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a compact work list
 
 struct DecodeParams {
   float* part_acc;            // [rows][D], rows = num_seqs * num_heads * max_parts
   float2* part_ml;            // [rows] = (m in base-2 units, l)
+  int* counter;               // work counter, zero at launch
   const uint16_t* q;          // [num_seqs][num_heads][D]
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t* err;
+  int num_seqs;
   int num_heads;
   int group;                  // query heads per KV head (num_heads / num_kv_heads)
+  int subs;                   // CTAs' query-head slices per KV head (group / GS)
+  int kv_slices;              // num_kv_heads * subs
   int num_blocks;
   int block_size;
   int max_blocks_per_seq;
   int partition_tokens;
   int max_parts;
+  int total_units;            // max_parts * num_seqs * kv_slices
   int box_rows;               // rows per TMA copy: min(block_size, kTile)
   float q_scale;              // scale * log2(e)
+};
+
+// What the producer tells the consumers about the next unit of work.
+struct UnitDesc {
+  int seq;                    // -1: no more units; -2: the producer gave up (timeout)
+  int head0;
+  int part;
+  int len;
 };
 
 template <int D, int GS>
@@ -72,113 +86,428 @@ struct DecodeLayout {
   static constexpr int kTileBytes = kTile * kRowBytes;        // K (or V) of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kQBytes = GS * D * 2;                  // query rows of one unit
   static constexpr int kCombineFloats = kConsumerWarps * GS * (D + 2);
   static constexpr int kChunks = D / 64;                      // 16-byte pieces per lane per row
   static constexpr int kE = 8 * kChunks;                      // elements per lane per row
+  // offsets (bytes) from the 1024-aligned base
+  static constexpr int kOffCombine = kRingBytes;
+  static constexpr int kOffQ = kOffCombine + kCombineFloats * 4;
+  static constexpr int kOffBars = kOffQ + 2 * kQBytes;        // 16-byte aligned
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;    // full, empty, q_full, q_empty, merge
+  static constexpr int kOffUnits = kOffBars + kNumBars * 8;
+  static constexpr int kOffFlag = kOffUnits + 2 * sizeof(UnitDesc);
+  static constexpr int kOffPref = kOffFlag + 16;               // prefix of partitions per sequence
+  static constexpr int kOffSlice = kOffPref + ((kCompactMaxSeqs + 1) * 4 + 15) / 16 * 16;
   static int smem_bytes(int table_slice) {
-    return 1024 /*alignment slack*/ + kRingBytes + kCombineFloats * 4 + 2 * kStages * 8 +
-           ((table_slice * 4 + 15) / 16) * 16;
+    return 1024 /*alignment slack*/ + kOffSlice + ((table_slice * 4 + 15) / 16) * 16;
+  }
+};
+
+// Transposed reduction inside an 8-lane token group: every lane holds partial
+// dot products for the GS heads over its 16 (or 8) elements; after three
+// exchange steps each lane holds the full score of one head (lane pairs for
+// GS=4, quads for GS=2), owners of a head agreeing bit for bit. It replaces
+// GS separate butterflies (3*GS shuffles) by 4 (GS=4) or 3 shuffles.
+template <int GS>
+struct GroupHeads;
+template <>
+struct GroupHeads<2> {
+  // lane j owns head (j >> 2) & 1
+  static __device__ __forceinline__ int owner(int g) { return 4 * g; }
+  static __device__ __forceinline__ float reduce(const float* s, int j, unsigned mask) {
+    const bool hi = (j >> 2) & 1;
+    const float send = hi ? s[0] : s[1];
+    float x = hi ? s[1] : s[0];
+    x += __shfl_xor_sync(mask, send, 4);
+    x += __shfl_xor_sync(mask, x, 2);
+    x += __shfl_xor_sync(mask, x, 1);
+    return x;
+  }
+};
+template <>
+struct GroupHeads<4> {
+  // lane j owns head 2 * ((j >> 2) & 1) + ((j >> 1) & 1)
+  static __device__ __forceinline__ int owner(int g) { return 4 * (g >> 1) + 2 * (g & 1); }
+  static __device__ __forceinline__ float reduce(const float* s, int j, unsigned mask) {
+    const bool b2 = (j >> 2) & 1;
+    const bool b1 = (j >> 1) & 1;
+    const float send0 = b2 ? s[0] : s[2];
+    const float send1 = b2 ? s[1] : s[3];
+    float k0 = b2 ? s[2] : s[0];
+    float k1 = b2 ? s[3] : s[1];
+    k0 += __shfl_xor_sync(mask, send0, 4);
+    k1 += __shfl_xor_sync(mask, send1, 4);
+    const float send = b1 ? k0 : k1;
+    float x = b1 ? k1 : k0;
+    x += __shfl_xor_sync(mask, send, 2);
+    x += __shfl_xor_sync(mask, x, 1);
+    return x;
+  }
+};
+
+__device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+__device__ __forceinline__ void st_volatile(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
+
+// Per-lane state of one unit for one token group: scalar math for one query
+// head (GS = 1), packed f32x2 math with the transposed reduction otherwise.
+template <int D, int GS, typename T>
+struct GroupState;
+
+template <int D, typename T>
+struct GroupState<D, 1, T> {
+  static constexpr int E = DecodeLayout<D, 1>::kE;
+  static constexpr int kChunks = DecodeLayout<D, 1>::kChunks;
+  float q[E], acc[E], m, l;
+
+  __device__ __forceinline__ void begin(const uint16_t* qs, int j, float q_scale) {
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(qs + c * 64 + 8 * j);
+      widen8<T>(raw, &q[c * 8]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[c * 8 + e] *= q_scale;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  __device__ __forceinline__ void token(const uint16_t* krow, const uint16_t* vrow, int j,
+                                        unsigned gmask, int) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(krow + c * 64 + 8 * j);
+      float kf[8];
+      widen8<T>(raw, kf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s = fmaf(q[c * 8 + e], kf[e], s);
+    }
+    s += __shfl_xor_sync(gmask, s, 1);
+    s += __shfl_xor_sync(gmask, s, 2);
+    s += __shfl_xor_sync(gmask, s, 4);
+    if (s > m + kRescaleThreshold) {            // uniform in the group
+      const float corr = ex2(m - s);
+      l *= corr;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] *= corr;
+      m = s;
+    }
+    const float pr = ex2(s - m);
+    l += pr;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(vrow + c * 64 + 8 * j);
+      float vf[8];
+      widen8<T>(raw, vf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[c * 8 + e] = fmaf(pr, vf[e], acc[c * 8 + e]);
+    }
+  }
+
+  __device__ __forceinline__ float head_m(int, int) const { return m; }
+  __device__ __forceinline__ float head_l(int, int) const { return l; }
+  __device__ __forceinline__ void head_acc(int, int e, float& a, float& b) const {
+    a = acc[2 * e];
+    b = acc[2 * e + 1];
   }
 };
 
 template <int D, int GS, typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+struct GroupState {
+  static constexpr int E = DecodeLayout<D, GS>::kE;
+  static constexpr int P2 = E / 2;
+  static constexpr int kChunks = DecodeLayout<D, GS>::kChunks;
+  f32x2 q2[GS][P2], acc[GS][P2];
+  float m, l;     // state of the head this lane owns (GroupHeads<GS>)
+
+  __device__ __forceinline__ void begin(const uint16_t* qs, int j, float q_scale) {
+    const f32x2 sc = pack2(q_scale, q_scale);
+#pragma unroll
+    for (int g = 0; g < GS; ++g)
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * D + c * 64 + 8 * j);
+        q2[g][c * 4 + 0] = mul2(T::to_pair(raw.x), sc);
+        q2[g][c * 4 + 1] = mul2(T::to_pair(raw.y), sc);
+        q2[g][c * 4 + 2] = mul2(T::to_pair(raw.z), sc);
+        q2[g][c * 4 + 3] = mul2(T::to_pair(raw.w), sc);
+      }
+#pragma unroll
+    for (int g = 0; g < GS; ++g)
+#pragma unroll
+      for (int e = 0; e < P2; ++e) acc[g][e] = 0ull;
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  __device__ __forceinline__ void token(const uint16_t* krow, const uint16_t* vrow, int j,
+                                        unsigned gmask, int base) {
+    // q.k for the GS heads: one widening of each key pair serves all heads.
+    f32x2 d2[GS];
+#pragma unroll
+    for (int g = 0; g < GS; ++g) d2[g] = 0ull;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(krow + c * 64 + 8 * j);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const f32x2 kp = T::to_pair(w[u]);
+#pragma unroll
+        for (int g = 0; g < GS; ++g) d2[g] = fma2(q2[g][c * 4 + u], kp, d2[g]);
+      }
+    }
+    float s[GS];
+#pragma unroll
+    for (int g = 0; g < GS; ++g) {
+      float a, b;
+      unpack2(d2[g], a, b);
+      s[g] = a + b;
+    }
+    const float sc = GroupHeads<GS>::reduce(s, j, gmask);
+    // Online softmax of the owned head; the accumulators of every head are
+    // rescaled only when some head's maximum grows by more than 2^8.
+    const bool need = sc > m + kRescaleThreshold;
+    if (__any_sync(gmask, need)) {
+      const float mn = need ? sc : m;
+      const float corr = need ? ex2(m - mn) : 1.f;
+      m = mn;
+      l *= corr;
+#pragma unroll
+      for (int g = 0; g < GS; ++g) {
+        const float cg = __shfl_sync(gmask, corr, base + GroupHeads<GS>::owner(g));
+        const f32x2 c2 = pack2(cg, cg);
+#pragma unroll
+        for (int e = 0; e < P2; ++e) acc[g][e] = mul2(acc[g][e], c2);
+      }
+    }
+    const float pr = ex2(sc - m);
+    l += pr;
+    f32x2 pg[GS];
+#pragma unroll
+    for (int g = 0; g < GS; ++g) {
+      const float x = __shfl_sync(gmask, pr, base + GroupHeads<GS>::owner(g));
+      pg[g] = pack2(x, x);
+    }
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(vrow + c * 64 + 8 * j);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const f32x2 vp = T::to_pair(w[u]);
+#pragma unroll
+        for (int g = 0; g < GS; ++g) acc[g][c * 4 + u] = fma2(pg[g], vp, acc[g][c * 4 + u]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ float head_m(int g, int base) const {
+    return __shfl_sync(0xffffffffu, m, base + GroupHeads<GS>::owner(g));
+  }
+  __device__ __forceinline__ float head_l(int g, int base) const {
+    return __shfl_sync(0xffffffffu, l, base + GroupHeads<GS>::owner(g));
+  }
+  __device__ __forceinline__ void head_acc(int g, int e, float& a, float& b) const {
+    unpack2(acc[g][e], a, b);
+  }
+};
+
+// Persistent: each CTA takes units of work — (context partition, sequence,
+// KV-head slice), partition-major — from a global counter until none is
+// left. The producer warp fetches the next unit, its slice of the block table
+// and its query rows while the consumers still work on the current one.
+template <int D, int GS, typename T>
+__global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using Lay = DecodeLayout<D, GS>;
-  constexpr int E = Lay::kE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  float* combine = reinterpret_cast<float*>(smem + Lay::kRingBytes);
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(combine + Lay::kCombineFloats);
+  float* combine = reinterpret_cast<float*>(smem + Lay::kOffCombine);
+  uint16_t* qbuf = reinterpret_cast<uint16_t*>(smem + Lay::kOffQ);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* empty_bar = full_bar + kStages;
-  int32_t* slice = reinterpret_cast<int32_t*>(empty_bar + kStages);
+  uint64_t* q_full = empty_bar + kStages;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* merge_bar = q_empty + 2;          // [0]: partials written, [1]: partials read
+  UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + Lay::kOffUnits);
+  int* abort_flag = reinterpret_cast<int*>(smem + Lay::kOffFlag);
+  int* pref = reinterpret_cast<int*>(smem + Lay::kOffPref);
+  int32_t* slice = reinterpret_cast<int32_t*>(smem + Lay::kOffSlice);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int subs = p.group / GS;                 // CTAs per KV head
-  const int kvh = blockIdx.x / subs;
-  const int head0 = kvh * p.group + (blockIdx.x % subs) * GS;
-  const int seq = blockIdx.y;
-  const int part = blockIdx.z;
   const int B = p.block_size;
-
-  const int L = __ldg(p.context_lens + seq);
-  if (L < 1 || L > p.max_blocks_per_seq * B) {
-    if (threadIdx.x == 0 && part == 0 && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-    return;
-  }
-  const int t_begin = part * p.partition_tokens;
-  if (t_begin >= L) return;
-  const int t_end = min(L, t_begin + p.partition_tokens);
-  const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
-  const int jb0 = t_begin / B;
-  const int nb = (t_end - 1) / B - jb0 + 1;
+  const int max_ctx = p.max_blocks_per_seq * B;
+  const int per_part = p.num_seqs * p.kv_slices;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], kConsumerWarps);
+      mbar_init(&merge_bar[i], kConsumerWarps);
+    }
+    *abort_flag = 0;
     fence_barrier_init();
   }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer warp
   if (warp == kConsumerWarps) {
+    const uint64_t policy = l2_evict_first_policy();
+    const uint32_t copy_bytes = static_cast<uint32_t>(p.box_rows) * Lay::kRowBytes;
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
     }
-    const int32_t* row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0;
-    for (int i = lane; i < nb; i += 32) {
-      int32_t id = __ldg(row + i);
-      if (id < 0 || id >= p.num_blocks) {
-        flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-        id = 0;
+    // The work list. For batches of up to kCompactMaxSeqs sequences only the
+    // units that exist are numbered, sequence-major (a prefix sum of each
+    // sequence's partition count, then a binary search per unit); larger
+    // batches number every (partition, sequence, slice) and skip the empty ones.
+    const bool compact = p.num_seqs <= kCompactMaxSeqs;
+    int total = p.total_units;
+    if (compact) {
+      int carry = 0;
+      for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        int np = 0;
+        if (s < p.num_seqs) {
+          const int L = __ldg(p.context_lens + s);
+          if (L >= 1 && L <= max_ctx)
+            np = (L + p.partition_tokens - 1) / p.partition_tokens;
+          else if (blockIdx.x == 0)
+            flag_error(p.err, PKV_DEVERR_CONTEXT);
+        }
+        int x = np;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (s < p.num_seqs) pref[s + 1] = carry + x;
+        carry += __shfl_sync(0xffffffffu, x, 31);
       }
-      slice[i] = id;
+      if (lane == 0) pref[0] = 0;
+      __syncwarp();
+      total = carry * p.kv_slices;
     }
-  }
-  __syncthreads();
-
-  // ------------------------------------------------------------ producer
-  if (warp == kConsumerWarps) {
-    if (lane != 0) return;
-    const uint64_t policy = l2_evict_first_policy();
-    const uint32_t copy_bytes = static_cast<uint32_t>(p.box_rows) * Lay::kRowBytes;
+    int issued = 0;                           // tiles issued (ring position)
+    int k = 0;                                // units published
+    int ok = 1;
     int last_issued[kStages];
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
-    bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kStages;
-      if (i >= kStages && !mbar_wait(&empty_bar[st], ((i / kStages) & 1) ^ 1)) {
-        ok = false;
-        break;
-      }
-      const int t0 = t_begin + i * kTile;
-      const int valid = min(kTile, t_end - t0);
-      const int copies = B >= kTile ? 1 : (valid + B - 1) / B;
-      uint8_t* kdst = ring + st * Lay::kStageBytes;
-      uint8_t* vdst = kdst + Lay::kTileBytes;
-      mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
-      for (int c = 0; c < copies; ++c) {
-        int z;
-        if (B >= kTile) {
-          z = slice[t0 / B - jb0] * B + (t0 % B);
-        } else {
-          z = slice[t0 / B + c - jb0] * B;
+    while (true) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(p.counter, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= total) break;
+      int part, seq, kvs;
+      if (compact) {
+        int lo = 0, hi = p.num_seqs;          // largest lo with pref[lo] * slices <= u
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pref[mid] * p.kv_slices <= u) lo = mid; else hi = mid;
         }
-        tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
-        tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
+        seq = lo;
+        const int rem = u - pref[lo] * p.kv_slices;
+        part = rem / p.kv_slices;
+        kvs = rem - part * p.kv_slices;
+      } else {
+        part = u / per_part;
+        const int rem = u - part * per_part;
+        seq = rem / p.kv_slices;
+        kvs = rem - seq * p.kv_slices;
       }
-      last_issued[st] = i;
+      const int L = __ldg(p.context_lens + seq);
+      if (L < 1 || L > max_ctx) {
+        if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+        continue;
+      }
+      const int t_begin = part * p.partition_tokens;
+      if (t_begin >= L) continue;             // this sequence has no such partition
+      const int t_end = min(L, t_begin + p.partition_tokens);
+      const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+      const int jb0 = t_begin / B;
+      const int nb = (t_end - 1) / B - jb0 + 1;
+      const int kvh = kvs / p.subs;
+      const int head0 = kvh * p.group + (kvs - kvh * p.subs) * GS;
+      const int32_t* row =
+          p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0;
+      for (int i = lane; i < nb; i += 32) {
+        int32_t id = __ldg(row + i);
+        if (id < 0 || id >= p.num_blocks) {
+          flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+          id = 0;
+        }
+        slice[i] = id;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const int qb = k & 1;
+        if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
+        if (ok) {
+          units[qb] = UnitDesc{seq, head0, part, L};
+          mbar_arrive_expect_tx(&q_full[qb], Lay::kQBytes);
+          bulk_load(qbuf + qb * GS * D,
+                    p.q + (static_cast<int64_t>(seq) * p.num_heads + head0) * D, Lay::kQBytes,
+                    &q_full[qb]);
+        }
+        for (int i = 0; ok && i < n_tiles; ++i, ++issued) {
+          const int st = issued % kStages;
+          if (issued >= kStages && !mbar_wait(&empty_bar[st], ((issued / kStages) & 1) ^ 1)) {
+            ok = 0;
+            break;
+          }
+          if (ld_volatile(abort_flag)) {
+            ok = 0;
+            break;
+          }
+          const int t0 = t_begin + i * kTile;
+          const int valid = min(kTile, t_end - t0);
+          const int copies = B >= kTile ? 1 : (valid + B - 1) / B;
+          uint8_t* kdst = ring + st * Lay::kStageBytes;
+          uint8_t* vdst = kdst + Lay::kTileBytes;
+          mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
+          for (int c = 0; c < copies; ++c) {
+            const int z = B >= kTile ? slice[t0 / B - jb0] * B + (t0 % B)
+                                     : slice[t0 / B + c - jb0] * B;
+            tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
+            tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
+          }
+          last_issued[st] = issued;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++k;
+      __syncwarp();                           // lane 0 is done reading the slice
+      if (!ok) break;
     }
-    if (!ok) {
-      flag_error(p.err, PKV_DEVERR_TIMEOUT);
-      // Let the copies already in flight land before the CTA can retire.
-      for (int st = 0; st < kStages; ++st)
-        if (last_issued[st] >= 0) mbar_wait(&full_bar[st], (last_issued[st] / kStages) & 1);
+    if (lane == 0) {
+      // Publish the end of the work (or the abort) to the consumers.
+      const int qb = k & 1;
+      if (ok && k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
+      if (!ok) {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        st_volatile(abort_flag, 1);
+      }
+      units[qb].seq = ok ? -1 : -2;
+      mbar_arrive(&q_full[qb]);
+      if (!ok) {
+        // Let the copies already in flight land before the CTA can retire.
+        for (int st = 0; st < kStages; ++st)
+          if (last_issued[st] >= 0) mbar_wait(&full_bar[st], (last_issued[st] / kStages) & 1);
+      }
     }
     return;
   }
@@ -187,142 +516,111 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int grp = lane >> 3;                      // group within the warp
   const int gi = warp * 4 + grp;                  // group within the CTA (0..15)
   const int j = lane & 7;                         // lane within the group
-  const unsigned gmask = 0xffu << (grp * 8);
-
-  float qf[GS][E];
-#pragma unroll
-  for (int g = 0; g < GS; ++g) {
-    const uint16_t* qrow = p.q + (static_cast<int64_t>(seq) * p.num_heads + head0 + g) * D;
-#pragma unroll
-    for (int c = 0; c < Lay::kChunks; ++c) {
-      uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + 8 * j));
-      widen8<T>(raw, &qf[g][c * 8]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[g][c * 8 + e] *= p.q_scale;
-    }
-  }
-  float m[GS], l[GS], acc[GS][E];
-#pragma unroll
-  for (int g = 0; g < GS; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
-  }
-
-  bool ok = true;
-  for (int i = 0; i < n_tiles; ++i) {
-    const int st = i % kStages;
-    if (!mbar_wait(&full_bar[st], (i / kStages) & 1)) {
-      ok = false;
+  const int base = grp * 8;
+  const unsigned gmask = 0xffu << base;
+  GroupState<D, GS, T> gs;
+  int consumed = 0;                               // tiles consumed (ring position)
+  for (int k = 0;; ++k) {
+    const int qb = k & 1;
+    UnitDesc ud{-2, 0, 0, 0};
+    if (!ld_volatile(abort_flag) && mbar_wait(&q_full[qb], (k >> 1) & 1)) ud = units[qb];
+    if (ud.seq == -1) break;                      // all work done
+    if (ud.seq == -2) {                           // abort: nothing more is coming
+      if (lane == 0) {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        st_volatile(abort_flag, 1);
+      }
       break;
     }
-    const int valid = min(kTile, t_end - (t_begin + i * kTile));
-    const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * Lay::kStageBytes);
-    const uint16_t* vs = ks + kTile * D;
+    gs.begin(qbuf + qb * GS * D, j, p.q_scale);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[qb]);
+
+    const int t_begin = ud.part * p.partition_tokens;
+    const int t_end = min(ud.len, t_begin + p.partition_tokens);
+    const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+    for (int i = 0; i < n_tiles; ++i, ++consumed) {
+      const int st = consumed % kStages;
+      if (ld_volatile(abort_flag) || !mbar_wait(&full_bar[st], (consumed / kStages) & 1)) {
+        if (lane == 0) st_volatile(abort_flag, 1);
+        continue;                                 // keep the unit's control flow, skip work
+      }
+      const int valid = min(kTile, t_end - (t_begin + i * kTile));
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * Lay::kStageBytes);
+      const uint16_t* vs = ks + kTile * D;
 #pragma unroll
-    for (int r = 0; r < kTile / kGroups; ++r) {
-      const int tk = gi + r * kGroups;
-      if (tk < valid) {
-        float s[GS];
+      for (int r = 0; r < kTile / kGroups; ++r) {
+        const int tk = gi + r * kGroups;
+        if (tk < valid) gs.token(ks + tk * D, vs + tk * D, j, gmask, base);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+
+    // Merge the four groups of this warp (lanes j, j+8, j+16, j+24 hold the
+    // same elements), then the four warps through shared memory.
+    if (k >= 1) mbar_wait(&merge_bar[1], (k - 1) & 1);   // previous unit's partials read
 #pragma unroll
-        for (int g = 0; g < GS; ++g) s[g] = 0.f;
+    for (int g = 0; g < GS; ++g) {
+      const float mg = gs.head_m(g, base);
+      const float lg = gs.head_l(g, base);
+      float mx = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float f = (mx == -INFINITY) ? 0.f : ex2(mg - mx);
+      float ls = lg * f;
+      ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+      float* cw = combine + (warp * GS + g) * (D + 2);
 #pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c) {
-          uint4 raw = *reinterpret_cast<const uint4*>(ks + tk * D + c * 64 + 8 * j);
-          float kf[8];
-          widen8<T>(raw, kf);
-#pragma unroll
-          for (int g = 0; g < GS; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s[g] = fmaf(qf[g][c * 8 + e], kf[e], s[g]);
-        }
-        float pr[GS];
-#pragma unroll
-        for (int g = 0; g < GS; ++g) {
-          s[g] += __shfl_xor_sync(gmask, s[g], 1);
-          s[g] += __shfl_xor_sync(gmask, s[g], 2);
-          s[g] += __shfl_xor_sync(gmask, s[g], 4);
-          if (s[g] > m[g] + kRescaleThreshold) {
-            const float corr = ex2(m[g] - s[g]);
-            l[g] *= corr;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[g][e] *= corr;
-            m[g] = s[g];
-          }
-          pr[g] = ex2(s[g] - m[g]);
-          l[g] += pr[g];
-        }
-#pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c) {
-          uint4 raw = *reinterpret_cast<const uint4*>(vs + tk * D + c * 64 + 8 * j);
-          float vf[8];
-          widen8<T>(raw, vf);
-#pragma unroll
-          for (int g = 0; g < GS; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][c * 8 + e] = fmaf(pr[g], vf[e], acc[g][c * 8 + e]);
+      for (int e = 0; e < Lay::kE / 2; ++e) {
+        float a, b;
+        gs.head_acc(g, e, a, b);
+        a *= f;
+        b *= f;
+        a += __shfl_xor_sync(0xffffffffu, a, 8);
+        b += __shfl_xor_sync(0xffffffffu, b, 8);
+        a += __shfl_xor_sync(0xffffffffu, a, 16);
+        b += __shfl_xor_sync(0xffffffffu, b, 16);
+        if (grp == 0) {
+          const int el = (e / 4) * 64 + 8 * j + 2 * (e % 4);
+          cw[2 + el] = a;
+          cw[2 + el + 1] = b;
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[st]);
-  }
-  if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
-
-  // Merge the four groups of this warp (lanes j, j+8, j+16, j+24 hold the same
-  // elements), then the four warps through shared memory.
-#pragma unroll
-  for (int g = 0; g < GS; ++g) {
-    float mx = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float f = (mx == -INFINITY) ? 0.f : ex2(m[g] - mx);
-    float ls = l[g] * f;
-    ls += __shfl_xor_sync(0xffffffffu, ls, 8);
-    ls += __shfl_xor_sync(0xffffffffu, ls, 16);
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      float a = acc[g][e] * f;
-      a += __shfl_xor_sync(0xffffffffu, a, 8);
-      a += __shfl_xor_sync(0xffffffffu, a, 16);
-      acc[g][e] = a;
-    }
-    float* cw = combine + (warp * GS + g) * (D + 2);
-    if (grp == 0) {
-#pragma unroll
-      for (int c = 0; c < Lay::kChunks; ++c)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cw[2 + c * 64 + 8 * j + e] = acc[g][c * 8 + e];
-      if (j == 0) {
+      if (grp == 0 && j == 0) {
         cw[0] = mx;
         cw[1] = ls;
       }
     }
-  }
-  named_sync(1, kConsumerWarps * 32);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&merge_bar[0]);
+    mbar_wait(&merge_bar[0], k & 1);
 
-  const int64_t row0 =
-      (static_cast<int64_t>(seq) * p.num_heads + head0) * p.max_parts + part;
-  for (int idx = threadIdx.x; idx < GS * D; idx += kConsumerWarps * 32) {
-    const int g = idx / D;
-    const int e = idx % D;
-    float mw[kConsumerWarps];
-    float M = -INFINITY;
+    const int64_t row0 =
+        (static_cast<int64_t>(ud.seq) * p.num_heads + ud.head0) * p.max_parts + ud.part;
+    for (int idx = threadIdx.x; idx < GS * D; idx += kConsumerWarps * 32) {
+      const int g = idx / D;
+      const int e = idx % D;
+      float mw[kConsumerWarps];
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      mw[w] = combine[(w * GS + g) * (D + 2)];
-      M = fmaxf(M, mw[w]);
-    }
-    float a = 0.f, lsum = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        mw[w] = combine[(w * GS + g) * (D + 2)];
+        M = fmaxf(M, mw[w]);
+      }
+      float a = 0.f, lsum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
-      a = fmaf(combine[(w * GS + g) * (D + 2) + 2 + e], f, a);
-      lsum = fmaf(combine[(w * GS + g) * (D + 2) + 1], f, lsum);
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
+        a = fmaf(combine[(w * GS + g) * (D + 2) + 2 + e], f, a);
+        lsum = fmaf(combine[(w * GS + g) * (D + 2) + 1], f, lsum);
+      }
+      const int64_t row = row0 + static_cast<int64_t>(g) * p.max_parts;
+      p.part_acc[row * D + e] = a;
+      if (e == 0) p.part_ml[row] = make_float2(M, lsum);
     }
-    const int64_t row = row0 + static_cast<int64_t>(g) * p.max_parts;
-    p.part_acc[row * D + e] = a;
-    if (e == 0) p.part_ml[row] = make_float2(M, lsum);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&merge_bar[1]);
   }
 }
 
@@ -431,35 +729,64 @@ static bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_k
   return r == CUDA_SUCCESS;
 }
 
+// Query heads per CTA: 4, 2 or 1, the largest that divides the group.
 static int pick_group_slice(int group) {
-  for (int gs = 4; gs > 1; --gs)
-    if (group % gs == 0) return gs;
+  if (group % 4 == 0) return 4;
+  if (group % 2 == 0) return 2;
   return 1;
+}
+
+static int device_sm_count() {
+  static int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      v = 0;
+    return v;
+  }();
+  return n;
 }
 
 template <int D, int GS, typename T>
 static cudaError_t launch_partition(const CUtensorMap& tk, const CUtensorMap& tv,
-                                    const DecodeParams& p, int num_kv_heads, int num_seqs,
-                                    cudaStream_t stream) {
+                                    const DecodeParams& p, cudaStream_t stream) {
   auto kern = decode_partition_kernel<D, GS, T>;
   const int slice = p.partition_tokens / p.block_size + 2;
   const int smem = DecodeLayout<D, GS>::smem_bytes(slice);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // Attribute and occupancy are looked up once per shared-memory size.
+  static int cached_smem = -1, cached_blocks = 0;
+  static std::mutex mu;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached_smem != smem) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      int blocks = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, smem);
+      if (e != cudaSuccess) return e;
+      cached_smem = smem;
+      cached_blocks = blocks;
+    }
+    per_sm = cached_blocks;
+  }
+  const int sms = device_sm_count();
+  if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+  const int grid = static_cast<int>(std::min<int64_t>(p.total_units,
+                                                      static_cast<int64_t>(sms) * per_sm));
+  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
-  dim3 grid(num_kv_heads * (p.group / GS), num_seqs, p.max_parts);
   kern<<<grid, kThreads, smem, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
 template <int D, typename T>
 static cudaError_t dispatch_gs(int gs, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeParams& p, int num_kv_heads, int num_seqs,
-                               cudaStream_t s) {
+                               const DecodeParams& p, cudaStream_t s) {
   switch (gs) {
-    case 1: return launch_partition<D, 1, T>(tk, tv, p, num_kv_heads, num_seqs, s);
-    case 2: return launch_partition<D, 2, T>(tk, tv, p, num_kv_heads, num_seqs, s);
-    case 3: return launch_partition<D, 3, T>(tk, tv, p, num_kv_heads, num_seqs, s);
-    default: return launch_partition<D, 4, T>(tk, tv, p, num_kv_heads, num_seqs, s);
+    case 1: return launch_partition<D, 1, T>(tk, tv, p, s);
+    case 2: return launch_partition<D, 2, T>(tk, tv, p, s);
+    default: return launch_partition<D, 4, T>(tk, tv, p, s);
   }
 }
 
@@ -502,7 +829,8 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int hea
     return 0;
   const int64_t parts = (static_cast<int64_t>(max_blocks_per_seq) * block_size + pt - 1) / pt;
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_heads * parts;
-  return static_cast<size_t>(rows * head_size * 4 + rows * 8 + 16);
+  // partial accumulators, (m, l) pairs, then the work counter (16-byte aligned)
+  return static_cast<size_t>(rows * head_size * 4 + ((rows * 8 + 15) / 16) * 16 + 16);
 }
 
 extern "C" pkv_status pkv_paged_attention_decode(
@@ -544,9 +872,19 @@ extern "C" pkv_status pkv_paged_attention_decode(
     return PKV_ECUDA;
 
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_heads * parts;
+  const int gs = pick_group_slice(num_heads / num_kv_heads);
+  const int64_t kv_slices = static_cast<int64_t>(num_kv_heads) * (num_heads / num_kv_heads / gs);
+  const int64_t total_units = parts * num_seqs * kv_slices;
+  if (total_units > INT32_MAX / 2) return PKV_EINVAL;
   DecodeParams p{};
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float2*>(static_cast<float*>(workspace) + rows * head_size);
+  p.counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + rows * head_size * 4 +
+                                     ((rows * 8 + 15) / 16) * 16);
+  p.num_seqs = num_seqs;
+  p.subs = num_heads / num_kv_heads / gs;
+  p.kv_slices = static_cast<int>(kv_slices);
+  p.total_units = static_cast<int>(total_units);
   p.q = static_cast<const uint16_t*>(q);
   p.block_tables = block_tables;
   p.context_lens = context_lens;
@@ -560,16 +898,15 @@ extern "C" pkv_status pkv_paged_attention_decode(
   p.max_parts = static_cast<int>(parts);
   p.box_rows = box_rows;
   p.q_scale = scale * kLog2e;
-  const int gs = pick_group_slice(p.group);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
   if (head_size == 128) {
-    e = kv_dtype == PKV_F16 ? dispatch_gs<128, F16>(gs, tk, tv, p, num_kv_heads, num_seqs, s)
-                            : dispatch_gs<128, BF16>(gs, tk, tv, p, num_kv_heads, num_seqs, s);
+    e = kv_dtype == PKV_F16 ? dispatch_gs<128, F16>(gs, tk, tv, p, s)
+                            : dispatch_gs<128, BF16>(gs, tk, tv, p, s);
   } else {
-    e = kv_dtype == PKV_F16 ? dispatch_gs<64, F16>(gs, tk, tv, p, num_kv_heads, num_seqs, s)
-                            : dispatch_gs<64, BF16>(gs, tk, tv, p, num_kv_heads, num_seqs, s);
+    e = kv_dtype == PKV_F16 ? dispatch_gs<64, F16>(gs, tk, tv, p, s)
+                            : dispatch_gs<64, BF16>(gs, tk, tv, p, s);
   }
   if (e != cudaSuccess) return PKV_ECUDA;
 

@@ -72,6 +72,14 @@ def test_against_oracle(case):
     run_case(batch, pt=pt)
 
 
+def test_large_batch_uses_the_plain_work_list():
+    """More than 1024 sequences: units are numbered (partition, sequence, head
+    slice) with empty ones skipped instead of a compact list."""
+    lens = np.random.default_rng(7).integers(1, 700, size=1100)
+    batch = decode_batch("t", lens, 4, 2, 64, 16, "bf16", seed=8)
+    run_case(batch, pt=256)
+
+
 def test_outlier_keys_long_context():
     """1% of the keys x8: softmax weights nearly one-hot in places."""
     batch = decode_batch("t", (2500, 6000, 700), 32, 8, 128, 16, "bf16", seed=3,
