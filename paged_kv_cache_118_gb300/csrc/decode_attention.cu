@@ -32,6 +32,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "pagedkv.h"
 #include "pkv_device.cuh"
@@ -48,6 +49,7 @@ constexpr int kStages = 4;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 growth of the max that forces a rescale
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a compact work list
+constexpr int kMmaHeads = 8;                // query heads one CTA serves on the tensor path
 
 struct DecodeParams {
   float* part_acc;            // [rows][D], rows = num_seqs * num_heads * max_parts
@@ -60,7 +62,8 @@ struct DecodeParams {
   int num_seqs;
   int num_heads;
   int group;                  // query heads per KV head (num_heads / num_kv_heads)
-  int subs;                   // CTAs' query-head slices per KV head (group / GS)
+  int subs;                   // CTAs' query-head slices per KV head
+  int heads_per_cta;          // query heads one CTA serves (GS; at most 8 on the tensor path)
   int kv_slices;              // num_kv_heads * subs
   int num_blocks;
   int block_size;
@@ -316,12 +319,110 @@ struct GroupState {
   }
 };
 
+// Tensor-core state of one consumer warp (grouped query heads): the warp owns
+// 8 tokens of every 32-token tile. q.k and p.v run as warp-level m16n8k16 /
+// m16n8k8 products with fp32 accumulation; the query heads of the CTA are the
+// 16 rows of A (rows past heads_per_cta, and rows 8..15, are zero). Lane
+// (g = lane/4, t = lane%4) holds head g's scores of tokens 2t, 2t+1 and its
+// output columns 8j + 2t, 8j + 2t + 1. P is fed as two halves in the input
+// format (p = hi + lo), which keeps p.v at close to fp32 accuracy.
+// K and V tiles are stored by TMA with 128-byte swizzle, one 128-byte
+// (64-element) half of the head dimension per region, so that the 16-byte
+// chunk c of token row r sits at chunk c ^ (r % 8): ldmatrix without bank
+// conflicts.
+template <int D, typename T>
+struct MmaState {
+  static constexpr int KS = D / 16;               // k-steps of q.k
+  static constexpr int NT = D / 8;                // 8-column tiles of the output
+  static constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a tile
+  uint32_t qa[KS][2];                             // A fragments, rows g: k 2t.. and 2t+8..
+  float o[NT][4];
+  float m, l;
+
+  __device__ __forceinline__ void begin(const uint16_t* qs, int heads, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = g < heads ? *reinterpret_cast<const uint32_t*>(qs + g * D + 16 * ks + 2 * t) : 0u;
+      qa[ks][1] =
+          g < heads ? *reinterpret_cast<const uint32_t*>(qs + g * D + 16 * ks + 8 + 2 * t) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  // kt, vt: the stage's K and V tiles (each D/64 swizzled halves); tok0: first
+  // token of this warp in the tile; valid: tokens of the tile that exist.
+  __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int tok0, int valid,
+                                       float q_scale, int lane) {
+    const int t = lane & 3;
+    const int r = lane & 7;                       // row this lane addresses in ldmatrix
+    const int mat = lane >> 3;                    // matrix this lane addresses
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp) {
+      const int chunk = 4 * kp + mat;             // 16-byte chunk along d
+      const uint8_t* a = kt + (chunk >> 3) * kHalfBytes + (tok0 + r) * 128 +
+                         (((chunk & 7) ^ r) << 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(smem_addr(a), b0, b1, b2, b3);
+      T::mma16816(s, qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
+      T::mma16816(s, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+    }
+    const int tk = tok0 + 2 * t;
+    const float s0 = tk < valid ? s[0] * q_scale : -INFINITY;
+    const float s1 = tk + 1 < valid ? s[1] * q_scale : -INFINITY;
+    float tm = fmaxf(s0, s1);
+    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+    const bool need = tm > m + kRescaleThreshold;
+    if (__any_sync(0xffffffffu, need)) {
+      const float mn = need ? tm : m;
+      const float corr = need ? ex2(m - mn) : 1.f;
+      m = mn;
+      l *= corr;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= corr;
+        o[j][1] *= corr;
+      }
+    }
+    const float p0 = s0 == -INFINITY ? 0.f : ex2(s0 - m);
+    const float p1 = s1 == -INFINITY ? 0.f : ex2(s1 - m);
+    l += p0 + p1;
+    const uint32_t ph = T::pack(p0, p1);
+    const float2 hf = T::to_float2(ph);
+    const uint32_t pl = T::pack(p0 - hf.x, p1 - hf.y);
+    // V rows of tokens past the tile's end may hold anything: zero their halves.
+    const uint32_t keep = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int nq = 0; nq < NT / 4; ++nq) {
+      const int chunk = 4 * nq + mat;
+      const uint8_t* a = vt + (chunk >> 3) * kHalfBytes + (tok0 + r) * 128 +
+                         (((chunk & 7) ^ r) << 4);
+      uint32_t b[4];
+      ldsm_x4_t(smem_addr(a), b[0], b[1], b[2], b[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t bv = b[i] & keep;
+        T::mma1688(o[4 * nq + i], ph, 0u, bv);
+        T::mma1688(o[4 * nq + i], pl, 0u, bv);
+      }
+    }
+  }
+};
+
 // Persistent: each CTA takes units of work — (context partition, sequence,
 // KV-head slice), partition-major — from a global counter until none is
 // left. The producer warp fetches the next unit, its slice of the block table
 // and its query rows while the consumers still work on the current one.
-template <int D, int GS, typename T>
-__global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
+// kMma: grouped query heads on the tensor path (MmaState; K/V tiles stored
+// with 128-byte swizzle by 64-element halves; GS is then the capacity, 8, and
+// p.heads_per_cta the heads actually served). Otherwise GroupState.
+template <int D, int GS, typename T, bool kMma>
+__global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using Lay = DecodeLayout<D, GS>;
@@ -441,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
       const int jb0 = t_begin / B;
       const int nb = (t_end - 1) / B - jb0 + 1;
       const int kvh = kvs / p.subs;
-      const int head0 = kvh * p.group + (kvs - kvh * p.subs) * GS;
+      const int head0 = kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta;
       const int32_t* row =
           p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0;
       for (int i = lane; i < nb; i += 32) {
@@ -458,9 +559,10 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
         if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
         if (ok) {
           units[qb] = UnitDesc{seq, head0, part, L};
-          mbar_arrive_expect_tx(&q_full[qb], Lay::kQBytes);
+          const uint32_t qbytes = static_cast<uint32_t>(p.heads_per_cta) * D * 2;
+          mbar_arrive_expect_tx(&q_full[qb], qbytes);
           bulk_load(qbuf + qb * GS * D,
-                    p.q + (static_cast<int64_t>(seq) * p.num_heads + head0) * D, Lay::kQBytes,
+                    p.q + (static_cast<int64_t>(seq) * p.num_heads + head0) * D, qbytes,
                     &q_full[qb]);
         }
         for (int i = 0; ok && i < n_tiles; ++i, ++issued) {
@@ -482,8 +584,18 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
           for (int c = 0; c < copies; ++c) {
             const int z = B >= kTile ? slice[t0 / B - jb0] * B + (t0 % B)
                                      : slice[t0 / B + c - jb0] * B;
-            tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
-            tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
+            if constexpr (kMma) {
+              // one copy per 64-element half of the head dimension, 128 B per row
+#pragma unroll
+              for (int h = 0; h < D / 64; ++h) {
+                const int off = h * MmaState<D, T>::kHalfBytes + c * p.box_rows * 128;
+                tma_load_3d(kdst + off, &tm_k, &full_bar[st], 64 * h, kvh, z, policy);
+                tma_load_3d(vdst + off, &tm_v, &full_bar[st], 64 * h, kvh, z, policy);
+              }
+            } else {
+              tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
+              tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
+            }
           }
           last_issued[st] = issued;
         }
@@ -518,7 +630,9 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
   const int j = lane & 7;                         // lane within the group
   const int base = grp * 8;
   const unsigned gmask = 0xffu << base;
-  GroupState<D, GS, T> gs;
+  const int heads = p.heads_per_cta;
+  using State = typename std::conditional<kMma, MmaState<D, T>, GroupState<D, GS, T>>::type;
+  State gs;
   int consumed = 0;                               // tiles consumed (ring position)
   for (int k = 0;; ++k) {
     const int qb = k & 1;
@@ -532,7 +646,11 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
       }
       break;
     }
-    gs.begin(qbuf + qb * GS * D, j, p.q_scale);
+    if constexpr (kMma) {
+      gs.begin(qbuf + qb * GS * D, heads, lane);
+    } else {
+      gs.begin(qbuf + qb * GS * D, j, p.q_scale);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&q_empty[qb]);
 
@@ -546,50 +664,75 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
         continue;                                 // keep the unit's control flow, skip work
       }
       const int valid = min(kTile, t_end - (t_begin + i * kTile));
-      const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * Lay::kStageBytes);
-      const uint16_t* vs = ks + kTile * D;
+      if constexpr (kMma) {
+        const uint8_t* kt = ring + st * Lay::kStageBytes;
+        if (warp * 8 < valid) gs.tile(kt, kt + Lay::kTileBytes, warp * 8, valid, p.q_scale, lane);
+      } else {
+        const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * Lay::kStageBytes);
+        const uint16_t* vs = ks + kTile * D;
 #pragma unroll
-      for (int r = 0; r < kTile / kGroups; ++r) {
-        const int tk = gi + r * kGroups;
-        if (tk < valid) gs.token(ks + tk * D, vs + tk * D, j, gmask, base);
+        for (int r = 0; r < kTile / kGroups; ++r) {
+          const int tk = gi + r * kGroups;
+          if (tk < valid) gs.token(ks + tk * D, vs + tk * D, j, gmask, base);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
 
-    // Merge the four groups of this warp (lanes j, j+8, j+16, j+24 hold the
-    // same elements), then the four warps through shared memory.
+    // Merge this warp's partial into shared memory (one row of D + 2 floats
+    // per head: m, l, acc), then the four warps' rows into the unit's partial.
     if (k >= 1) mbar_wait(&merge_bar[1], (k - 1) & 1);   // previous unit's partials read
+    if constexpr (kMma) {
+      const int g = lane >> 2, t = lane & 3;
+      float ls = gs.l;
+      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+      if (g < heads) {
+        float* cw = combine + (warp * GS + g) * (D + 2);
 #pragma unroll
-    for (int g = 0; g < GS; ++g) {
-      const float mg = gs.head_m(g, base);
-      const float lg = gs.head_l(g, base);
-      float mx = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float f = (mx == -INFINITY) ? 0.f : ex2(mg - mx);
-      float ls = lg * f;
-      ls += __shfl_xor_sync(0xffffffffu, ls, 8);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 16);
-      float* cw = combine + (warp * GS + g) * (D + 2);
-#pragma unroll
-      for (int e = 0; e < Lay::kE / 2; ++e) {
-        float a, b;
-        gs.head_acc(g, e, a, b);
-        a *= f;
-        b *= f;
-        a += __shfl_xor_sync(0xffffffffu, a, 8);
-        b += __shfl_xor_sync(0xffffffffu, b, 8);
-        a += __shfl_xor_sync(0xffffffffu, a, 16);
-        b += __shfl_xor_sync(0xffffffffu, b, 16);
-        if (grp == 0) {
-          const int el = (e / 4) * 64 + 8 * j + 2 * (e % 4);
-          cw[2 + el] = a;
-          cw[2 + el + 1] = b;
+        for (int jn = 0; jn < MmaState<D, T>::NT; ++jn) {
+          cw[2 + 8 * jn + 2 * t] = gs.o[jn][0];
+          cw[2 + 8 * jn + 2 * t + 1] = gs.o[jn][1];
+        }
+        if (t == 0) {
+          cw[0] = gs.m;
+          cw[1] = ls;
         }
       }
-      if (grp == 0 && j == 0) {
-        cw[0] = mx;
-        cw[1] = ls;
+    } else {
+      // Lanes j, j+8, j+16, j+24 hold the same elements: merge the groups first.
+#pragma unroll
+      for (int g = 0; g < GS; ++g) {
+        const float mg = gs.head_m(g, base);
+        const float lg = gs.head_l(g, base);
+        float mx = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float f = (mx == -INFINITY) ? 0.f : ex2(mg - mx);
+        float ls = lg * f;
+        ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+        float* cw = combine + (warp * GS + g) * (D + 2);
+#pragma unroll
+        for (int e = 0; e < Lay::kE / 2; ++e) {
+          float a, b;
+          gs.head_acc(g, e, a, b);
+          a *= f;
+          b *= f;
+          a += __shfl_xor_sync(0xffffffffu, a, 8);
+          b += __shfl_xor_sync(0xffffffffu, b, 8);
+          a += __shfl_xor_sync(0xffffffffu, a, 16);
+          b += __shfl_xor_sync(0xffffffffu, b, 16);
+          if (grp == 0) {
+            const int el = (e / 4) * 64 + 8 * j + 2 * (e % 4);
+            cw[2 + el] = a;
+            cw[2 + el + 1] = b;
+          }
+        }
+        if (grp == 0 && j == 0) {
+          cw[0] = mx;
+          cw[1] = ls;
+        }
       }
     }
     __syncwarp();
@@ -598,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, GS >= 4 ? 2 : 3)
 
     const int64_t row0 =
         (static_cast<int64_t>(ud.seq) * p.num_heads + ud.head0) * p.max_parts + ud.part;
-    for (int idx = threadIdx.x; idx < GS * D; idx += kConsumerWarps * 32) {
+    for (int idx = threadIdx.x; idx < heads * D; idx += kConsumerWarps * 32) {
       const int g = idx / D;
       const int e = idx % D;
       float mw[kConsumerWarps];
@@ -714,22 +857,32 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D view of a cache: x = element within the head (D), y = KV head,
 // z = slot (block * B + row); box = D x 1 x box_rows.
 static bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads,
-                             int64_t slots, int box_rows) {
+                             int64_t slots, int box_rows, bool swizzled) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_kv_heads),
                         static_cast<cuuint64_t>(slots)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows)};
+  // swizzled: 64-element (128-byte) boxes stored with the 128-byte swizzle
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(swizzled ? 64 : D), 1,
+                       static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// Query heads per CTA: 4, 2 or 1, the largest that divides the group.
+// Largest divisor of n that is at most cap.
+static int largest_divisor_upto(int n, int cap) {
+  for (int d = std::min(n, cap); d > 1; --d)
+    if (n % d == 0) return d;
+  return 1;
+}
+
+// Query heads per CTA on the packed-pair path: 4, 2 or 1, the largest that divides the group.
 static int pick_group_slice(int group) {
   if (group % 4 == 0) return 4;
   if (group % 2 == 0) return 2;
@@ -747,10 +900,10 @@ static int device_sm_count() {
   return n;
 }
 
-template <int D, int GS, typename T>
+template <int D, int GS, typename T, bool kMma>
 static cudaError_t launch_partition(const CUtensorMap& tk, const CUtensorMap& tv,
                                     const DecodeParams& p, cudaStream_t stream) {
-  auto kern = decode_partition_kernel<D, GS, T>;
+  auto kern = decode_partition_kernel<D, GS, T, kMma>;
   const int slice = p.partition_tokens / p.block_size + 2;
   const int smem = DecodeLayout<D, GS>::smem_bytes(slice);
   // Attribute and occupancy are looked up once per shared-memory size.
@@ -781,12 +934,13 @@ static cudaError_t launch_partition(const CUtensorMap& tk, const CUtensorMap& tv
 }
 
 template <int D, typename T>
-static cudaError_t dispatch_gs(int gs, const CUtensorMap& tk, const CUtensorMap& tv,
+static cudaError_t dispatch_gs(bool mma, int gs, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeParams& p, cudaStream_t s) {
+  if (mma) return launch_partition<D, kMmaHeads, T, true>(tk, tv, p, s);
   switch (gs) {
-    case 1: return launch_partition<D, 1, T>(tk, tv, p, s);
-    case 2: return launch_partition<D, 2, T>(tk, tv, p, s);
-    default: return launch_partition<D, 4, T>(tk, tv, p, s);
+    case 1: return launch_partition<D, 1, T, false>(tk, tv, p, s);
+    case 2: return launch_partition<D, 2, T, false>(tk, tv, p, s);
+    default: return launch_partition<D, 4, T, false>(tk, tv, p, s);
   }
 }
 
@@ -864,15 +1018,21 @@ extern "C" pkv_status pkv_paged_attention_decode(
                                                 max_blocks_per_seq, block_size, pt);
   if (workspace_bytes < need) return PKV_EWORKSPACE;
 
+  // Grouped query heads go to the tensor path when every TMA copy lands on a
+  // 1 KB boundary of a tile half (block_size >= 8), else to the packed-pair path.
+  const int group = num_heads / num_kv_heads;
+  const bool mma = group >= 2 && block_size >= 8;
   const int box_rows = std::min(block_size, kTile);
   CUtensorMap tk, tv;
   const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
-  if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows) ||
-      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows))
+  if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, mma) ||
+      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, mma))
     return PKV_ECUDA;
 
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_heads * parts;
-  const int gs = pick_group_slice(num_heads / num_kv_heads);
+  const int gs = (num_heads / num_kv_heads >= 2 && block_size >= 8)
+                     ? largest_divisor_upto(num_heads / num_kv_heads, kMmaHeads)
+                     : pick_group_slice(num_heads / num_kv_heads);
   const int64_t kv_slices = static_cast<int64_t>(num_kv_heads) * (num_heads / num_kv_heads / gs);
   const int64_t total_units = parts * num_seqs * kv_slices;
   if (total_units > INT32_MAX / 2) return PKV_EINVAL;
@@ -883,6 +1043,7 @@ extern "C" pkv_status pkv_paged_attention_decode(
                                      ((rows * 8 + 15) / 16) * 16);
   p.num_seqs = num_seqs;
   p.subs = num_heads / num_kv_heads / gs;
+  p.heads_per_cta = gs;
   p.kv_slices = static_cast<int>(kv_slices);
   p.total_units = static_cast<int>(total_units);
   p.q = static_cast<const uint16_t*>(q);
@@ -902,11 +1063,11 @@ extern "C" pkv_status pkv_paged_attention_decode(
 
   cudaError_t e;
   if (head_size == 128) {
-    e = kv_dtype == PKV_F16 ? dispatch_gs<128, F16>(gs, tk, tv, p, s)
-                            : dispatch_gs<128, BF16>(gs, tk, tv, p, s);
+    e = kv_dtype == PKV_F16 ? dispatch_gs<128, F16>(mma, gs, tk, tv, p, s)
+                            : dispatch_gs<128, BF16>(mma, gs, tk, tv, p, s);
   } else {
-    e = kv_dtype == PKV_F16 ? dispatch_gs<64, F16>(gs, tk, tv, p, s)
-                            : dispatch_gs<64, BF16>(gs, tk, tv, p, s);
+    e = kv_dtype == PKV_F16 ? dispatch_gs<64, F16>(mma, gs, tk, tv, p, s)
+                            : dispatch_gs<64, BF16>(mma, gs, tk, tv, p, s);
   }
   if (e != cudaSuccess) return PKV_ECUDA;
 
