@@ -45,7 +45,6 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kGroupLanes = 8;      // lanes that share one token row
 constexpr int kGroups = kConsumerWarps * 32 / kGroupLanes;  // token groups per CTA (16)
-constexpr int kStages = 4;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 growth of the max that forces a rescale
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a compact work list
@@ -83,8 +82,11 @@ struct UnitDesc {
   int len;
 };
 
-template <int D, int GS>
+// kMma: the tensor path keeps 2 CTAs per SM and affords a 5-stage ring; the
+// scalar paths keep 3 CTAs per SM with 4 stages.
+template <int D, int GS, bool kMma = false>
 struct DecodeLayout {
+  static constexpr int kStages = kMma ? 5 : 4;
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kTile * kRowBytes;        // K (or V) of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
@@ -326,15 +328,20 @@ struct GroupState {
 // (g = lane/4, t = lane%4) holds head g's scores of tokens 2t, 2t+1 and its
 // output columns 8j + 2t, 8j + 2t + 1. P is fed as two halves in the input
 // format (p = hi + lo), which keeps p.v at close to fp32 accuracy.
-// K and V tiles are stored by TMA with 128-byte swizzle, one 128-byte
-// (64-element) half of the head dimension per region, so that the 16-byte
-// chunk c of token row r sits at chunk c ^ (r % 8): ldmatrix without bank
-// conflicts.
+// K and V tiles are stored by TMA with the 128-byte swizzle: token row r of
+// the tile is NH = D/64 lines of 128 bytes (64 elements each), line
+// L = r * NH + h, and the 16-byte chunk c of line L sits at chunk c ^ (L % 8).
+// ldmatrix then meets no bank conflict for d = 64 and at most two-way ones
+// for d = 128, while one TMA box moves a whole block (whole rows).
 template <int D, typename T>
 struct MmaState {
   static constexpr int KS = D / 16;               // k-steps of q.k
   static constexpr int NT = D / 8;                // 8-column tiles of the output
-  static constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a tile
+  static constexpr int NH = D / 64;               // 128-byte lines per token row
+  static __device__ __forceinline__ uint32_t line_addr(const uint8_t* tile, int row, int chunk) {
+    const int line = row * NH + (chunk >> 3);
+    return smem_addr(tile + line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
+  }
   uint32_t qa[KS][2];                             // A fragments, rows g: k 2t.. and 2t+8..
   float o[NT][4];
   float m, l;
@@ -360,17 +367,18 @@ struct MmaState {
     const int t = lane & 3;
     const int r = lane & 7;                       // row this lane addresses in ldmatrix
     const int mat = lane >> 3;                    // matrix this lane addresses
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // two accumulators halve the dependent chain of products
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kp = 0; kp < KS / 2; ++kp) {
       const int chunk = 4 * kp + mat;             // 16-byte chunk along d
-      const uint8_t* a = kt + (chunk >> 3) * kHalfBytes + (tok0 + r) * 128 +
-                         (((chunk & 7) ^ r) << 4);
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(smem_addr(a), b0, b1, b2, b3);
+      ldsm_x4(line_addr(kt, tok0 + r, chunk), b0, b1, b2, b3);
       T::mma16816(s, qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
-      T::mma16816(s, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+      T::mma16816(s2, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
     }
+    s[0] += s2[0];
+    s[1] += s2[1];
     const int tk = tok0 + 2 * t;
     const float s0 = tk < valid ? s[0] * q_scale : -INFINITY;
     const float s1 = tk + 1 < valid ? s[1] * q_scale : -INFINITY;
@@ -400,16 +408,14 @@ struct MmaState {
 #pragma unroll
     for (int nq = 0; nq < NT / 4; ++nq) {
       const int chunk = 4 * nq + mat;
-      const uint8_t* a = vt + (chunk >> 3) * kHalfBytes + (tok0 + r) * 128 +
-                         (((chunk & 7) ^ r) << 4);
       uint32_t b[4];
-      ldsm_x4_t(smem_addr(a), b[0], b[1], b[2], b[3]);
+      ldsm_x4_t(line_addr(vt, tok0 + r, chunk), b[0], b[1], b[2], b[3]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t bv = b[i] & keep;
-        T::mma1688(o[4 * nq + i], ph, 0u, bv);
-        T::mma1688(o[4 * nq + i], pl, 0u, bv);
-      }
+      for (int i = 0; i < 4; ++i) b[i] &= keep;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) T::mma1688(o[4 * nq + i], ph, 0u, b[i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) T::mma1688(o[4 * nq + i], pl, 0u, b[i]);
     }
   }
 };
@@ -425,7 +431,8 @@ template <int D, int GS, typename T, bool kMma>
 __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-  using Lay = DecodeLayout<D, GS>;
+  using Lay = DecodeLayout<D, GS, kMma>;
+  constexpr int kStages = Lay::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -585,13 +592,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
             const int z = B >= kTile ? slice[t0 / B - jb0] * B + (t0 % B)
                                      : slice[t0 / B + c - jb0] * B;
             if constexpr (kMma) {
-              // one copy per 64-element half of the head dimension, 128 B per row
-#pragma unroll
-              for (int h = 0; h < D / 64; ++h) {
-                const int off = h * MmaState<D, T>::kHalfBytes + c * p.box_rows * 128;
-                tma_load_3d(kdst + off, &tm_k, &full_bar[st], 64 * h, kvh, z, policy);
-                tma_load_3d(vdst + off, &tm_v, &full_bar[st], 64 * h, kvh, z, policy);
-              }
+              // 4-D view (64 elements, D/64 lines, head, slot): whole rows, swizzled
+              tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, 0, kvh, z, policy);
+              tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, 0, kvh, z, policy);
             } else {
               tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
               tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
@@ -860,18 +863,33 @@ static bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_k
                              int64_t slots, int box_rows, bool swizzled) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_kv_heads),
-                        static_cast<cuuint64_t>(slots)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                           static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
-  // swizzled: 64-element (128-byte) boxes stored with the 128-byte swizzle
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(swizzled ? 64 : D), 1,
-                       static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (!swizzled) {
+    // 3-D view: x = element within the head (D), y = KV head, z = slot; box D x 1 x rows.
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_kv_heads),
+                          static_cast<cuuint64_t>(slots)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // 4-D view: x = 64 elements (128 bytes), y = which 64-element line of the
+    // head, z = KV head, w = slot; box 64 x D/64 x 1 x rows with the 128-byte
+    // swizzle: one copy moves whole rows of a block.
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64),
+                          static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(slots)};
+    cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(D / 64), 1,
+                         static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS;
 }
 
@@ -905,7 +923,7 @@ static cudaError_t launch_partition(const CUtensorMap& tk, const CUtensorMap& tv
                                     const DecodeParams& p, cudaStream_t stream) {
   auto kern = decode_partition_kernel<D, GS, T, kMma>;
   const int slice = p.partition_tokens / p.block_size + 2;
-  const int smem = DecodeLayout<D, GS>::smem_bytes(slice);
+  const int smem = DecodeLayout<D, GS, kMma>::smem_bytes(slice);
   // Attribute and occupancy are looked up once per shared-memory size.
   static int cached_smem = -1, cached_blocks = 0;
   static std::mutex mu;
