@@ -53,6 +53,23 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device or "cpu")
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processes its own batch of the same size, so
+    the job moves world x bytes_per_rank in the slowest rank's time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -318,12 +335,6 @@ def run_ours(args, rank, world, local_rank):
             td.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if not dist:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        return float(t.item())
 
     # ---- device-resident run
     for _ in range(args.warmup):
@@ -343,14 +354,14 @@ def run_ours(args, rank, world, local_rank):
     t1.record(stream)
     barrier()
     clk = clocks.stop() if rank == 0 else None
-    ms = max_over_ranks(t0.elapsed_time(t1))
+    ms = max_over_ranks(t0.elapsed_time(t1), dev)
     out_bytes = 2
     # unique bytes: a token stored once but read by several beams counts once
     shared_bytes = st["shared_extra"] * 2 * Hkv * D * 2
     logical_call = [decode_bytes(c, H, Hkv, D, out_bytes) for c in ctx_log]
     per_call = [b - shared_bytes for b in logical_call]
     step_bytes = sum(per_call) * layers
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    value = whole_job_gbps(step_bytes, world, ms)
     dec_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     achieved = (sum(per_call) * layers) / (sum(dec_ms) * 1e-3) / 1e9
     n_launches = launches[0]
@@ -374,11 +385,11 @@ def run_ours(args, rank, world, local_rank):
             out_host.copy_(out, non_blocking=True)
         t1.record(stream)
         barrier()
-        ms_e2e = max_over_ranks(max(t0.elapsed_time(t1), (time.perf_counter() - w0) * 1e3))
+        ms_e2e = max_over_ranks(max(t0.elapsed_time(t1), (time.perf_counter() - w0) * 1e3), dev)
         e_bytes = sum(decode_bytes(c, H, Hkv, D, out_bytes) - shared_bytes
                       for c in ctx_log) * layers
         h2d = (q.numel() + knew.numel() + vnew.numel()) * 2 + S * (8 + 4 + 4 * width)
-        e2e = {"value": round(e_bytes * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(whole_job_gbps(e_bytes, world, ms_e2e), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2)}
 
     peak, peak_kind = load_peaks()
