@@ -422,6 +422,68 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ---------------------------------------------------------------- swap measurement
+
+def run_swap(args):
+    """swap_blocks bandwidth: the whole opt13b batch's blocks (one layer's pool)
+    out to a pinned host pool and back into other device blocks, against
+    contiguous cudaMemcpyAsync copies of the same number of bytes."""
+    import torch
+    import paged_kv_cache_118_gb300 as pk
+    import workloads as wl
+    batch = make_workload("opt13b", args.seed)
+    B, Hkv, D = batch.block_size, batch.num_kv_heads, batch.head_size
+    L0 = batch.context_lens.astype(np.int64)
+    demand = int(np.sum(-(-L0 // B)))
+    n = 2 * demand + 8
+    bm = pk.BlockManager(n, B, wl.free_order(n, args.seed))
+    for s in range(batch.num_seqs):
+        bm.allocate(s, int(L0[s]))
+    dev = torch.device("cuda")
+    kc = torch.empty((n, B, Hkv, D), dtype=torch.float16, device=dev)
+    vc = torch.empty_like(kc)
+    kc.view(torch.int16).random_(-30000, 30000)
+    vc.view(torch.int16).random_(-30000, 30000)
+    hk = torch.empty((demand + 8, B, Hkv, D), dtype=torch.float16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    cpu = pk.BlockManager(demand + 8, B, wl.free_order(demand + 8, args.seed + 1))
+    seqs = list(range(batch.num_seqs))
+    out_pairs = bm.swap(seqs, cpu)
+    in_pairs = cpu.swap(seqs, bm)              # bookkeeping only: the timed copies repeat
+    nbytes = 2 * len(out_pairs) * kc[0].numel() * 2
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(3, args.steps // 4)
+    t_out = timed(lambda: pk.pkv_swap_blocks(hk, hv, kc, vc, out_pairs), reps)
+    t_in = timed(lambda: pk.pkv_swap_blocks(kc, vc, hk, hv, in_pairs), reps)
+    flat_d = kc.view(-1)[: nbytes // 4]
+    flat_h = hk.view(-1)[: nbytes // 4]
+    t_d2h = timed(lambda: (flat_h.copy_(flat_d, non_blocking=True),
+                           hv.view(-1)[: nbytes // 4].copy_(vc.view(-1)[: nbytes // 4],
+                                                            non_blocking=True)), reps)
+    t_h2d = timed(lambda: (flat_d.copy_(flat_h, non_blocking=True),
+                           vc.view(-1)[: nbytes // 4].copy_(hv.view(-1)[: nbytes // 4],
+                                                            non_blocking=True)), reps)
+    gbs = lambda t: round(nbytes / (t * 1e-3) / 1e9, 1)
+    return {"op": "swap_blocks", "metric": "swap GB/s (blocks copied per second)",
+            "unit": "GB/s", "bytes_per_swap": nbytes, "pairs": int(len(out_pairs)),
+            "swap_out": gbs(t_out), "swap_in": gbs(t_in),
+            "memcpy_d2h_same_bytes": gbs(t_d2h), "memcpy_h2d_same_bytes": gbs(t_h2d),
+            "frac_of_memcpy": {"out": round(t_d2h / t_out, 3), "in": round(t_h2d / t_in, 3)},
+            "config": {"workload": "opt13b one layer", "block_size": B,
+                       "block_bytes_k_plus_v": 2 * kc[0].numel() * 2}}
+
+
 # ---------------------------------------------------------------- oracle (CPU) arm
 
 def _oracle_worker(args):
@@ -506,10 +568,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+                    help="decode: the headline measurement; swap: swap_blocks bandwidth")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local_rank = dist_env()
+
+    if args.op == "swap":
+        if rank == 0:
+            print(json.dumps(run_swap(args)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank == 0:

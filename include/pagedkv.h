@@ -187,6 +187,28 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_
                            int num_pairs, int num_blocks, size_t block_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * swap_blocks: copies between two block pools, one of which is typically in
+ * pinned host memory (swap space).
+ *
+ * Defines ([R] §3 algorithm box: a preempted group's cache is swapped out and
+ * later swapped back in; [D] "Swap 机制"): for every pair i,
+ *     dst_K[dst_i] = src_K[src_i], dst_V[dst_i] = src_V[src_i]   (block_bytes each).
+ *
+ *   src_k, src_v, dst_k, dst_v  device memory, or pinned host memory the GPU can
+ *                  address (cudaHostAlloc / cudaHostRegister); the kernel reads
+ *                  and writes host memory directly over the CPU-GPU link
+ *   src_dst_pairs  HOST int32 [num_pairs][2] = {src, dst}, read before the call returns
+ *   src_blocks, dst_blocks  blocks in the two pools (ids must lie below them)
+ *   block_bytes    as for copy_blocks
+ * Distinct destinations required (PKV_EINVAL); ids out of range give
+ * PKV_ERANGE; a pointer the GPU cannot address gives PKV_EINVAL.
+ * num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                           const int32_t* src_dst_pairs, int num_pairs, int src_blocks,
+                           int dst_blocks, size_t block_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Host block manager: free list, reference counts, fork, copy-on-write.
  *
  * Defines: [D] "分页机制设计" (a free list of block ids; a request takes
@@ -229,6 +251,20 @@ pkv_status pkv_bm_append_slots(pkv_bm* bm, const int64_t* seqs, int n, int64_t* 
 /* Drop seq; blocks whose count reaches zero return to the free list in the
  * sequence's logical order. */
 pkv_status pkv_bm_free(pkv_bm* bm, int64_t seq);
+
+/* Swap: move the sequence group seqs[0..n) from pool src to pool dst (for
+ * instance GPU pool -> CPU pool on preemption and back on resumption; [R] §3
+ * algorithm box, [Z] §3.3 swapped queue, [D] "Swap 机制"). Every distinct
+ * block the group references gets one dst block, in order of first reference;
+ * blocks shared inside the group stay shared; the sequences leave src (blocks
+ * still referenced by other src sequences stay there). pairs[i] = {src block,
+ * dst block} receives the copies to make (pkv_swap_blocks), *num_pairs their
+ * number. All or nothing: PKV_ENOMEM if dst has too few free blocks,
+ * PKV_ERANGE if cap < the number of pairs (*num_pairs still set),
+ * PKV_ESTATE for an unknown, repeated or already-present sequence, PKV_EINVAL
+ * if the block sizes differ. */
+pkv_status pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seqs, int n, int32_t* pairs,
+                       int cap, int* num_pairs);
 
 /* Queries. */
 int pkv_bm_num_free(const pkv_bm* bm);

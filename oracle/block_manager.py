@@ -18,6 +18,15 @@ Sources, in the order the rules are taken from them:
   block; copy a shared tail before writing).
 * tail waste: same review, §2 "块大小决定有多少无法借给别人的尾部空间":
   a sequence of L tokens holds B*ceil(L/B) slots.
+* swapping: same review, §3 algorithm box (when memory runs short, preempt a
+  sequence group and swap its cache out; on resumption swap it back in) and
+  zhy-blog.vercel.app §3.3 (the swapped queue holds requests whose KV blocks
+  moved to CPU memory); "PagedAttention 内存管理深度解析" (deepinsea.top),
+  "Swap 机制" (a CPU swap space of blocks). A swap moves a group of sequences
+  from one pool's manager to another's: every distinct block they reference is
+  given one block in the destination (blocks shared inside the group stay
+  shared), the sequences leave the source, and the (source, destination) block
+  pairs to copy come back in order of first reference.
 
 Readings (listed in the design notes): when several sequences share a tail and
 append in turn, each writer that still sees a count above one takes a copy;
@@ -144,6 +153,40 @@ class BlockManager:
                 self.free.append(b)
         del self.tables[seq]
         del self.lens[seq]
+
+    def swap(self, seqs, dst: "BlockManager"):
+        """Move ``seqs`` (a sequence group) from this pool to ``dst``.
+
+        All or nothing: raises OutOfBlocks (nothing changed) if ``dst`` has
+        fewer free blocks than the group references distinct blocks. Returns
+        the (source block, destination block) pairs to copy.
+        """
+        seqs = [int(x) for x in seqs]
+        if len(set(seqs)) != len(seqs):
+            raise BlockManagerStateError("a sequence appears twice in the group")
+        for x in seqs:
+            self._known(x)
+            if x in dst.tables:
+                raise BlockManagerStateError(f"sequence {x} already in the destination pool")
+        if dst.block_size != self.block_size:
+            raise ValueError("pools differ in block size")
+        distinct = []
+        for x in seqs:
+            for b in self.tables[x]:
+                if b not in distinct:
+                    distinct.append(b)
+        if len(distinct) > len(dst.free):
+            raise OutOfBlocks(f"need {len(distinct)} blocks, {len(dst.free)} free")
+        mapping = {b: dst.free.pop() for b in distinct}
+        for x in seqs:
+            table = [mapping[b] for b in self.tables[x]]
+            for b in table:
+                dst.ref[b] += 1
+            dst.tables[x] = table
+            dst.lens[x] = self.lens[x]
+        for x in seqs:
+            self.free_seq(x)
+        return [(b, mapping[b]) for b in distinct]
 
     # -- helpers ---------------------------------------------------------
     def padded_tables(self, seqs, width: int | None = None):

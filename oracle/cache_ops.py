@@ -12,7 +12,11 @@
   "共享与写时复制" and "一次分叉什么时候真的要复制缓存块"; "vLLM 推理引擎"
   gitcode.csdn.net overview of Copy-on-Write).
 
-Both are bitwise copies, written as plain loops.
+* swap_blocks — the copies of a swap: block src of one pool (K and V) becomes
+  block dst of another pool ("079｜vLLM 与 PagedAttention" §3 algorithm box;
+  "PagedAttention 内存管理深度解析", "Swap 机制").
+
+All are bitwise copies, written as plain loops.
 """
 
 import numpy as np
@@ -50,3 +54,15 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
     for src, dst in pairs:
         k_cache[dst] = snapshot_k[src]
         v_cache[dst] = snapshot_v[src]
+
+
+def swap_blocks(src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray, dst_v: np.ndarray,
+                pairs) -> None:
+    """In place: dst pool block d becomes a copy of src pool block s for each
+    (s, d). Destinations must be distinct."""
+    pairs = [(int(s), int(d)) for s, d in pairs]
+    if len({d for _, d in pairs}) != len(pairs):
+        raise ValueError("swap destinations repeat")
+    for s, d in pairs:
+        dst_k[d] = src_k[s]
+        dst_v[d] = src_v[s]

@@ -43,6 +43,8 @@ SIGNATURES = {
     "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _vp, _vp]),
     "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_sz, _vp]),
+    "pkv_swap_blocks": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_sz, _vp]),
+    "pkv_bm_swap": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _c_int, _vp]),
     "pkv_bm_create": (_vp, [_c_int, _c_int, _vp]),
     "pkv_bm_destroy": (None, [_vp]),
     "pkv_bm_allocate": (_c_int, [_vp, _c_i64, _c_i64]),
@@ -189,6 +191,22 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
     _check(st, "pkv_copy_blocks")
 
 
+def pkv_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor,
+                    src_v: torch.Tensor, src_dst_pairs, stream=None) -> None:
+    """dst pool block d = src pool block s for each (s, d); either pool may be a
+    pinned host tensor (swap space)."""
+    import numpy as np
+    for t in (dst_k, dst_v, src_k, src_v):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("swap pools must be CUDA tensors or pinned host tensors")
+    pairs = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int32).reshape(-1, 2))
+    block_bytes = src_k[0].numel() * src_k.element_size()
+    st = lib.pkv_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v),
+                             pairs.ctypes.data, pairs.shape[0], src_k.shape[0], dst_k.shape[0],
+                             block_bytes, _stream(stream))
+    _check(st, "pkv_swap_blocks")
+
+
 # ---------------------------------------------------------------- block manager
 
 class BlockManager:
@@ -240,6 +258,24 @@ class BlockManager:
 
     def free_seq(self, seq: int) -> None:
         _check(lib.pkv_bm_free(self._h, seq), "pkv_bm_free")
+
+    def swap(self, seqs, dst: "BlockManager"):
+        """Move a sequence group to another pool's manager; returns the
+        (src block, dst block) pairs to copy (int32 [k, 2])."""
+        import numpy as np
+        seqs = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        n = ctypes.c_int()
+        st = lib.pkv_bm_swap(self._h, dst._h, seqs.ctypes.data, seqs.shape[0], None, 0,
+                             ctypes.byref(n))
+        if st == PKV_OK:                      # nothing to copy: the swap is done
+            return np.empty((0, 2), np.int32)
+        if st != PKV_ERANGE:
+            _check(st, "pkv_bm_swap")
+        pairs = np.empty((max(n.value, 1), 2), np.int32)
+        _check(lib.pkv_bm_swap(self._h, dst._h, seqs.ctypes.data, seqs.shape[0],
+                               pairs.ctypes.data, pairs.shape[0], ctypes.byref(n)),
+               "pkv_bm_swap")
+        return pairs[:n.value]
 
     def num_free(self) -> int:
         return int(lib.pkv_bm_num_free(self._h))

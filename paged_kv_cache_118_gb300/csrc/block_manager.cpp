@@ -192,6 +192,46 @@ pkv_status pkv_bm_free(pkv_bm* bm, int64_t seq) {
   return PKV_OK;
 }
 
+pkv_status pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seqs, int n, int32_t* pairs,
+                       int cap, int* num_pairs) {
+  if (src == nullptr || dst == nullptr || src == dst || n < 0 || num_pairs == nullptr ||
+      (n > 0 && seqs == nullptr) || src->block_size != dst->block_size)
+    return PKV_EINVAL;
+  // Validate the group, then count its distinct blocks in order of first reference.
+  std::unordered_map<int64_t, int> seen_seq;
+  for (int i = 0; i < n; ++i) {
+    if (!src->seqs.count(seqs[i]) || dst->seqs.count(seqs[i]) || seen_seq.count(seqs[i]))
+      return PKV_ESTATE;
+    seen_seq[seqs[i]] = i;
+  }
+  std::vector<int32_t> distinct;
+  std::unordered_map<int32_t, int32_t> mapping;
+  for (int i = 0; i < n; ++i)
+    for (int32_t b : src->seqs[seqs[i]].table)
+      if (mapping.emplace(b, -1).second) distinct.push_back(b);
+  *num_pairs = static_cast<int>(distinct.size());
+  if (static_cast<int64_t>(distinct.size()) > cap || (cap > 0 && pairs == nullptr)) return PKV_ERANGE;
+  if (distinct.size() > dst->free_list.size()) return PKV_ENOMEM;
+  for (size_t i = 0; i < distinct.size(); ++i) {
+    int32_t d = dst->free_list.back();
+    dst->free_list.pop_back();
+    dst->ref[d] = 0;
+    mapping[distinct[i]] = d;
+    pairs[2 * i] = distinct[i];
+    pairs[2 * i + 1] = d;
+  }
+  for (int i = 0; i < n; ++i) {
+    Sequence moved = src->seqs[seqs[i]];
+    for (int32_t& b : moved.table) {
+      b = mapping[b];
+      dst->ref[b] += 1;
+    }
+    dst->seqs.emplace(seqs[i], std::move(moved));
+  }
+  for (int i = 0; i < n; ++i) pkv_bm_free(src, seqs[i]);
+  return PKV_OK;
+}
+
 int pkv_bm_num_free(const pkv_bm* bm) {
   return bm ? static_cast<int>(bm->free_list.size()) : -1;
 }

@@ -120,3 +120,61 @@ def test_error_statuses():
     with pytest.raises(pk.PagedKVError) as e:
         bm.fill_tables([1], 1)
     assert e.value.status == pk.PKV_ERANGE
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_swap_matches_oracle(seed):
+    rng = random.Random(100 + seed)
+    B = rng.choice([2, 4, 16])
+    N, M = 60, 40
+    og, oc = free_order(N, seed), free_order(M, seed + 7)
+    gpu, cpu = pk.BlockManager(N, B, og), pk.BlockManager(M, B, oc)
+    rg, rc = RefBM(N, B, og), RefBM(M, B, oc)
+    nxt = 0
+    groups = []
+    for _ in range(5):                      # beam groups sharing a partial prefix
+        lead, L = nxt, rng.randint(0, 3 * B)
+        for m in (gpu, rg):
+            m.allocate(lead, L)
+        members = [lead]
+        for j in range(rng.randint(0, 3)):
+            for m in (gpu, rg):
+                m.fork(lead, nxt + 1 + j)
+            members.append(nxt + 1 + j)
+        for s in members:
+            if rng.random() < 0.7:
+                assert gpu.append_slot(s) == rg.append_slot(s)
+        nxt += len(members)
+        groups.append(members)
+    for g in groups:                          # out, then back in, comparing each time
+        for (src, dst, rs, rd) in ((gpu, cpu, rg, rc), (cpu, gpu, rc, rg)):
+            try:
+                want = rs.swap(g, rd)
+            except OutOfBlocks:
+                with pytest.raises(pk.PagedKVError) as e:
+                    src.swap(g, dst)
+                assert e.value.status == pk.PKV_ENOMEM
+                continue
+            got = src.swap(g, dst)
+            assert [tuple(p) for p in got] == want
+            live_src = [s for gg in groups for s in gg if s in rs.tables]
+            live_dst = [s for gg in groups for s in gg if s in rd.tables]
+            same_state(src, rs, live_src)
+            same_state(dst, rd, live_dst)
+
+
+def test_swap_errors():
+    a, b, c = pk.BlockManager(8, 4), pk.BlockManager(2, 4), pk.BlockManager(8, 8)
+    a.allocate(0, 12)
+    with pytest.raises(pk.PagedKVError) as e:
+        a.swap([0], b)
+    assert e.value.status == pk.PKV_ENOMEM
+    assert a.num_free() == 5 and b.num_free() == 2
+    with pytest.raises(pk.PagedKVError) as e:
+        a.swap([0], c)
+    assert e.value.status == pk.PKV_EINVAL
+    with pytest.raises(pk.PagedKVError) as e:
+        a.swap([7], b)
+    assert e.value.status == pk.PKV_ESTATE
+    a.allocate(1, 0)                          # empty table: nothing to copy
+    assert len(a.swap([1], b)) == 0 and b.length(1) == 0

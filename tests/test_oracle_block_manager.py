@@ -197,3 +197,42 @@ def test_pool_bytes_follow_the_kv_size_formula():
     for (N, B, Hkv, d) in [(64, 4, 4, 64), (10, 16, 40, 128), (3, 128, 8, 128)]:
         kc, vc = empty_pool(N, B, Hkv, d, 0x7E00)
         assert kc.nbytes + vc.nbytes == 2 * 1 * (N * B) * Hkv * d * 2
+
+
+def test_swap_moves_a_group_and_keeps_sharing():
+    """Swap out a beam group (4 sequences sharing a prefix): each distinct block
+    gets one destination block, sharing is kept, the source blocks return to
+    the source free list only when nothing references them."""
+    gpu, cpu = BlockManager(32, 4), BlockManager(16, 4)
+    gpu.allocate(0, 10)                                 # 3 blocks, tail holds 2
+    for b in (1, 2, 3):
+        gpu.fork(0, b)
+    for b in range(4):
+        gpu.append_slot(b)                              # 3 copy-on-write tails + 1 in place
+    gpu.allocate(9, 5)                                  # bystander
+    before = {s: gpu.table(s) for s in range(4)}
+    distinct = sorted({b for t in before.values() for b in t})
+    pairs = gpu.swap([0, 1, 2, 3], cpu)
+    assert sorted(p[0] for p in pairs) == distinct
+    assert len({p[1] for p in pairs}) == len(pairs) == 2 + 4  # shared prefix blocks once
+    m = dict(pairs)
+    for s in range(4):
+        assert cpu.table(s) == [m[b] for b in before[s]]
+        assert cpu.length(s) == 11
+    assert cpu.ref[m[before[0][0]]] == 4                # shared prefix block
+    assert gpu.num_free() == 32 - 2                     # only the bystander remains
+    back = cpu.swap([0, 1, 2, 3], gpu)
+    assert len(back) == len(pairs) and cpu.num_free() == 16
+    for s in range(4):
+        assert len(gpu.table(s)) == 3
+
+
+def test_swap_is_all_or_nothing():
+    gpu, cpu = BlockManager(16, 4), BlockManager(2, 4)
+    gpu.allocate(0, 12)
+    snap = (list(gpu.free), list(gpu.ref), list(cpu.free))
+    with pytest.raises(OutOfBlocks):
+        gpu.swap([0], cpu)
+    assert snap == (list(gpu.free), list(gpu.ref), list(cpu.free))
+    with pytest.raises(BlockManagerStateError):
+        gpu.swap([0, 0], cpu)

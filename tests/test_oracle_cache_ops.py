@@ -61,3 +61,17 @@ def test_copy_blocks_copies_named_blocks_only():
         copy_blocks(kc, vc, [(1, 2), (2, 3)])
     with pytest.raises(ValueError):
         copy_blocks(kc, vc, [(1, 2), (3, 2)])
+
+
+def test_swap_blocks_copies_between_pools():
+    from oracle.cache_ops import swap_blocks
+    rng = np.random.default_rng(2)
+    gk = rng.integers(0, 1 << 16, (8, 4, 2, 8), dtype=np.uint16)
+    gv = rng.integers(0, 1 << 16, (8, 4, 2, 8), dtype=np.uint16)
+    hk = np.zeros((5, 4, 2, 8), np.uint16)
+    hv = np.zeros_like(hk)
+    swap_blocks(gk, gv, hk, hv, [(7, 0), (2, 4)])
+    assert np.array_equal(hk[0], gk[7]) and np.array_equal(hv[4], gv[2])
+    assert not hk[1:4].any()
+    with pytest.raises(ValueError):
+        swap_blocks(gk, gv, hk, hv, [(1, 2), (3, 2)])
