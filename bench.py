@@ -484,6 +484,50 @@ def run_swap(args):
                        "block_bytes_k_plus_v": 2 * kc[0].numel() * 2}}
 
 
+# ---------------------------------------------------------------- host block manager
+
+def run_blockmgr(args):
+    """Host costs of the block manager's per-iteration work (the library's C++
+    through its C ABI; microseconds per call, median of repeats)."""
+    import paged_kv_cache_118_gb300 as pk
+    import workloads as wl
+    rng = np.random.default_rng(args.seed)
+    lens = wl.opt13b_lengths(64, args.seed)
+    out = {}
+
+    def med(fn, reps=50):
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return round(1e6 * float(np.median(ts)), 2)
+
+    n = 2 * int(np.sum(-(-lens // 16))) + 4096
+    bm = pk.BlockManager(n, 16, wl.free_order(n, args.seed))
+    for s in range(64):
+        bm.allocate(s, int(lens[s]))
+    seqs = np.arange(64, dtype=np.int64)
+    out["append_slots_64_seqs_us"] = med(lambda: bm.append_slots(seqs))
+    width = int(np.max(-(-(lens + 200) // 16)))
+    out["fill_tables_64_seqs_us"] = med(lambda: bm.fill_tables(seqs, width))
+    prompt = rng.integers(0, 32000, 2048).astype(np.int32)
+    pc = pk.BlockManager(8192, 16)
+    ids = iter(range(10 ** 6))
+    out["allocate_prefix_2048_tokens_miss_us"] = med(lambda: pc.allocate_prefix(
+        next(ids), rng.integers(0, 32000, 2048).astype(np.int32)), reps=20)
+    pc.allocate_prefix(next(ids), prompt)
+    out["allocate_prefix_2048_tokens_hit_us"] = med(lambda: pc.allocate_prefix(next(ids), prompt),
+                                                    reps=20)
+    cpu = pk.BlockManager(n, 16)
+    t0 = time.perf_counter()
+    pairs = bm.swap(list(range(32)), cpu)
+    out["swap_32_seqs_bookkeeping_us"] = round(1e6 * (time.perf_counter() - t0), 2)
+    out["swap_32_seqs_pairs"] = int(len(pairs))
+    return {"op": "block_manager", "metric": "host microseconds per call", "unit": "us",
+            "results": out, "config": {"workload": "opt13b lengths, block_size 16"}}
+
+
 # ---------------------------------------------------------------- oracle (CPU) arm
 
 def _oracle_worker(args):
@@ -568,8 +612,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
-                    help="decode: the headline measurement; swap: swap_blocks bandwidth")
+    ap.add_argument("--op", choices=["decode", "swap", "blockmgr"], default="decode",
+                    help="decode: the headline measurement; swap: swap_blocks bandwidth; "
+                         "blockmgr: host costs of the block manager")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -578,6 +623,10 @@ def main():
     if args.op == "swap":
         if rank == 0:
             print(json.dumps(run_swap(args)), flush=True)
+        return
+    if args.op == "blockmgr":
+        if rank == 0:
+            print(json.dumps(run_blockmgr(args)), flush=True)
         return
 
     if args.impl == "reference":

@@ -235,6 +235,23 @@ void pkv_bm_destroy(pkv_bm* bm);
 /* A new sequence holding num_tokens >= 0 tokens (ceil(n/B) blocks, count 1).
  * PKV_ESTATE if seq exists; PKV_ENOMEM (no change) if too few blocks are free. */
 pkv_status pkv_bm_allocate(pkv_bm* bm, int64_t seq, int64_t num_tokens);
+/* Automatic prefix caching ([Z] §2.2(5): every block is kept in a hash table
+ * keyed by its tokens and all the tokens before it; a new request reuses the
+ * cached blocks of its prefix). A new sequence holding the n prompt tokens
+ * token_ids: for each full block j the chained hash h_j = FNV-1a-64(h_{j-1} as
+ * 8 little-endian bytes, then the block's token ids as 4 little-endian bytes
+ * each), h_{-1} = 0, is looked up; the blocks of the longest run of hits from
+ * the start are shared (count + 1), the remaining blocks are fresh and the full
+ * ones among them are registered. *cached_tokens (nullable) receives the
+ * number of leading tokens whose keys/values are already in the pool — the
+ * caller writes only the rest. A registered block whose count drops to zero
+ * keeps its contents and is evictable (oldest first) when the free list runs
+ * out. PKV_ESTATE if seq exists; PKV_ENOMEM (no change) if too few blocks. */
+pkv_status pkv_bm_allocate_prefix(pkv_bm* bm, int64_t seq, const int32_t* token_ids, int64_t n,
+                                  int64_t* cached_tokens);
+/* Number of blocks registered in the prefix cache. */
+int pkv_bm_num_cached(const pkv_bm* bm);
+
 /* child shares all of parent's blocks (each count + 1) and its length. */
 pkv_status pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child);
 /* Room for one more token of seq. *slot receives its slot. If the tail block
@@ -266,7 +283,7 @@ pkv_status pkv_bm_free(pkv_bm* bm, int64_t seq);
 pkv_status pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seqs, int n, int32_t* pairs,
                        int cap, int* num_pairs);
 
-/* Queries. */
+/* Queries. num_free counts the free list and evictable cached blocks. */
 int pkv_bm_num_free(const pkv_bm* bm);
 int pkv_bm_refcount(const pkv_bm* bm, int32_t block); /* -1 if out of range */
 int64_t pkv_bm_length(const pkv_bm* bm, int64_t seq); /* -1 if unknown */
@@ -279,8 +296,9 @@ pkv_status pkv_bm_fill_tables(const pkv_bm* bm, const int64_t* seqs, int n, int3
 /* Slots of positions first .. first+count-1 of seq into out[count]. */
 pkv_status pkv_bm_slots(const pkv_bm* bm, int64_t seq, int64_t first, int64_t count,
                         int64_t* out);
-/* The free list, bottom to top (the next block handed out is the last one);
- * returns its length, writes at most cap entries. */
+/* The free list (without evictable cached blocks), bottom to top (the next
+ * block handed out is the last one); returns its length, writes at most cap
+ * entries. */
 int pkv_bm_free_list(const pkv_bm* bm, int32_t* out, int cap);
 
 #ifdef __cplusplus

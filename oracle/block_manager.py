@@ -28,6 +28,18 @@ Sources, in the order the rules are taken from them:
   shared), the sequences leave the source, and the (source, destination) block
   pairs to copy come back in order of first reference.
 
+* prefix caching: zhy-blog.vercel.app §2.2(5) — every KV block is kept in a
+  hash table keyed by a hash of the block's tokens and all the tokens before
+  it; a new request looks its prefix up and reuses the blocks it finds.
+  Readings: only full blocks of a prompt are registered (a partial tail will
+  be written to and is never shared); reuse stops at the first miss (a later
+  block's KV needs every block before it); a registered block whose count
+  drops to zero stays cached and evictable, least recently freed first, until
+  a fresh allocation finds the free list empty; the hash is 64-bit FNV-1a
+  (offset basis 14695981039346656037, prime 1099511628211, over bytes) of the
+  previous block's hash (8 bytes, little-endian) followed by the block's token
+  ids (4 bytes each, little-endian), the first block's "previous hash" being 0.
+
 Readings (listed in the design notes): when several sequences share a tail and
 append in turn, each writer that still sees a count above one takes a copy;
 the last one (count one) writes in place. Freed blocks go back to the free list
@@ -47,6 +59,31 @@ class BlockManagerStateError(RuntimeError):
     """Unknown or duplicate sequence id, or a bad block id."""
 
 
+FNV_OFFSET = 14695981039346656037
+FNV_PRIME = 1099511628211
+MASK64 = (1 << 64) - 1
+
+
+def fnv1a64(data: bytes, h: int = FNV_OFFSET) -> int:
+    """64-bit FNV-1a: for every byte, xor it in, then multiply by the prime."""
+    for byte in data:
+        h ^= byte
+        h = (h * FNV_PRIME) & MASK64
+    return h
+
+
+def block_hashes(token_ids, block_size: int) -> list[int]:
+    """Chained hashes of the full blocks of a token sequence."""
+    out, prev = [], 0
+    for j in range(len(token_ids) // block_size):
+        data = prev.to_bytes(8, "little") + b"".join(
+            int(t).to_bytes(4, "little", signed=True)
+            for t in token_ids[j * block_size:(j + 1) * block_size])
+        prev = fnv1a64(data)
+        out.append(prev)
+    return out
+
+
 class BlockManager:
     def __init__(self, num_blocks: int, block_size: int, free_order=None):
         if num_blocks < 1 or block_size < 1:
@@ -60,13 +97,27 @@ class BlockManager:
         self.ref = [0] * num_blocks
         self.tables: dict[int, list[int]] = {}
         self.lens: dict[int, int] = {}
+        self.cached: dict[int, int] = {}      # block hash -> block
+        self.hash_of: dict[int, int] = {}     # block -> its registered hash
+        self.evictable: list[int] = []        # cached blocks with count 0, oldest first
 
     # -- queries ---------------------------------------------------------
     def blocks_needed(self, num_tokens: int) -> int:
         return -(-int(num_tokens) // self.block_size)
 
     def num_free(self) -> int:
-        return len(self.free)
+        """Blocks an allocation can take: the free list and evictable cached blocks."""
+        return len(self.free) + len(self.evictable)
+
+    def _take(self) -> int:
+        """A fresh block: from the free list, else the least recently freed cached one."""
+        if self.free:
+            b = self.free.pop()
+        else:
+            b = self.evictable.pop(0)
+            del self.cached[self.hash_of.pop(b)]
+        self.ref[b] = 1
+        return b
 
     def table(self, seq: int) -> list[int]:
         self._known(seq)
@@ -92,11 +143,9 @@ class BlockManager:
         if num_tokens < 0:
             raise ValueError("negative token count")
         need = self.blocks_needed(num_tokens)
-        if need > len(self.free):
-            raise OutOfBlocks(f"need {need} blocks, {len(self.free)} free")
-        ids = [self.free.pop() for _ in range(need)]
-        for b in ids:
-            self.ref[b] = 1
+        if need > self.num_free():
+            raise OutOfBlocks(f"need {need} blocks, {self.num_free()} free")
+        ids = [self._take() for _ in range(need)]
         self.tables[seq] = ids
         self.lens[seq] = int(num_tokens)
         return list(ids)
@@ -123,18 +172,15 @@ class BlockManager:
         t = self.tables[seq]
         cow = None
         if L % self.block_size == 0:              # tail full (or no block yet)
-            if not self.free:
+            if not self.num_free():
                 raise OutOfBlocks("no free block for the next token")
-            b = self.free.pop()
-            self.ref[b] = 1
-            t.append(b)
+            t.append(self._take())
         else:
             tail = t[L // self.block_size]
             if self.ref[tail] > 1:                # shared partial tail: copy on write
-                if not self.free:
+                if not self.num_free():
                     raise OutOfBlocks("no free block for copy-on-write")
-                b = self.free.pop()
-                self.ref[b] = 1
+                b = self._take()
                 self.ref[tail] -= 1
                 t[L // self.block_size] = b
                 cow = (tail, b)
@@ -150,9 +196,45 @@ class BlockManager:
                 raise BlockManagerStateError(f"reference count of block {b} underflows")
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                if b in self.hash_of:
+                    self.evictable.append(b)      # keep its contents for later hits
+                else:
+                    self.free.append(b)
         del self.tables[seq]
         del self.lens[seq]
+
+    def allocate_prefix(self, seq: int, token_ids) -> int:
+        """A new sequence holding the prompt ``token_ids``, reusing cached blocks
+        of the longest cached prefix of full blocks. Returns how many leading
+        tokens already have their keys/values in the cache."""
+        if seq in self.tables:
+            raise BlockManagerStateError(f"sequence {seq} already allocated")
+        n = len(token_ids)
+        hashes = block_hashes(token_ids, self.block_size)
+        hits = []
+        for h in hashes:
+            b = self.cached.get(h)
+            if b is None:
+                break
+            hits.append(b)
+        revived = sum(1 for b in hits if self.ref[b] == 0)
+        fresh = self.blocks_needed(n) - len(hits)
+        if fresh > self.num_free() - revived:
+            raise OutOfBlocks(f"need {fresh} blocks, {self.num_free() - revived} free")
+        for b in hits:
+            if self.ref[b] == 0:
+                self.evictable.remove(b)
+            self.ref[b] += 1
+        table = list(hits)
+        for j in range(len(hits), self.blocks_needed(n)):
+            b = self._take()
+            if j < len(hashes):                   # a full block: registered for later hits
+                self.cached[hashes[j]] = b
+                self.hash_of[b] = hashes[j]
+            table.append(b)
+        self.tables[seq] = table
+        self.lens[seq] = n
+        return len(hits) * self.block_size
 
     def swap(self, seqs, dst: "BlockManager"):
         """Move ``seqs`` (a sequence group) from this pool to ``dst``.
@@ -175,9 +257,12 @@ class BlockManager:
             for b in self.tables[x]:
                 if b not in distinct:
                     distinct.append(b)
-        if len(distinct) > len(dst.free):
-            raise OutOfBlocks(f"need {len(distinct)} blocks, {len(dst.free)} free")
-        mapping = {b: dst.free.pop() for b in distinct}
+        if len(distinct) > dst.num_free():
+            raise OutOfBlocks(f"need {len(distinct)} blocks, {dst.num_free()} free")
+        mapping = {}
+        for b in distinct:
+            mapping[b] = dst._take()
+            dst.ref[mapping[b]] = 0
         for x in seqs:
             table = [mapping[b] for b in self.tables[x]]
             for b in table:

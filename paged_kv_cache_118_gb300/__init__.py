@@ -52,6 +52,8 @@ SIGNATURES = {
     "pkv_bm_append_slot": (_c_int, [_vp, _c_i64, _vp, _vp, _vp]),
     "pkv_bm_append_slots": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp]),
     "pkv_bm_free": (_c_int, [_vp, _c_i64]),
+    "pkv_bm_allocate_prefix": (_c_int, [_vp, _c_i64, _vp, _c_i64, _vp]),
+    "pkv_bm_num_cached": (_c_int, [_vp]),
     "pkv_bm_num_free": (_c_int, [_vp]),
     "pkv_bm_refcount": (_c_int, [_vp, ctypes.c_int32]),
     "pkv_bm_length": (_c_i64, [_vp, _c_i64]),
@@ -234,6 +236,19 @@ class BlockManager:
 
     def allocate(self, seq: int, num_tokens: int) -> None:
         _check(lib.pkv_bm_allocate(self._h, seq, num_tokens), "pkv_bm_allocate")
+
+    def allocate_prefix(self, seq: int, token_ids) -> int:
+        """A new sequence holding the prompt token_ids, sharing cached blocks of
+        its prefix; returns the number of leading tokens already cached."""
+        import numpy as np
+        toks = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int32))
+        cached = ctypes.c_int64()
+        _check(lib.pkv_bm_allocate_prefix(self._h, seq, toks.ctypes.data, toks.shape[0],
+                                          ctypes.byref(cached)), "pkv_bm_allocate_prefix")
+        return cached.value
+
+    def num_cached(self) -> int:
+        return int(lib.pkv_bm_num_cached(self._h))
 
     def fork(self, parent: int, child: int) -> None:
         _check(lib.pkv_bm_fork(self._h, parent, child), "pkv_bm_fork")

@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <list>
 #include <unordered_map>
 #include <vector>
 
@@ -31,16 +32,70 @@ struct pkv_bm {
   std::vector<int32_t> free_list;  // top of the stack is the back
   std::vector<int32_t> ref;
   std::unordered_map<int64_t, Sequence> seqs;
+  // Prefix cache: registered full prompt blocks by chained hash. A registered
+  // block whose count reaches zero keeps its contents and waits, oldest first,
+  // in `evictable` until a fresh allocation finds the free list empty.
+  std::unordered_map<uint64_t, int32_t> cached;
+  std::unordered_map<int32_t, uint64_t> hash_of;
+  std::list<int32_t> evictable;
+  std::unordered_map<int32_t, std::list<int32_t>::iterator> evict_pos;
 
   int64_t blocks_for(int64_t tokens) const { return (tokens + block_size - 1) / block_size; }
+  int64_t available() const {
+    return static_cast<int64_t>(free_list.size() + evictable.size());
+  }
 
+  // A fresh block with count 1: from the free list, else the least recently
+  // freed cached block (which leaves the cache).
   int32_t pop() {
-    int32_t b = free_list.back();
-    free_list.pop_back();
+    int32_t b;
+    if (!free_list.empty()) {
+      b = free_list.back();
+      free_list.pop_back();
+    } else {
+      b = evictable.front();
+      evictable.pop_front();
+      evict_pos.erase(b);
+      cached.erase(hash_of[b]);
+      hash_of.erase(b);
+    }
     ref[b] = 1;
     return b;
   }
+
+  void release(int32_t b) {  // count reached zero
+    if (hash_of.count(b)) {
+      evictable.push_back(b);
+      evict_pos[b] = std::prev(evictable.end());
+    } else {
+      free_list.push_back(b);
+    }
+  }
 };
+
+// 64-bit FNV-1a (offset basis 14695981039346656037, prime 1099511628211).
+static uint64_t fnv1a64(const uint8_t* data, size_t n, uint64_t h) {
+  for (size_t i = 0; i < n; ++i) {
+    h ^= data[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+// Chained hash of one full block: FNV-1a over the previous block's hash (8
+// bytes, little-endian) and the block's token ids (4 bytes each, little-endian).
+static uint64_t block_hash(uint64_t prev, const int32_t* tokens, int block_size) {
+  uint8_t buf[8];
+  for (int i = 0; i < 8; ++i) buf[i] = static_cast<uint8_t>(prev >> (8 * i));
+  uint64_t h = fnv1a64(buf, 8, 14695981039346656037ull);
+  for (int t = 0; t < block_size; ++t) {
+    const uint32_t v = static_cast<uint32_t>(tokens[t]);
+    uint8_t w[4] = {static_cast<uint8_t>(v), static_cast<uint8_t>(v >> 8),
+                    static_cast<uint8_t>(v >> 16), static_cast<uint8_t>(v >> 24)};
+    h = fnv1a64(w, 4, h);
+  }
+  return h;
+}
 
 extern "C" {
 
@@ -74,7 +129,7 @@ pkv_status pkv_bm_allocate(pkv_bm* bm, int64_t seq, int64_t num_tokens) {
   if (bm == nullptr || num_tokens < 0) return PKV_EINVAL;
   if (bm->seqs.count(seq)) return PKV_ESTATE;
   int64_t need = bm->blocks_for(num_tokens);
-  if (need > static_cast<int64_t>(bm->free_list.size())) return PKV_ENOMEM;
+  if (need > bm->available()) return PKV_ENOMEM;
   Sequence s;
   s.len = num_tokens;
   s.table.reserve(need);
@@ -127,7 +182,7 @@ pkv_status pkv_bm_append_slot(pkv_bm* bm, int64_t seq, int64_t* slot, int32_t* c
     return PKV_EINVAL;
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PKV_ESTATE;
-  if (append_needs_block(bm, it->second) && bm->free_list.empty()) return PKV_ENOMEM;
+  if (append_needs_block(bm, it->second) && bm->available() == 0) return PKV_ENOMEM;
   append_one(bm, it->second, slot, cow_src, cow_dst);
   return PKV_OK;
 }
@@ -163,7 +218,7 @@ pkv_status pkv_bm_append_slots(pkv_bm* bm, const int64_t* seqs, int n, int64_t* 
     }
     len[seqs[i]] = L + 1;
   }
-  if (need > static_cast<int64_t>(bm->free_list.size())) return PKV_ENOMEM;
+  if (need > bm->available()) return PKV_ENOMEM;
   int k = 0;
   for (int i = 0; i < n; ++i) {
     int32_t src, dst;
@@ -186,10 +241,56 @@ pkv_status pkv_bm_free(pkv_bm* bm, int64_t seq) {
     if (bm->ref[b] < 1) return PKV_ESTATE;  // would underflow; leave state as is
   for (int32_t b : it->second.table) {
     bm->ref[b] -= 1;
-    if (bm->ref[b] == 0) bm->free_list.push_back(b);
+    if (bm->ref[b] == 0) bm->release(b);
   }
   bm->seqs.erase(it);
   return PKV_OK;
+}
+
+pkv_status pkv_bm_allocate_prefix(pkv_bm* bm, int64_t seq, const int32_t* token_ids, int64_t n,
+                                  int64_t* cached_tokens) {
+  if (bm == nullptr || n < 0 || (n > 0 && token_ids == nullptr)) return PKV_EINVAL;
+  if (bm->seqs.count(seq)) return PKV_ESTATE;
+  const int B = bm->block_size;
+  const int64_t full = n / B;
+  std::vector<uint64_t> hashes(full);
+  uint64_t prev = 0;
+  for (int64_t j = 0; j < full; ++j) prev = hashes[j] = block_hash(prev, token_ids + j * B, B);
+  std::vector<int32_t> hits;
+  for (int64_t j = 0; j < full; ++j) {
+    auto c = bm->cached.find(hashes[j]);
+    if (c == bm->cached.end()) break;       // a later block needs every block before it
+    hits.push_back(c->second);
+  }
+  int64_t revived = 0;
+  for (int32_t b : hits) revived += bm->ref[b] == 0;
+  const int64_t fresh = bm->blocks_for(n) - static_cast<int64_t>(hits.size());
+  if (fresh > bm->available() - revived) return PKV_ENOMEM;
+  for (int32_t b : hits) {
+    if (bm->ref[b] == 0) {
+      bm->evictable.erase(bm->evict_pos[b]);
+      bm->evict_pos.erase(b);
+    }
+    bm->ref[b] += 1;
+  }
+  Sequence s;
+  s.len = n;
+  s.table = hits;
+  for (int64_t j = static_cast<int64_t>(hits.size()); j < bm->blocks_for(n); ++j) {
+    const int32_t b = bm->pop();
+    if (j < full) {                          // full prompt block: registered for later hits
+      bm->cached[hashes[j]] = b;
+      bm->hash_of[b] = hashes[j];
+    }
+    s.table.push_back(b);
+  }
+  bm->seqs.emplace(seq, std::move(s));
+  if (cached_tokens) *cached_tokens = static_cast<int64_t>(hits.size()) * B;
+  return PKV_OK;
+}
+
+int pkv_bm_num_cached(const pkv_bm* bm) {
+  return bm ? static_cast<int>(bm->cached.size()) : -1;
 }
 
 pkv_status pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seqs, int n, int32_t* pairs,
@@ -211,10 +312,9 @@ pkv_status pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seqs, int n, int
       if (mapping.emplace(b, -1).second) distinct.push_back(b);
   *num_pairs = static_cast<int>(distinct.size());
   if (static_cast<int64_t>(distinct.size()) > cap || (cap > 0 && pairs == nullptr)) return PKV_ERANGE;
-  if (distinct.size() > dst->free_list.size()) return PKV_ENOMEM;
+  if (static_cast<int64_t>(distinct.size()) > dst->available()) return PKV_ENOMEM;
   for (size_t i = 0; i < distinct.size(); ++i) {
-    int32_t d = dst->free_list.back();
-    dst->free_list.pop_back();
+    int32_t d = dst->pop();
     dst->ref[d] = 0;
     mapping[distinct[i]] = d;
     pairs[2 * i] = distinct[i];
@@ -233,7 +333,7 @@ pkv_status pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seqs, int n, int
 }
 
 int pkv_bm_num_free(const pkv_bm* bm) {
-  return bm ? static_cast<int>(bm->free_list.size()) : -1;
+  return bm ? static_cast<int>(bm->available()) : -1;
 }
 
 int pkv_bm_refcount(const pkv_bm* bm, int32_t block) {

@@ -178,3 +178,45 @@ def test_swap_errors():
     assert e.value.status == pk.PKV_ESTATE
     a.allocate(1, 0)                          # empty table: nothing to copy
     assert len(a.swap([1], b)) == 0 and b.length(1) == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefix_cache_matches_oracle(seed):
+    rng = random.Random(300 + seed)
+    N, B = rng.randint(20, 60), rng.choice([2, 4, 8])
+    order = free_order(N, seed)
+    bm, ref = pk.BlockManager(N, B, order), RefBM(N, B, order)
+    prompts = [[rng.randint(0, 3) for _ in range(rng.randint(0, 4 * B))] for _ in range(6)]
+    live, nxt = [], 0
+    for _ in range(150):
+        op = rng.random()
+        if op < 0.45 or not live:
+            base = rng.choice(prompts)
+            toks = base[:rng.randint(0, len(base))] + [rng.randint(0, 3) for _ in range(rng.randint(0, B))]
+            try:
+                want = ref.allocate_prefix(nxt, toks)
+            except OutOfBlocks:
+                with pytest.raises(pk.PagedKVError) as e:
+                    bm.allocate_prefix(nxt, toks)
+                assert e.value.status == pk.PKV_ENOMEM
+            else:
+                assert bm.allocate_prefix(nxt, toks) == want
+                live.append(nxt)
+            nxt += 1
+        elif op < 0.6:
+            s = rng.choice(live)
+            try:
+                want = ref.append_slot(s)
+            except OutOfBlocks:
+                with pytest.raises(pk.PagedKVError):
+                    bm.append_slot(s)
+            else:
+                assert bm.append_slot(s) == want
+        elif op < 0.7:
+            p = rng.choice(live)
+            ref.fork(p, nxt); bm.fork(p, nxt); live.append(nxt); nxt += 1
+        else:
+            s = rng.choice(live)
+            ref.free_seq(s); bm.free_seq(s); live.remove(s)
+        same_state(bm, ref, live)
+        assert bm.num_cached() == len(ref.cached)

@@ -236,3 +236,40 @@ def test_swap_is_all_or_nothing():
     assert snap == (list(gpu.free), list(gpu.ref), list(cpu.free))
     with pytest.raises(BlockManagerStateError):
         gpu.swap([0, 0], cpu)
+
+
+def test_fnv1a64_published_vectors():
+    from oracle.block_manager import fnv1a64
+    assert fnv1a64(b"") == 0xcbf29ce484222325
+    assert fnv1a64(b"a") == 0xaf63dc4c8601ec8c
+    assert fnv1a64(b"foobar") == 0x85944171f73967e8
+
+
+def test_prefix_cache_reuses_full_prompt_blocks():
+    bm = BlockManager(32, 4)
+    prompt = list(range(100, 111))                    # 11 tokens: 2 full blocks + 3
+    assert bm.allocate_prefix(0, prompt) == 0         # nothing cached yet
+    assert bm.allocate_prefix(1, prompt) == 8         # both full blocks reused
+    assert bm.table(1)[:2] == bm.table(0)[:2] and bm.table(1)[2] != bm.table(0)[2]
+    assert bm.ref[bm.table(0)[0]] == 2 and bm.ref[bm.table(0)[2]] == 1
+    # same second-block tokens after a different first block: no hit (chained hash)
+    other = [7, 7, 7, 7] + prompt[4:8]
+    assert bm.allocate_prefix(2, other) == 0
+    assert bm.table(2)[1] != bm.table(0)[1]
+    # a prompt sharing only the first block
+    assert bm.allocate_prefix(3, prompt[:4] + [1, 2, 3, 4, 5]) == 4
+
+
+def test_prefix_cache_keeps_freed_blocks_until_evicted():
+    bm = BlockManager(6, 4)
+    a = [1, 2, 3, 4, 5, 6, 7, 8]                     # 2 full blocks
+    bm.allocate_prefix(0, a)
+    bm.free_seq(0)
+    assert bm.num_free() == 6 and len(bm.free) == 4 and len(bm.evictable) == 2
+    assert bm.allocate_prefix(1, a) == 8              # revived from the cache
+    bm.free_seq(1)
+    bm.allocate(2, 16)                                # takes the 4 free blocks ...
+    bm.allocate(3, 4)                                 # ... then evicts the oldest cached one
+    assert len(bm.evictable) == 1 and len(bm.cached) == 1
+    bm.free_seq(3)
+    assert bm.allocate_prefix(4, a) == 0              # the chain is broken at block 0
