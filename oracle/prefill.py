@@ -24,6 +24,12 @@ from .attention import gather_sequence, kv_head_of, softmax_weights
 from .formats import decode_bits
 
 
+def causal_visibility(context_len: int, chunk: int) -> np.ndarray:
+    """[C, L] booleans: query i (position L - C + i) sees key positions <= its own."""
+    pos = context_len - chunk + np.arange(chunk)
+    return np.arange(context_len)[None, :] <= pos[:, None]
+
+
 def prefill_sequence(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                      table_row: np.ndarray, context_len: int, block_size: int, scale: float,
                      dtype: str) -> np.ndarray:
@@ -37,8 +43,7 @@ def prefill_sequence(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarra
     V = decode_bits(gather_sequence(v_cache, table_row, L, block_size), dtype)
     Q = decode_bits(q_bits, dtype)
     s64 = float(np.float32(scale))
-    pos = L - C + np.arange(C)
-    visible = np.arange(L)[None, :] <= pos[:, None]             # [C, L] causal mask
+    visible = causal_visibility(L, C)                          # [C, L]
     out = np.empty(Q.shape, dtype=np.float64)
     for h in range(H):
         g = kv_head_of(h, H, Hkv)

@@ -79,13 +79,9 @@ def test_planted_mistake_no_causal_mask_is_caught(monkeypatch):
     L = 40
     batch, st = _state((L,), 4, 2, 64, 8, "f16", 5)
     q = normal_bits(np.random.default_rng(1), (10, 4, 64), "f16")
-    real = np.arange(L)
-    monkeypatch.setattr(pf.np, "arange", lambda n, *a, **k: real if n == L else np.arange(n, *a, **k))
-    orig_where = np.where
-    monkeypatch.setattr(pf.np, "where", lambda c, x, y: x)          # drop the mask
+    monkeypatch.setattr(pf, "causal_visibility", lambda L_, C_: np.ones((C_, L_), bool))
     got = pf.prefill_sequence(q, st["k_cache"], st["v_cache"], st["block_tables"][0], L, 8,
                               batch.scale, "f16")
-    monkeypatch.setattr(pf.np, "where", orig_where)
     pos = L - 10 + np.arange(10)
     mask = np.arange(L)[None, :] <= pos[:, None]
     want = _sdpa(q, batch.k_tokens, batch.v_tokens, "f16", float(batch.scale), mask)
