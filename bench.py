@@ -484,6 +484,62 @@ def run_swap(args):
                        "block_bytes_k_plus_v": 2 * kc[0].numel() * 2}}
 
 
+# ---------------------------------------------------------------- chunked prefill
+
+def run_prefill(args):
+    """Chunked-prefill attention throughput: 16 LLaMA-13B-shaped sequences
+    (40 heads, d = 128, fp16, B = 16) whose last 512 tokens of a 2k..4k-token
+    context form the query chunk. FLOPs are the causal ones: 4 d H per (query,
+    visible key) pair."""
+    import torch
+    import paged_kv_cache_118_gb300 as pk
+    import workloads as wl
+    from paged_kv_cache_118_gb300.cache import PagedKVCache
+    rng = np.random.default_rng(args.seed)
+    S, H, Hkv, D, B, C = 16, 40, 40, 128, 16, 512
+    lens = rng.integers(2048, 4096, size=S, endpoint=True).astype(np.int64)
+    n = int(np.sum(-(-lens // B))) + 8
+    cache = PagedKVCache(n, B, Hkv, D, torch.float16, free_order=wl.free_order(n, args.seed),
+                         poison=False)
+    k = torch.randn(int(lens.sum()), Hkv, D, dtype=torch.float16, device="cuda")
+    v = torch.randn_like(k)
+    cache.prefill(range(S), lens, k, v)
+    del k, v
+    tables, ctx = cache.tables(range(S))
+    starts = torch.arange(0, (S + 1) * C, C, dtype=torch.int32, device="cuda")
+    q = torch.randn(S * C, H, D, dtype=torch.float16, device="cuda")
+    out = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(D)
+    visible = sum(int(np.sum(L - C + np.arange(C) + 1)) for L in lens)
+    flops = 4 * D * H * visible
+    call = lambda: pk.pkv_paged_attention_prefill(out, q, cache.k_cache, cache.v_cache, tables,
+                                                  ctx, starts, C, B, scale, cache.err)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(5, args.steps)
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    assert cache.err.item() == 0
+    tflops = flops / (ms * 1e-3) / 1e12
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1900.0}
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    return {"op": "prefill", "metric": "chunked-prefill attention TFLOP/s", "unit": "TFLOP/s",
+            "value": round(tflops, 1), "ms": round(ms, 4),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "peak_source": "measured bf16 dense GEMM (fp16 runs at the same rate)"},
+            "config": {"workload": "llama13b-shaped chunked prefill", "num_seqs": S,
+                       "chunk": C, "context": "U[2048, 4096]", "num_heads": H,
+                       "num_kv_heads": Hkv, "head_size": D, "block_size": B, "dtype": "f16"}}
+
+
 # ---------------------------------------------------------------- host block manager
 
 def run_blockmgr(args):
@@ -612,7 +668,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--op", choices=["decode", "swap", "blockmgr"], default="decode",
+    ap.add_argument("--op", choices=["decode", "swap", "blockmgr", "prefill"], default="decode",
                     help="decode: the headline measurement; swap: swap_blocks bandwidth; "
                          "blockmgr: host costs of the block manager")
     args = ap.parse_args()
@@ -623,6 +679,10 @@ def main():
     if args.op == "swap":
         if rank == 0:
             print(json.dumps(run_swap(args)), flush=True)
+        return
+    if args.op == "prefill":
+        if rank == 0:
+            print(json.dumps(run_prefill(args)), flush=True)
         return
     if args.op == "blockmgr":
         if rank == 0:

@@ -144,6 +144,38 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, int out_dtype, const vo
                                               void* stream);
 
 /* ------------------------------------------------------------------------
+ * Chunked prefill attention over the paged cache.
+ *
+ * Defines ([Z] §4 chunked prefill: a long prompt is processed in chunks whose
+ * attention masks follow their position in the prompt, each attending to the
+ * cache the earlier chunks left; [R] §2 for the one global denominator):
+ * sequence s holds L = context_lens[s] tokens, the last C of which are its
+ * query chunk, rows query_start[s] .. query_start[s+1]-1 of q; query i
+ * (position L - C + i) attends over positions 0 .. L - C + i:
+ *     o_i = sum_{u <= L-C+i} exp(scale * q_i.k_u) v_u / sum_{u <= L-C+i} exp(scale * q_i.k_u).
+ * The chunk's keys and values must already be in the cache (reshape_and_cache).
+ * C = 1 is a decode step; C = 0 leaves the sequence out.
+ *
+ *   out, q        device, [total_queries][num_heads][head_size] (out_dtype / kv_dtype)
+ *   caches, tables, context_lens  as for pkv_paged_attention_decode
+ *   query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
+ *   max_query_len host int >= every C (sizes the grid)
+ *   head_size 64 or 128; block_size a power of two from 8 to 256;
+ *   64 % (num_heads / num_kv_heads) == 0
+ * Device checks: 0 <= C <= min(L, max_query_len) and L <= max_blocks_per_seq *
+ * block_size, else the sequence is skipped (its rows untouched) and
+ * PKV_DEVERR_CONTEXT set; bad block ids as for decode. Needs no workspace.
+ * Errors: PKV_EINVAL, PKV_ECUDA.
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_paged_attention_prefill(void* out, int out_dtype, const void* q,
+                                       const void* k_cache, const void* v_cache, int kv_dtype,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       const int32_t* query_start, int num_seqs, int num_heads,
+                                       int num_kv_heads, int head_size, int num_blocks,
+                                       int block_size, int max_blocks_per_seq, int max_query_len,
+                                       float scale, int32_t* err_flag, void* stream);
+
+/* ------------------------------------------------------------------------
  * reshape_and_cache: write new tokens' keys and values into their slots.
  *
  * Defines ([R] §2 "共享与写时复制" and the §3 per-iteration algorithm box: the

@@ -40,6 +40,9 @@ SIGNATURES = {
     "pkv_paged_attention_decode_noalloc": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp,
                                                     _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                     _c_int, _c_int, _c_f, _c_int, _vp, _vp]),
+    "pkv_paged_attention_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _vp,
+                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                             _c_int, _c_int, _c_f, _vp, _vp]),
     "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _vp, _vp]),
     "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_sz, _vp]),
@@ -164,6 +167,25 @@ def pkv_paged_attention_decode_noalloc(out: torch.Tensor, q: torch.Tensor,
         _ptr(block_tables), _ptr(context_lens), S, H, Hkv, D, nb, block_size,
         block_tables.shape[1], float(scale), partition_tokens, _ptr(err_flag), _stream(stream))
     _check(st, "pkv_paged_attention_decode_noalloc")
+
+
+def pkv_paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                context_lens: torch.Tensor, query_start: torch.Tensor,
+                                max_query_len: int, block_size: int, scale: float,
+                                err_flag: torch.Tensor | None = None, stream=None) -> None:
+    """Causal attention of each sequence's query chunk (its last C tokens) over
+    its paged history. q, out: [total_queries, num_heads, head_size];
+    query_start: int32 [num_seqs + 1]."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start, err_flag)
+    _, H, D = q.shape
+    nb, B, Hkv, _ = k_cache.shape
+    st = lib.pkv_paged_attention_prefill(
+        _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
+        _ptr(block_tables), _ptr(context_lens), _ptr(query_start), context_lens.shape[0], H,
+        Hkv, D, nb, block_size, block_tables.shape[1], int(max_query_len), float(scale),
+        _ptr(err_flag), _stream(stream))
+    _check(st, "pkv_paged_attention_prefill")
 
 
 def pkv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,

@@ -1,0 +1,62 @@
+// TMA tensor maps of a KV cache [num_blocks][block_size][num_kv_heads][D]
+// (16-bit elements), shared by the attention kernels' launchers. The driver's
+// encoder is reached through the runtime's entry-point query, so the library
+// does not link the driver library.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "pkv_host.h"
+
+namespace pkv {
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads,
+                             int64_t slots, int box_rows, bool swizzled) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  CUresult r;
+  if (!swizzled) {
+    // 3-D view: x = element within the head (D), y = KV head, z = slot; box D x 1 x rows.
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_kv_heads),
+                          static_cast<cuuint64_t>(slots)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // 4-D view: x = 64 elements (128 bytes), y = which 64-element line of the
+    // head, z = KV head, w = slot; box 64 x D/64 x 1 x rows with the 128-byte
+    // swizzle: one copy moves whole rows of a block.
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64),
+                          static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(slots)};
+    cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(D / 64), 1,
+                         static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace pkv

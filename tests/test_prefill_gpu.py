@@ -1,0 +1,68 @@
+"""Chunked-prefill attention on the GPU against the fp64 oracle: varied chunk
+sizes (one token, ragged, several row tiles, the whole prompt), MHA and GQA,
+d = 64 / 128, fp16 / bf16, block sizes 8..128, fp32 outputs held to the
+stated bound; bad chunk lengths reported."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_118_gb300 as pk
+from oracle.pipeline import build_decode_state, pool_demand
+from oracle.prefill import paged_attention_prefill
+from parity import TORCH_DTYPE, assert_close, dev, gpu_decode_state
+from workloads import decode_batch, free_order, normal_bits, poison_bits
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # lens, chunks, H, H_kv, D, B, dtype
+    ((100, 37, 1, 700), (1, 37, 1, 300), 8, 8, 128, 16, "f16"),
+    ((513, 64, 2049), (200, 64, 130), 32, 8, 128, 16, "bf16"),
+    ((90, 300), (90, 17), 4, 2, 64, 8, "f16"),
+    ((1500, 33), (129, 5), 16, 2, 128, 32, "bf16"),
+    ((640,), (640,), 64, 1, 64, 128, "bf16"),
+    ((77, 400, 9), (3, 65, 9), 40, 40, 128, 64, "f16"),
+]
+
+
+def _run(case, seed=0):
+    lens, chunks, H, Hkv, D, B, dt = case
+    batch = decode_batch("p", lens, H, Hkv, D, B, dt, seed=seed + len(lens))
+    n = pool_demand(batch.context_lens, B) + 9
+    order = free_order(n, seed)
+    cache, tables, ctx = gpu_decode_state(batch, n, order)
+    ref = build_decode_state(batch, n, order, poison_bits(dt))
+    starts = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = normal_bits(np.random.default_rng(seed + 99), (int(starts[-1]), H, D), dt)
+    want = paged_attention_prefill(q, ref["k_cache"], ref["v_cache"], ref["block_tables"],
+                                   batch.context_lens, starts, B, batch.scale, dt)
+    qd = dev(q, dt)
+    qsd = torch.from_numpy(starts).cuda()
+    for od in (TORCH_DTYPE[dt], torch.float32):
+        out = torch.full(qd.shape, float("nan"), dtype=od, device="cuda")
+        pk.pkv_paged_attention_prefill(out, qd, cache.k_cache, cache.v_cache, tables, ctx, qsd,
+                                       max(chunks), B, float(batch.scale), cache.err)
+        torch.cuda.synchronize()
+        assert_close(out, want, dt)
+    assert cache.err.item() == 0
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_prefill_against_oracle(case):
+    _run(case)
+
+
+def test_bad_chunk_is_reported_and_skipped():
+    batch = decode_batch("p", (40, 50), 4, 4, 64, 16, "f16", seed=3)
+    n = pool_demand(batch.context_lens, 16) + 2
+    cache, tables, ctx = gpu_decode_state(batch, n, free_order(n, 1))
+    starts = torch.tensor([0, 10, 70], dtype=torch.int32, device="cuda")   # 60 > L = 50
+    q = torch.randn(70, 4, 64, dtype=torch.float16, device="cuda")
+    out = torch.zeros_like(q)
+    pk.pkv_paged_attention_prefill(out, q, cache.k_cache, cache.v_cache, tables, ctx, starts,
+                                   60, 16, 0.125, cache.err)
+    torch.cuda.synchronize()
+    assert cache.err.item() & pk.PKV_DEVERR_CONTEXT
+    assert torch.all(out[10:] == 0) and torch.all(torch.isfinite(out[:10]))
+    assert not torch.all(out[:10] == 0)
