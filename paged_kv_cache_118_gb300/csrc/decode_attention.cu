@@ -48,7 +48,8 @@ constexpr int kGroups = kConsumerWarps * 32 / kGroupLanes;  // token groups per 
 constexpr float kRescaleThreshold = 8.0f;  // base-2 growth of the max that forces a rescale
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a compact work list
-constexpr int kMmaHeads = 8;                // query heads one CTA serves on the tensor path
+constexpr int kMmaHeads = 8;                // query heads of one KV head a tensor-path CTA serves
+constexpr int kMmaRows = 16;                // rows of its products: heads x sequences of a run
 
 struct DecodeParams {
   float* part_acc;            // [rows][D], rows = num_seqs * num_heads * max_parts
@@ -80,18 +81,19 @@ struct UnitDesc {
   int head0;
   int part;
   int len;
+  int nrun;                   // sequences seq .. seq+nrun-1 whose blocks for this
+                              // partition are identical (shared prefix), served together
 };
 
-// kMma: the tensor path keeps 2 CTAs per SM and affords a 5-stage ring; the
-// scalar paths keep 3 CTAs per SM with 4 stages.
+// A 4-stage ring; on the tensor path GS is the row capacity (kMmaRows).
 template <int D, int GS, bool kMma = false>
 struct DecodeLayout {
-  static constexpr int kStages = kMma ? 5 : 4;
+  static constexpr int kStages = 4;
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kTile * kRowBytes;        // K (or V) of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kQBytes = GS * D * 2;                  // query rows of one unit
+  static constexpr int kQBytes = GS * D * 2;                  // query rows of one unit (capacity)
   static constexpr int kCombineFloats = kConsumerWarps * GS * (D + 2);
   static constexpr int kChunks = D / 64;                      // 16-byte pieces per lane per row
   static constexpr int kE = 8 * kChunks;                      // elements per lane per row
@@ -342,26 +344,31 @@ struct MmaState {
     const int line = row * NH + (chunk >> 3);
     return smem_addr(tile + line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
   }
-  uint32_t qa[KS][2];                             // A fragments, rows g: k 2t.. and 2t+8..
-  float o[NT][4];
-  float m, l;
+  // A fragments: [0] row g, k 2t..; [1] row g+8, k 2t..; [2] row g, k 2t+8..; [3] row g+8, k 2t+8..
+  uint32_t qa[KS][4];
+  float o[NT][4];                                 // [0..1] row g, [2..3] row g+8
+  float mA, lA, mB, lB;                           // rows g and g+8
 
-  __device__ __forceinline__ void begin(const uint16_t* qs, int heads, int lane) {
+  // rows: query rows of the unit (sequences of the run x heads), at most 16
+  __device__ __forceinline__ void begin(const uint16_t* qs, int rows, int lane) {
     const int g = lane >> 2, t = lane & 3;
+    const bool ra = g < rows, rb = g + 8 < rows;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = g < heads ? *reinterpret_cast<const uint32_t*>(qs + g * D + 16 * ks + 2 * t) : 0u;
-      qa[ks][1] =
-          g < heads ? *reinterpret_cast<const uint32_t*>(qs + g * D + 16 * ks + 8 + 2 * t) : 0u;
+      const int c = 16 * ks + 2 * t;
+      qa[ks][0] = ra ? *reinterpret_cast<const uint32_t*>(qs + g * D + c) : 0u;
+      qa[ks][1] = rb ? *reinterpret_cast<const uint32_t*>(qs + (g + 8) * D + c) : 0u;
+      qa[ks][2] = ra ? *reinterpret_cast<const uint32_t*>(qs + g * D + c + 8) : 0u;
+      qa[ks][3] = rb ? *reinterpret_cast<const uint32_t*>(qs + (g + 8) * D + c + 8) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    m = -INFINITY;
-    l = 0.f;
+    mA = mB = -INFINITY;
+    lA = lB = 0.f;
   }
 
-  // kt, vt: the stage's K and V tiles (each D/64 swizzled halves); tok0: first
-  // token of this warp in the tile; valid: tokens of the tile that exist.
+  // kt, vt: the stage's K and V tiles; tok0: first token of this warp in the
+  // tile; valid: tokens of the tile that exist.
   __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int tok0, int valid,
                                        float q_scale, int lane) {
     const int t = lane & 3;
@@ -371,51 +378,60 @@ struct MmaState {
     float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kp = 0; kp < KS / 2; ++kp) {
-      const int chunk = 4 * kp + mat;             // 16-byte chunk along d
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(line_addr(kt, tok0 + r, chunk), b0, b1, b2, b3);
-      T::mma16816(s, qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
-      T::mma16816(s2, qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+      ldsm_x4(line_addr(kt, tok0 + r, 4 * kp + mat), b0, b1, b2, b3);
+      T::mma16816(s, qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+      T::mma16816(s2, qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3],
+                  b2, b3);
     }
-    s[0] += s2[0];
-    s[1] += s2[1];
     const int tk = tok0 + 2 * t;
-    const float s0 = tk < valid ? s[0] * q_scale : -INFINITY;
-    const float s1 = tk + 1 < valid ? s[1] * q_scale : -INFINITY;
-    float tm = fmaxf(s0, s1);
-    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
-    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
-    const bool need = tm > m + kRescaleThreshold;
-    if (__any_sync(0xffffffffu, need)) {
-      const float mn = need ? tm : m;
-      const float corr = need ? ex2(m - mn) : 1.f;
-      m = mn;
-      l *= corr;
+    const bool v0 = tk < valid, v1 = tk + 1 < valid;
+    const float a0 = v0 ? (s[0] + s2[0]) * q_scale : -INFINITY;
+    const float a1 = v1 ? (s[1] + s2[1]) * q_scale : -INFINITY;
+    const float b0s = v0 ? (s[2] + s2[2]) * q_scale : -INFINITY;
+    const float b1s = v1 ? (s[3] + s2[3]) * q_scale : -INFINITY;
+    float tmA = fmaxf(a0, a1), tmB = fmaxf(b0s, b1s);
+    tmA = fmaxf(tmA, __shfl_xor_sync(0xffffffffu, tmA, 1));
+    tmA = fmaxf(tmA, __shfl_xor_sync(0xffffffffu, tmA, 2));
+    tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 1));
+    tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 2));
+    const bool needA = tmA > mA + kRescaleThreshold, needB = tmB > mB + kRescaleThreshold;
+    if (__any_sync(0xffffffffu, needA || needB)) {
+      const float cA = needA ? ex2(mA - tmA) : 1.f, cB = needB ? ex2(mB - tmB) : 1.f;
+      if (needA) mA = tmA;
+      if (needB) mB = tmB;
+      lA *= cA;
+      lB *= cB;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        o[j][0] *= corr;
-        o[j][1] *= corr;
+        o[j][0] *= cA;
+        o[j][1] *= cA;
+        o[j][2] *= cB;
+        o[j][3] *= cB;
       }
     }
-    const float p0 = s0 == -INFINITY ? 0.f : ex2(s0 - m);
-    const float p1 = s1 == -INFINITY ? 0.f : ex2(s1 - m);
-    l += p0 + p1;
-    const uint32_t ph = T::pack(p0, p1);
-    const float2 hf = T::to_float2(ph);
-    const uint32_t pl = T::pack(p0 - hf.x, p1 - hf.y);
+    const float pa0 = a0 == -INFINITY ? 0.f : ex2(a0 - mA);
+    const float pa1 = a1 == -INFINITY ? 0.f : ex2(a1 - mA);
+    const float pb0 = b0s == -INFINITY ? 0.f : ex2(b0s - mB);
+    const float pb1 = b1s == -INFINITY ? 0.f : ex2(b1s - mB);
+    lA += pa0 + pa1;
+    lB += pb0 + pb1;
+    // P as two halves in the input format: p = hi + lo
+    const uint32_t hA = T::pack(pa0, pa1), hB = T::pack(pb0, pb1);
+    const float2 fA = T::to_float2(hA), fB = T::to_float2(hB);
+    const uint32_t lAo = T::pack(pa0 - fA.x, pa1 - fA.y), lBo = T::pack(pb0 - fB.x, pb1 - fB.y);
     // V rows of tokens past the tile's end may hold anything: zero their halves.
-    const uint32_t keep = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t keep = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
 #pragma unroll
     for (int nq = 0; nq < NT / 4; ++nq) {
-      const int chunk = 4 * nq + mat;
       uint32_t b[4];
-      ldsm_x4_t(line_addr(vt, tok0 + r, chunk), b[0], b[1], b[2], b[3]);
+      ldsm_x4_t(line_addr(vt, tok0 + r, 4 * nq + mat), b[0], b[1], b[2], b[3]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) b[i] &= keep;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) T::mma1688(o[4 * nq + i], ph, 0u, b[i]);
+      for (int i = 0; i < 4; ++i) T::mma1688(o[4 * nq + i], hA, hB, b[i]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) T::mma1688(o[4 * nq + i], pl, 0u, b[i]);
+      for (int i = 0; i < 4; ++i) T::mma1688(o[4 * nq + i], lAo, lBo, b[i]);
     }
   }
 };
@@ -425,8 +441,9 @@ struct MmaState {
 // left. The producer warp fetches the next unit, its slice of the block table
 // and its query rows while the consumers still work on the current one.
 // kMma: grouped query heads on the tensor path (MmaState; K/V tiles stored
-// with 128-byte swizzle by 64-element halves; GS is then the capacity, 8, and
-// p.heads_per_cta the heads actually served). Otherwise GroupState.
+// with 128-byte swizzle by 64-element halves; GS is then the row capacity, 16:
+// p.heads_per_cta heads of each of up to 16 / p.heads_per_cta sequences that
+// share the partition's blocks). Otherwise GroupState.
 template <int D, int GS, typename T, bool kMma>
 __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -550,6 +567,30 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
       const int nb = (t_end - 1) / B - jb0 + 1;
       const int kvh = kvs / p.subs;
       const int head0 = kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta;
+      // Shared prefix (tensor path): consecutive sequences of an aligned window
+      // whose blocks for this (full) partition are the same physical blocks are
+      // served by one unit, their query rows stacked into the 16 product rows.
+      int nrun = 1;
+      if constexpr (kMma) {
+        const int cap = kMmaRows / p.heads_per_cta;
+        if (cap > 1 && L >= t_begin + p.partition_tokens) {
+          auto shares = [&](int a, int b) -> bool {      // warp-collective
+            const int La = __ldg(p.context_lens + a), Lb = __ldg(p.context_lens + b);
+            const int need = t_begin + p.partition_tokens;
+            if (La < need || Lb < need || La > max_ctx || Lb > max_ctx) return false;
+            const int32_t* ra = p.block_tables + static_cast<int64_t>(a) * p.max_blocks_per_seq + jb0;
+            const int32_t* rb = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + jb0;
+            bool same = true;
+            for (int i = lane; i < nb; i += 32) same &= __ldg(ra + i) == __ldg(rb + i);
+            return __all_sync(0xffffffffu, same);
+          };
+          const int ws = seq - seq % cap, we = min(ws + cap, p.num_seqs);
+          if (seq > ws && shares(seq - 1, seq)) continue;  // served by the unit of an earlier sequence
+          int e = seq + 1;
+          while (e < we && shares(e - 1, e)) ++e;
+          nrun = e - seq;
+        }
+      }
       const int32_t* row =
           p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0;
       for (int i = lane; i < nb; i += 32) {
@@ -565,12 +606,13 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
         const int qb = k & 1;
         if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
         if (ok) {
-          units[qb] = UnitDesc{seq, head0, part, L};
+          units[qb] = UnitDesc{seq, head0, part, L, nrun};
           const uint32_t qbytes = static_cast<uint32_t>(p.heads_per_cta) * D * 2;
-          mbar_arrive_expect_tx(&q_full[qb], qbytes);
-          bulk_load(qbuf + qb * GS * D,
-                    p.q + (static_cast<int64_t>(seq) * p.num_heads + head0) * D, qbytes,
-                    &q_full[qb]);
+          mbar_arrive_expect_tx(&q_full[qb], qbytes * nrun);
+          for (int b = 0; b < nrun; ++b)
+            bulk_load(qbuf + qb * GS * D + b * p.heads_per_cta * D,
+                      p.q + (static_cast<int64_t>(seq + b) * p.num_heads + head0) * D, qbytes,
+                      &q_full[qb]);
         }
         for (int i = 0; ok && i < n_tiles; ++i, ++issued) {
           const int st = issued % kStages;
@@ -639,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
   int consumed = 0;                               // tiles consumed (ring position)
   for (int k = 0;; ++k) {
     const int qb = k & 1;
-    UnitDesc ud{-2, 0, 0, 0};
+    UnitDesc ud{-2, 0, 0, 0, 1};
     if (!ld_volatile(abort_flag) && mbar_wait(&q_full[qb], (k >> 1) & 1)) ud = units[qb];
     if (ud.seq == -1) break;                      // all work done
     if (ud.seq == -2) {                           // abort: nothing more is coming
@@ -649,8 +691,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
       }
       break;
     }
+    const int rows = ud.nrun * heads;            // query rows of this unit
     if constexpr (kMma) {
-      gs.begin(qbuf + qb * GS * D, heads, lane);
+      gs.begin(qbuf + qb * GS * D, rows, lane);
     } else {
       gs.begin(qbuf + qb * GS * D, j, p.q_scale);
     }
@@ -688,19 +731,25 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
     if (k >= 1) mbar_wait(&merge_bar[1], (k - 1) & 1);   // previous unit's partials read
     if constexpr (kMma) {
       const int g = lane >> 2, t = lane & 3;
-      float ls = gs.l;
-      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-      if (g < heads) {
-        float* cw = combine + (warp * GS + g) * (D + 2);
+      float lsA = gs.lA, lsB = gs.lB;
+      lsA += __shfl_xor_sync(0xffffffffu, lsA, 1);
+      lsA += __shfl_xor_sync(0xffffffffu, lsA, 2);
+      lsB += __shfl_xor_sync(0xffffffffu, lsB, 1);
+      lsB += __shfl_xor_sync(0xffffffffu, lsB, 2);
 #pragma unroll
-        for (int jn = 0; jn < MmaState<D, T>::NT; ++jn) {
-          cw[2 + 8 * jn + 2 * t] = gs.o[jn][0];
-          cw[2 + 8 * jn + 2 * t + 1] = gs.o[jn][1];
-        }
-        if (t == 0) {
-          cw[0] = gs.m;
-          cw[1] = ls;
+      for (int half = 0; half < 2; ++half) {
+        const int rw = g + 8 * half;
+        if (rw < rows) {
+          float* cw = combine + (warp * GS + rw) * (D + 2);
+#pragma unroll
+          for (int jn = 0; jn < MmaState<D, T>::NT; ++jn) {
+            cw[2 + 8 * jn + 2 * t] = gs.o[jn][2 * half];
+            cw[2 + 8 * jn + 2 * t + 1] = gs.o[jn][2 * half + 1];
+          }
+          if (t == 0) {
+            cw[0] = half ? gs.mB : gs.mA;
+            cw[1] = half ? lsB : lsA;
+          }
         }
       }
     } else {
@@ -742,10 +791,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
     if (lane == 0) mbar_arrive(&merge_bar[0]);
     mbar_wait(&merge_bar[0], k & 1);
 
-    const int64_t row0 =
-        (static_cast<int64_t>(ud.seq) * p.num_heads + ud.head0) * p.max_parts + ud.part;
-    for (int idx = threadIdx.x; idx < heads * D; idx += kConsumerWarps * 32) {
-      const int g = idx / D;
+    for (int idx = threadIdx.x; idx < rows * D; idx += kConsumerWarps * 32) {
+      const int g = idx / D;                      // row: sequence g / heads of the run, head g % heads
       const int e = idx % D;
       float mw[kConsumerWarps];
       float M = -INFINITY;
@@ -761,7 +808,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
         a = fmaf(combine[(w * GS + g) * (D + 2) + 2 + e], f, a);
         lsum = fmaf(combine[(w * GS + g) * (D + 2) + 1], f, lsum);
       }
-      const int64_t row = row0 + static_cast<int64_t>(g) * p.max_parts;
+      const int64_t row = ((static_cast<int64_t>(ud.seq) + g / heads) * p.num_heads + ud.head0 +
+                           g % heads) * p.max_parts + ud.part;
       p.part_acc[row * D + e] = a;
       if (e == 0) p.part_ml[row] = make_float2(M, lsum);
     }
@@ -905,7 +953,7 @@ static cudaError_t launch_partition(const CUtensorMap& tk, const CUtensorMap& tv
 template <int D, typename T>
 static cudaError_t dispatch_gs(bool mma, int gs, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeParams& p, cudaStream_t s) {
-  if (mma) return launch_partition<D, kMmaHeads, T, true>(tk, tv, p, s);
+  if (mma) return launch_partition<D, kMmaRows, T, true>(tk, tv, p, s);
   switch (gs) {
     case 1: return launch_partition<D, 1, T, false>(tk, tv, p, s);
     case 2: return launch_partition<D, 2, T, false>(tk, tv, p, s);

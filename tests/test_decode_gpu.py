@@ -216,3 +216,86 @@ def test_decode_flags_bad_block_ids_and_lengths():
     assert e & pk.PKV_DEVERR_BLOCK_ID and e & pk.PKV_DEVERR_CONTEXT and not e & pk.PKV_DEVERR_TIMEOUT
     assert torch.equal(out[0], good[0])         # untouched sequence
     assert torch.all(out[2] == 0)               # invalid length -> zeros
+
+
+def shared_tables(sizes, prefix_tokens, B, seed, diverge=0.25, max_tail=100):
+    """Beam groups at the table level: the sequences of a group name the same
+    physical blocks for their first prefix_tokens // B blocks (some beams only
+    for a random shorter run of them), then blocks of their own. Returns the
+    tables (-1 padded), context lengths and the number of physical blocks,
+    placed by a seeded permutation."""
+    rng = np.random.default_rng(seed)
+    nbp = prefix_tokens // B
+    rows, lens, nxt = [], [], 0
+    for n in sizes:
+        shared = list(range(nxt, nxt + nbp))
+        nxt += nbp
+        for _ in range(n):
+            L = nbp * B + int(rng.integers(1, max_tail, endpoint=True))
+            keep = nbp if rng.random() >= diverge else int(rng.integers(0, nbp + 1))
+            own = -(-L // B) - keep
+            rows.append(shared[:keep] + list(range(nxt, nxt + own)))
+            nxt += own
+            lens.append(L)
+    place = rng.permutation(nxt + 5)
+    w = max(len(r) for r in rows)
+    tables = np.full((len(rows), w), -1, np.int32)
+    for i, r in enumerate(rows):
+        tables[i, :len(r)] = place[r]
+    return tables, np.array(lens, np.int32), nxt + 5
+
+
+def privatize(tables, k, v, B):
+    """The same token data with every block of every sequence copied to a block
+    of its own (no two sequences share one)."""
+    rows, srcs = [], []
+    for r in tables:
+        ids = [int(x) for x in r if x >= 0]
+        rows.append(list(range(len(srcs), len(srcs) + len(ids))))
+        srcs += ids
+    pt = np.full(tables.shape, -1, np.int32)
+    for i, r in enumerate(rows):
+        pt[i, :len(r)] = r
+    return pt, k[srcs], v[srcs]
+
+
+SHARED_CASES = [
+    # beams per group, prefix tokens, H, H_kv, D, B, dtype, partition_tokens
+    ((3, 5, 1, 4, 2, 7), 300, 32, 8, 128, 16, "bf16", 64),     # 4 heads: 4 sequences a unit
+    ((4, 4, 4, 4, 4, 4), 1040, 32, 8, 128, 16, "bf16", 512),
+    ((2, 9, 3, 11), 520, 16, 8, 128, 32, "f16", 128),          # 2 heads: 8 sequences a unit
+    ((3, 3, 2, 6), 256, 64, 8, 64, 8, "f16", 64),              # 8 heads: 2 sequences a unit
+    ((5, 4), 200, 32, 2, 128, 16, "bf16", 32),                 # 16 heads in two slices of 8
+    ((6, 1, 6), 192, 24, 4, 128, 64, "bf16", 64),              # 6 heads: 2 sequences a unit
+]
+
+
+@pytest.mark.parametrize("case", SHARED_CASES, ids=[f"s{i}" for i in range(len(SHARED_CASES))])
+def test_shared_prefix_runs(case):
+    """Sequences whose blocks for a partition are the same physical blocks are
+    served together on the tensor path: the outputs match the oracle, and equal
+    bit for bit those of the same data with no block shared."""
+    sizes, P, H, Hkv, D, B, dt, pt = case
+    tables, lens, nb = shared_tables(sizes, P, B, seed=sum(sizes) + H)
+    rng = np.random.default_rng(len(sizes) * 7 + D)
+    from workloads import normal_bits
+    kc = normal_bits(rng, (nb, B, Hkv, D), dt)
+    vc = normal_bits(rng, (nb, B, Hkv, D), dt)
+    q = normal_bits(rng, (len(lens), H, D), dt)
+    scale = np.float32(1.0) / np.sqrt(np.float32(D))
+    want = oracle_decode(q, kc, vc, tables, lens, B, scale, dt)
+    ptab, pk_, pv_ = privatize(tables, kc, vc, B)
+    outs = []
+    for tab, k, v in ((tables, kc, vc), (ptab, pk_, pv_)):
+        out = torch.empty(q.shape, dtype=TORCH_DTYPE[dt], device="cuda")
+        tt = torch.from_numpy(tab).cuda()
+        ws = pk.decode_workspace(len(lens), H, D, tab.shape[1], B, pt)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pk.pkv_paged_attention_decode(out, dev(q, dt), dev(k, dt), dev(v, dt), tt,
+                                      torch.from_numpy(lens).cuda(), B, float(scale), ws,
+                                      partition_tokens=pt, err_flag=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert_close(out, want, dt)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
