@@ -42,7 +42,7 @@ namespace pkv {
 
 constexpr int kTile = 32;           // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // + copy warp + scheduler warp
 constexpr int kGroupLanes = 8;      // lanes that share one token row
 constexpr int kGroups = kConsumerWarps * 32 / kGroupLanes;  // token groups per CTA (16)
 constexpr float kRescaleThreshold = 8.0f;  // base-2 growth of the max that forces a rescale
@@ -50,6 +50,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a compact work list
 constexpr int kMmaHeads = 8;                // query heads of one KV head a tensor-path CTA serves
 constexpr int kMmaRows = 16;                // rows of its products: heads x sequences of a run
+constexpr int kMaxRun = 8;                  // sequences one tensor-path unit serves at most
+// The scheduler claims the next unit when this many of the current unit's
+// tiles are left to issue: enough to hide the claim, late enough to keep the
+// end of the work list balanced across CTAs.
+constexpr int kClaimAheadTiles = 2;
+constexpr int kClaimAheadTilesMma = 8;
 
 struct DecodeParams {
   float* part_acc;            // [rows][D], rows = num_seqs * num_heads * max_parts
@@ -101,13 +107,15 @@ struct DecodeLayout {
   static constexpr int kOffCombine = kRingBytes;
   static constexpr int kOffQ = kOffCombine + kCombineFloats * 4;
   static constexpr int kOffBars = kOffQ + 2 * kQBytes;        // 16-byte aligned
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;    // full, empty, q_full, q_empty, merge
-  static constexpr int kOffUnits = kOffBars + kNumBars * 8;
-  static constexpr int kOffFlag = kOffUnits + 2 * sizeof(UnitDesc);
-  static constexpr int kOffPref = kOffFlag + 16;               // prefix of partitions per sequence
+  // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty, sched_go
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1;
+  static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[2], then sched[2]
+  static constexpr int kOffFlag = kOffUnits + 4 * sizeof(UnitDesc);
+  static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of partitions per sequence
   static constexpr int kOffSlice = kOffPref + ((kCompactMaxSeqs + 1) * 4 + 15) / 16 * 16;
+  // table_slice: entries of one unit's block-table slice; two are staged
   static int smem_bytes(int table_slice) {
-    return 1024 /*alignment slack*/ + kOffSlice + ((table_slice * 4 + 15) / 16) * 16;
+    return 1024 /*alignment slack*/ + kOffSlice + ((2 * table_slice * 4 + 15) / 16) * 16;
   }
 };
 
@@ -445,7 +453,7 @@ struct MmaState {
 // p.heads_per_cta heads of each of up to 16 / p.heads_per_cta sequences that
 // share the partition's blocks). Otherwise GroupState.
 template <int D, int GS, typename T, bool kMma>
-__global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using Lay = DecodeLayout<D, GS, kMma>;
@@ -461,7 +469,11 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
   uint64_t* q_full = empty_bar + kStages;
   uint64_t* q_empty = q_full + 2;
   uint64_t* merge_bar = q_empty + 2;          // [0]: partials written, [1]: partials read
+  uint64_t* sched_full = merge_bar + 2;       // scheduler -> copy warp, per staged unit
+  uint64_t* sched_empty = sched_full + 2;
+  uint64_t* sched_go = sched_empty + 2;       // copy warp -> scheduler: claim the next unit
   UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + Lay::kOffUnits);
+  UnitDesc* sched = units + 2;
   int* abort_flag = reinterpret_cast<int*>(smem + Lay::kOffFlag);
   int* pref = reinterpret_cast<int*>(smem + Lay::kOffPref);
   int32_t* slice = reinterpret_cast<int32_t*>(smem + Lay::kOffSlice);
@@ -471,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
   const int B = p.block_size;
   const int max_ctx = p.max_blocks_per_seq * B;
   const int per_part = p.num_seqs * p.kv_slices;
+  const int slice_cap = p.partition_tokens / B + 2;   // entries of one staged slice
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -481,20 +494,22 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], kConsumerWarps);
       mbar_init(&merge_bar[i], kConsumerWarps);
+      mbar_init(&sched_full[i], 32);
+      mbar_init(&sched_empty[i], 1);
     }
+    mbar_init(sched_go, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  // ------------------------------------------------------------ producer warp
-  if (warp == kConsumerWarps) {
-    const uint64_t policy = l2_evict_first_policy();
-    const uint32_t copy_bytes = static_cast<uint32_t>(p.box_rows) * Lay::kRowBytes;
-    if (lane == 0) {
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-    }
+  // ------------------------------------------------------------ scheduler warp
+  // Claims units from the global counter, resolves each one (sequence,
+  // partition, head slice; on the tensor path the run of sequences that share
+  // the partition's blocks) and stages its block-table slice, one unit ahead of
+  // the copy warp, so that none of this latency falls between two units of the
+  // copy stream.
+  if (warp == kConsumerWarps + 1) {
     // The work list. For batches of up to kCompactMaxSeqs sequences only the
     // units that exist are numbered, sequence-major (a prefix sum of each
     // sequence's partition count, then a binary search per unit); larger
@@ -526,6 +541,132 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
       __syncwarp();
       total = carry * p.kv_slices;
     }
+    // Tensor path: a unit serves the sequences of an aligned window of `cap`
+    // whose blocks for the (whole) partition are the same physical blocks.
+    const int cap = kMma ? min(kMmaRows / p.heads_per_cta, kMaxRun) : 1;
+    bool ok = true;
+    for (int k = 0;; ++k) {
+      if (k >= 1) {                           // the copy warp is far enough into unit k-1
+        int w = 1;
+        if (lane == 0) w = mbar_wait(sched_go, (k - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      UnitDesc d{-1, 0, 0, 0, 1};
+      int jb0 = 0, nb = 0;
+      while (true) {
+        int u = 0;
+        if (lane == 0) u = atomicAdd(p.counter, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= total) break;
+        int part, seq, kvs;
+        if (compact) {
+          int lo = 0, hi = p.num_seqs;        // largest lo with pref[lo] * slices <= u
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pref[mid] * p.kv_slices <= u) lo = mid; else hi = mid;
+          }
+          seq = lo;
+          const int rem = u - pref[lo] * p.kv_slices;
+          part = rem / p.kv_slices;
+          kvs = rem - part * p.kv_slices;
+        } else {
+          part = u / per_part;
+          const int rem = u - part * per_part;
+          seq = rem / p.kv_slices;
+          kvs = rem - seq * p.kv_slices;
+        }
+        const int ws = seq - seq % cap, nw = min(cap, p.num_seqs - ws);
+        int Lm = 0;                             // lane m: length of window member m
+        if (lane < nw) Lm = __ldg(p.context_lens + ws + lane);
+        const int L = __shfl_sync(0xffffffffu, Lm, seq - ws);
+        if (L < 1 || L > max_ctx) {
+          if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+          continue;
+        }
+        const int t_begin = part * p.partition_tokens;
+        if (t_begin >= L) continue;           // this sequence has no such partition
+        const int t_end = min(L, t_begin + p.partition_tokens);
+        jb0 = t_begin / B;
+        nb = (t_end - 1) / B - jb0 + 1;
+        int nrun = 1;
+        const int need = t_begin + p.partition_tokens;
+        if (kMma && cap > 1 && L >= need) {
+          const unsigned full =
+              __ballot_sync(0xffffffffu, lane < nw && Lm >= need && Lm <= max_ctx);
+          // bit m: members m-1 and m name the same blocks over the partition
+          unsigned same = 0xffffffffu;
+          for (int i0 = 0; i0 < nb; i0 += 32) {
+            const int i = i0 + lane;
+            if (i < nb) {
+              int32_t id[kMaxRun];
+#pragma unroll
+              for (int m = 0; m < kMaxRun; ++m)
+                id[m] = m < nw ? __ldg(p.block_tables +
+                                       static_cast<int64_t>(ws + m) * p.max_blocks_per_seq + jb0 + i)
+                               : -1;
+              unsigned bits = 1u;
+#pragma unroll
+              for (int m = 1; m < kMaxRun; ++m) bits |= (id[m] == id[m - 1] ? 1u : 0u) << m;
+              same &= bits;
+            }
+          }
+          same = __reduce_and_sync(0xffffffffu, same);
+          const unsigned link = same & full & (full << 1);   // bit m: m-1 and m run together
+          const int o = seq - ws;
+          if (o > 0 && ((link >> o) & 1u)) continue;        // served by an earlier sequence's unit
+          int e = o + 1;
+          while (e < nw && ((link >> e) & 1u)) ++e;
+          nrun = e - o;
+        }
+        const int kvh = kvs / p.subs;
+        d = UnitDesc{seq, kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta, part, L, nrun};
+        break;
+      }
+      const int sb = k & 1;
+      if (k >= 2) {
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&sched_empty[sb], ((k >> 1) & 1) ^ 1);
+        if (!__shfl_sync(0xffffffffu, w, 0) || ld_volatile(abort_flag)) {
+          ok = false;
+          break;
+        }
+      }
+      if (d.seq >= 0) {
+        int32_t* sl = slice + sb * slice_cap;
+        const int32_t* row =
+            p.block_tables + static_cast<int64_t>(d.seq) * p.max_blocks_per_seq + jb0;
+        for (int i = lane; i < nb; i += 32) {
+          int32_t id = __ldg(row + i);
+          if (id < 0 || id >= p.num_blocks) {
+            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+            id = 0;
+          }
+          sl[i] = id;
+        }
+      }
+      if (lane == 0) sched[sb] = d;
+      mbar_arrive(&sched_full[sb]);             // every lane: its slice entries are written
+      if (d.seq < 0) break;
+    }
+    if (!ok && lane == 0) {
+      flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      st_volatile(abort_flag, 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ copy warp
+  // Publishes each staged unit to the consumers (its query rows by bulk copy)
+  // and streams its K/V tiles through the ring. One thread.
+  if (warp == kConsumerWarps) {
+    if (lane != 0) return;
+    const uint64_t policy = l2_evict_first_policy();
+    const uint32_t copy_bytes = static_cast<uint32_t>(p.box_rows) * Lay::kRowBytes;
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
     int issued = 0;                           // tiles issued (ring position)
     int k = 0;                                // units published
     int ok = 1;
@@ -533,138 +674,79 @@ __global__ void __launch_bounds__(kThreads, (GS >= 4 || kMma) ? 2 : 3)
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
     while (true) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(p.counter, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (u >= total) break;
-      int part, seq, kvs;
-      if (compact) {
-        int lo = 0, hi = p.num_seqs;          // largest lo with pref[lo] * slices <= u
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (pref[mid] * p.kv_slices <= u) lo = mid; else hi = mid;
-        }
-        seq = lo;
-        const int rem = u - pref[lo] * p.kv_slices;
-        part = rem / p.kv_slices;
-        kvs = rem - part * p.kv_slices;
-      } else {
-        part = u / per_part;
-        const int rem = u - part * per_part;
-        seq = rem / p.kv_slices;
-        kvs = rem - seq * p.kv_slices;
+      const int sb = k & 1;
+      if (!mbar_wait(&sched_full[sb], (k >> 1) & 1)) {
+        ok = 0;
+        break;
       }
-      const int L = __ldg(p.context_lens + seq);
-      if (L < 1 || L > max_ctx) {
-        if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-        continue;
-      }
-      const int t_begin = part * p.partition_tokens;
-      if (t_begin >= L) continue;             // this sequence has no such partition
-      const int t_end = min(L, t_begin + p.partition_tokens);
+      const UnitDesc d = sched[sb];
+      if (d.seq < 0) break;
+      const int t_begin = d.part * p.partition_tokens;
+      const int t_end = min(d.len, t_begin + p.partition_tokens);
       const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
       const int jb0 = t_begin / B;
-      const int nb = (t_end - 1) / B - jb0 + 1;
-      const int kvh = kvs / p.subs;
-      const int head0 = kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta;
-      // Shared prefix (tensor path): consecutive sequences of an aligned window
-      // whose blocks for this (full) partition are the same physical blocks are
-      // served by one unit, their query rows stacked into the 16 product rows.
-      int nrun = 1;
-      if constexpr (kMma) {
-        const int cap = kMmaRows / p.heads_per_cta;
-        if (cap > 1 && L >= t_begin + p.partition_tokens) {
-          auto shares = [&](int a, int b) -> bool {      // warp-collective
-            const int La = __ldg(p.context_lens + a), Lb = __ldg(p.context_lens + b);
-            const int need = t_begin + p.partition_tokens;
-            if (La < need || Lb < need || La > max_ctx || Lb > max_ctx) return false;
-            const int32_t* ra = p.block_tables + static_cast<int64_t>(a) * p.max_blocks_per_seq + jb0;
-            const int32_t* rb = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + jb0;
-            bool same = true;
-            for (int i = lane; i < nb; i += 32) same &= __ldg(ra + i) == __ldg(rb + i);
-            return __all_sync(0xffffffffu, same);
-          };
-          const int ws = seq - seq % cap, we = min(ws + cap, p.num_seqs);
-          if (seq > ws && shares(seq - 1, seq)) continue;  // served by the unit of an earlier sequence
-          int e = seq + 1;
-          while (e < we && shares(e - 1, e)) ++e;
-          nrun = e - seq;
-        }
-      }
-      const int32_t* row =
-          p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0;
-      for (int i = lane; i < nb; i += 32) {
-        int32_t id = __ldg(row + i);
-        if (id < 0 || id >= p.num_blocks) {
-          flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-          id = 0;
-        }
-        slice[i] = id;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        const int qb = k & 1;
-        if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
-        if (ok) {
-          units[qb] = UnitDesc{seq, head0, part, L, nrun};
-          const uint32_t qbytes = static_cast<uint32_t>(p.heads_per_cta) * D * 2;
-          mbar_arrive_expect_tx(&q_full[qb], qbytes * nrun);
-          for (int b = 0; b < nrun; ++b)
-            bulk_load(qbuf + qb * GS * D + b * p.heads_per_cta * D,
-                      p.q + (static_cast<int64_t>(seq + b) * p.num_heads + head0) * D, qbytes,
-                      &q_full[qb]);
-        }
-        for (int i = 0; ok && i < n_tiles; ++i, ++issued) {
-          const int st = issued % kStages;
-          if (issued >= kStages && !mbar_wait(&empty_bar[st], ((issued / kStages) & 1) ^ 1)) {
-            ok = 0;
-            break;
-          }
-          if (ld_volatile(abort_flag)) {
-            ok = 0;
-            break;
-          }
-          const int t0 = t_begin + i * kTile;
-          const int valid = min(kTile, t_end - t0);
-          const int copies = B >= kTile ? 1 : (valid + B - 1) / B;
-          uint8_t* kdst = ring + st * Lay::kStageBytes;
-          uint8_t* vdst = kdst + Lay::kTileBytes;
-          mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
-          for (int c = 0; c < copies; ++c) {
-            const int z = B >= kTile ? slice[t0 / B - jb0] * B + (t0 % B)
-                                     : slice[t0 / B + c - jb0] * B;
-            if constexpr (kMma) {
-              // 4-D view (64 elements, D/64 lines, head, slot): whole rows, swizzled
-              tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, 0, kvh, z, policy);
-              tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, 0, kvh, z, policy);
-            } else {
-              tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
-              tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
-            }
-          }
-          last_issued[st] = issued;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      ++k;
-      __syncwarp();                           // lane 0 is done reading the slice
-      if (!ok) break;
-    }
-    if (lane == 0) {
-      // Publish the end of the work (or the abort) to the consumers.
+      const int kvh = d.head0 / p.group;
+      const int32_t* sl = slice + sb * slice_cap;
       const int qb = k & 1;
-      if (ok && k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
-      if (!ok) {
-        flag_error(p.err, PKV_DEVERR_TIMEOUT);
-        st_volatile(abort_flag, 1);
+      if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) {
+        ok = 0;
+        break;
       }
-      units[qb].seq = ok ? -1 : -2;
-      mbar_arrive(&q_full[qb]);
-      if (!ok) {
-        // Let the copies already in flight land before the CTA can retire.
-        for (int st = 0; st < kStages; ++st)
-          if (last_issued[st] >= 0) mbar_wait(&full_bar[st], (last_issued[st] / kStages) & 1);
+      units[qb] = d;
+      const uint32_t qbytes = static_cast<uint32_t>(p.heads_per_cta) * D * 2;
+      mbar_arrive_expect_tx(&q_full[qb], qbytes * d.nrun);
+      for (int b = 0; b < d.nrun; ++b)
+        bulk_load(qbuf + qb * GS * D + b * p.heads_per_cta * D,
+                  p.q + (static_cast<int64_t>(d.seq + b) * p.num_heads + d.head0) * D, qbytes,
+                  &q_full[qb]);
+      ++k;
+      const int go_at = max(0, n_tiles - (kMma ? kClaimAheadTilesMma : kClaimAheadTiles));
+      for (int i = 0; i < n_tiles; ++i, ++issued) {
+        if (i == go_at) mbar_arrive(sched_go);
+        const int st = issued % kStages;
+        if (issued >= kStages && !mbar_wait(&empty_bar[st], ((issued / kStages) & 1) ^ 1)) {
+          ok = 0;
+          break;
+        }
+        if (ld_volatile(abort_flag)) {
+          ok = 0;
+          break;
+        }
+        const int t0 = t_begin + i * kTile;
+        const int valid = min(kTile, t_end - t0);
+        const int copies = B >= kTile ? 1 : (valid + B - 1) / B;
+        uint8_t* kdst = ring + st * Lay::kStageBytes;
+        uint8_t* vdst = kdst + Lay::kTileBytes;
+        mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
+        for (int c = 0; c < copies; ++c) {
+          const int z = B >= kTile ? sl[t0 / B - jb0] * B + (t0 % B) : sl[t0 / B + c - jb0] * B;
+          if constexpr (kMma) {
+            // 4-D view (64 elements, D/64 lines, head, slot): whole rows, swizzled
+            tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, 0, kvh, z, policy);
+            tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, 0, kvh, z, policy);
+          } else {
+            tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
+            tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
+          }
+        }
+        last_issued[st] = issued;
       }
+      if (!ok) break;
+      mbar_arrive(&sched_empty[sb]);          // the slice has been read
+    }
+    // Publish the end of the work (or the abort) to the consumers.
+    const int qb = k & 1;
+    if (ok && k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
+    if (!ok) {
+      flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      st_volatile(abort_flag, 1);
+    }
+    units[qb].seq = ok ? -1 : -2;
+    mbar_arrive(&q_full[qb]);
+    if (!ok) {
+      // Let the copies already in flight land before the CTA can retire.
+      for (int st = 0; st < kStages; ++st)
+        if (last_issued[st] >= 0) mbar_wait(&full_bar[st], (last_issued[st] / kStages) & 1);
     }
     return;
   }
