@@ -107,8 +107,9 @@ struct DecodeLayout {
   static constexpr int kOffCombine = kRingBytes;
   static constexpr int kOffQ = kOffCombine + kCombineFloats * 4;
   static constexpr int kOffBars = kOffQ + 2 * kQBytes;        // 16-byte aligned
-  // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty, sched_go
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1;
+  // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty, sched_go;
+  // tree merge of the tensor path: x_full, x_free, y_full, y_free
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 4;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[2], then sched[2]
   static constexpr int kOffFlag = kOffUnits + 4 * sizeof(UnitDesc);
   static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of partitions per sequence
@@ -472,6 +473,10 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   uint64_t* sched_full = merge_bar + 2;       // scheduler -> copy warp, per staged unit
   uint64_t* sched_empty = sched_full + 2;
   uint64_t* sched_go = sched_empty + 2;       // copy warp -> scheduler: claim the next unit
+  uint64_t* x_full = sched_go + 1;            // tensor path: warps 2, 3 -> warps 0, 1
+  uint64_t* x_free = x_full + 1;
+  uint64_t* y_full = x_free + 1;              // warp 1 -> warp 0
+  uint64_t* y_free = y_full + 1;
   UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + Lay::kOffUnits);
   UnitDesc* sched = units + 2;
   int* abort_flag = reinterpret_cast<int*>(smem + Lay::kOffFlag);
@@ -498,6 +503,10 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       mbar_init(&sched_empty[i], 1);
     }
     mbar_init(sched_go, 1);
+    mbar_init(x_full, 2);
+    mbar_init(x_free, 2);
+    mbar_init(y_full, 1);
+    mbar_init(y_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -808,33 +817,92 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
 
-    // Merge this warp's partial into shared memory (one row of D + 2 floats
-    // per head: m, l, acc), then the four warps' rows into the unit's partial.
-    if (k >= 1) mbar_wait(&merge_bar[1], (k - 1) & 1);   // previous unit's partials read
     if constexpr (kMma) {
-      const int g = lane >> 2, t = lane & 3;
-      float lsA = gs.lA, lsB = gs.lB;
-      lsA += __shfl_xor_sync(0xffffffffu, lsA, 1);
-      lsA += __shfl_xor_sync(0xffffffffu, lsA, 2);
-      lsB += __shfl_xor_sync(0xffffffffu, lsB, 1);
-      lsB += __shfl_xor_sync(0xffffffffu, lsB, 2);
+      // Tree merge of the four warps' states, fragment by fragment (every warp
+      // holds the same rows and columns in the same registers): warps 2 and 3
+      // hand theirs to warps 0 and 1, warp 1 hands the sum to warp 0, which
+      // writes the unit's partials.
+      using M = MmaState<D, T>;
+      constexpr int kFrag4 = M::NT + 1;                 // float4s per lane: o, then (mA, mB, lA, lB)
+      float4* xb = reinterpret_cast<float4*>(combine);  // [2][kFrag4][32]
+      float4* yb = xb + 2 * kFrag4 * 32;                // [kFrag4][32]
+      auto put = [&](float4* dst) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int rw = g + 8 * half;
-        if (rw < rows) {
-          float* cw = combine + (warp * GS + rw) * (D + 2);
+        for (int jn = 0; jn < M::NT; ++jn)
+          dst[jn * 32 + lane] = make_float4(gs.o[jn][0], gs.o[jn][1], gs.o[jn][2], gs.o[jn][3]);
+        dst[M::NT * 32 + lane] = make_float4(gs.mA, gs.mB, gs.lA, gs.lB);
+      };
+      auto take = [&](const float4* src) {
+        const float4 ml = src[M::NT * 32 + lane];
+        const float MA = fmaxf(gs.mA, ml.x), MB = fmaxf(gs.mB, ml.y);
+        const float fA = gs.mA == -INFINITY ? 0.f : ex2(gs.mA - MA);
+        const float hA = ml.x == -INFINITY ? 0.f : ex2(ml.x - MA);
+        const float fB = gs.mB == -INFINITY ? 0.f : ex2(gs.mB - MB);
+        const float hB = ml.y == -INFINITY ? 0.f : ex2(ml.y - MB);
+        gs.lA = fmaf(gs.lA, fA, ml.z * hA);
+        gs.lB = fmaf(gs.lB, fB, ml.w * hB);
 #pragma unroll
-          for (int jn = 0; jn < MmaState<D, T>::NT; ++jn) {
-            cw[2 + 8 * jn + 2 * t] = gs.o[jn][2 * half];
-            cw[2 + 8 * jn + 2 * t + 1] = gs.o[jn][2 * half + 1];
-          }
-          if (t == 0) {
-            cw[0] = half ? gs.mB : gs.mA;
-            cw[1] = half ? lsB : lsA;
+        for (int jn = 0; jn < M::NT; ++jn) {
+          const float4 v = src[jn * 32 + lane];
+          gs.o[jn][0] = fmaf(gs.o[jn][0], fA, v.x * hA);
+          gs.o[jn][1] = fmaf(gs.o[jn][1], fA, v.y * hA);
+          gs.o[jn][2] = fmaf(gs.o[jn][2], fB, v.z * hB);
+          gs.o[jn][3] = fmaf(gs.o[jn][3], fB, v.w * hB);
+        }
+        gs.mA = MA;
+        gs.mB = MB;
+      };
+      auto wait_or_abort = [&](uint64_t* bar, int parity) {
+        if (!mbar_wait(bar, parity) && lane == 0) {
+          flag_error(p.err, PKV_DEVERR_TIMEOUT);
+          st_volatile(abort_flag, 1);
+        }
+      };
+      if (warp >= 2) {
+        if (k >= 1) wait_or_abort(x_free, (k - 1) & 1);
+        put(xb + (warp - 2) * kFrag4 * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x_full);
+      } else {
+        wait_or_abort(x_full, k & 1);
+        take(xb + warp * kFrag4 * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x_free);
+        if (warp == 1) {
+          if (k >= 1) wait_or_abort(y_free, (k - 1) & 1);
+          put(yb);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(y_full);
+        } else {
+          wait_or_abort(y_full, k & 1);
+          take(yb);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(y_free);
+          const int g = lane >> 2, t = lane & 3;
+          float lsA = gs.lA, lsB = gs.lB;
+          lsA += __shfl_xor_sync(0xffffffffu, lsA, 1);
+          lsA += __shfl_xor_sync(0xffffffffu, lsA, 2);
+          lsB += __shfl_xor_sync(0xffffffffu, lsB, 1);
+          lsB += __shfl_xor_sync(0xffffffffu, lsB, 2);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int rw = g + 8 * half;          // sequence rw / heads of the run, head rw % heads
+            if (rw < rows) {
+              const int64_t row = ((static_cast<int64_t>(ud.seq) + rw / heads) * p.num_heads +
+                                   ud.head0 + rw % heads) * p.max_parts + ud.part;
+              float2* dst = reinterpret_cast<float2*>(p.part_acc + row * D);
+#pragma unroll
+              for (int jn = 0; jn < M::NT; ++jn)
+                dst[4 * jn + t] = make_float2(gs.o[jn][2 * half], gs.o[jn][2 * half + 1]);
+              if (t == 0) p.part_ml[row] = make_float2(half ? gs.mB : gs.mA, half ? lsB : lsA);
+            }
           }
         }
       }
     } else {
+      // Merge this warp's partial into shared memory (one row of D + 2 floats
+      // per head: m, l, acc), then the four warps' rows into the unit's partial.
+      if (k >= 1) mbar_wait(&merge_bar[1], (k - 1) & 1);   // previous unit's partials read
       // Lanes j, j+8, j+16, j+24 hold the same elements: merge the groups first.
 #pragma unroll
       for (int g = 0; g < GS; ++g) {
@@ -868,35 +936,35 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
           cw[1] = ls;
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&merge_bar[0]);
-    mbar_wait(&merge_bar[0], k & 1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&merge_bar[0]);
+      mbar_wait(&merge_bar[0], k & 1);
 
-    for (int idx = threadIdx.x; idx < rows * D; idx += kConsumerWarps * 32) {
-      const int g = idx / D;                      // row: sequence g / heads of the run, head g % heads
-      const int e = idx % D;
-      float mw[kConsumerWarps];
-      float M = -INFINITY;
+      for (int idx = threadIdx.x; idx < heads * D; idx += kConsumerWarps * 32) {
+        const int g = idx / D;
+        const int e = idx % D;
+        float mw[kConsumerWarps];
+        float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        mw[w] = combine[(w * GS + g) * (D + 2)];
-        M = fmaxf(M, mw[w]);
-      }
-      float a = 0.f, lsum = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          mw[w] = combine[(w * GS + g) * (D + 2)];
+          M = fmaxf(M, mw[w]);
+        }
+        float a = 0.f, lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
-        a = fmaf(combine[(w * GS + g) * (D + 2) + 2 + e], f, a);
-        lsum = fmaf(combine[(w * GS + g) * (D + 2) + 1], f, lsum);
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
+          a = fmaf(combine[(w * GS + g) * (D + 2) + 2 + e], f, a);
+          lsum = fmaf(combine[(w * GS + g) * (D + 2) + 1], f, lsum);
+        }
+        const int64_t row =
+            (static_cast<int64_t>(ud.seq) * p.num_heads + ud.head0 + g) * p.max_parts + ud.part;
+        p.part_acc[row * D + e] = a;
+        if (e == 0) p.part_ml[row] = make_float2(M, lsum);
       }
-      const int64_t row = ((static_cast<int64_t>(ud.seq) + g / heads) * p.num_heads + ud.head0 +
-                           g % heads) * p.max_parts + ud.part;
-      p.part_acc[row * D + e] = a;
-      if (e == 0) p.part_ml[row] = make_float2(M, lsum);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&merge_bar[1]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&merge_bar[1]);
   }
 }
 
