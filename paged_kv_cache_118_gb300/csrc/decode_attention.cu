@@ -51,11 +51,13 @@ constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a com
 constexpr int kMmaHeads = 8;                // query heads of one KV head a tensor-path CTA serves
 constexpr int kMmaRows = 16;                // rows of its products: heads x sequences of a run
 constexpr int kMaxRun = 8;                  // sequences one tensor-path unit serves at most
-// The scheduler claims the next unit when this many of the current unit's
-// tiles are left to issue: enough to hide the claim, late enough to keep the
-// end of the work list balanced across CTAs.
-constexpr int kClaimAheadTiles = 2;
+// The scheduler claims another unit whenever fewer than this many tiles of
+// staged units are left to issue: enough to hide the claims (several short
+// units may be staged at once), few enough to keep the end of the work list
+// balanced across CTAs.
+constexpr int kClaimAheadTiles = 4;
 constexpr int kClaimAheadTilesMma = 8;
+constexpr int kSchedSlots = 4;              // staged units (descriptor + table slice)
 
 struct DecodeParams {
   float* part_acc;            // [rows][D], rows = num_seqs * num_heads * max_parts
@@ -107,16 +109,16 @@ struct DecodeLayout {
   static constexpr int kOffCombine = kRingBytes;
   static constexpr int kOffQ = kOffCombine + kCombineFloats * 4;
   static constexpr int kOffBars = kOffQ + 2 * kQBytes;        // 16-byte aligned
-  // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty, sched_go;
+  // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty;
   // tree merge of the tensor path: x_full, x_free, y_full, y_free
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 4;
-  static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[2], then sched[2]
-  static constexpr int kOffFlag = kOffUnits + 4 * sizeof(UnitDesc);
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 * kSchedSlots + 4;
+  static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[2], then sched[]
+  static constexpr int kOffFlag = kOffUnits + (2 + kSchedSlots) * sizeof(UnitDesc);
   static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of partitions per sequence
   static constexpr int kOffSlice = kOffPref + ((kCompactMaxSeqs + 1) * 4 + 15) / 16 * 16;
-  // table_slice: entries of one unit's block-table slice; two are staged
+  // table_slice: entries of one unit's block-table slice; kSchedSlots are staged
   static int smem_bytes(int table_slice) {
-    return 1024 /*alignment slack*/ + kOffSlice + ((2 * table_slice * 4 + 15) / 16) * 16;
+    return 1024 /*alignment slack*/ + kOffSlice + ((kSchedSlots * table_slice * 4 + 15) / 16) * 16;
   }
 };
 
@@ -471,15 +473,15 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   uint64_t* q_empty = q_full + 2;
   uint64_t* merge_bar = q_empty + 2;          // [0]: partials written, [1]: partials read
   uint64_t* sched_full = merge_bar + 2;       // scheduler -> copy warp, per staged unit
-  uint64_t* sched_empty = sched_full + 2;
-  uint64_t* sched_go = sched_empty + 2;       // copy warp -> scheduler: claim the next unit
-  uint64_t* x_full = sched_go + 1;            // tensor path: warps 2, 3 -> warps 0, 1
+  uint64_t* sched_empty = sched_full + kSchedSlots;
+  uint64_t* x_full = sched_empty + kSchedSlots;   // tensor path: warps 2, 3 -> warps 0, 1
   uint64_t* x_free = x_full + 1;
   uint64_t* y_full = x_free + 1;              // warp 1 -> warp 0
   uint64_t* y_free = y_full + 1;
   UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + Lay::kOffUnits);
   UnitDesc* sched = units + 2;
   int* abort_flag = reinterpret_cast<int*>(smem + Lay::kOffFlag);
+  int* issued_tiles = abort_flag + 1;         // copy warp's tile count, read by the scheduler
   int* pref = reinterpret_cast<int*>(smem + Lay::kOffPref);
   int32_t* slice = reinterpret_cast<int32_t*>(smem + Lay::kOffSlice);
 
@@ -499,15 +501,17 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], kConsumerWarps);
       mbar_init(&merge_bar[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sched_full[i], 32);
       mbar_init(&sched_empty[i], 1);
     }
-    mbar_init(sched_go, 1);
     mbar_init(x_full, 2);
     mbar_init(x_free, 2);
     mbar_init(y_full, 1);
     mbar_init(y_free, 1);
     *abort_flag = 0;
+    *issued_tiles = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -526,12 +530,21 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     const bool compact = p.num_seqs <= kCompactMaxSeqs;
     int total = p.total_units;
     if (compact) {
+      // all lengths in one round of loads, then the scan
+      int lens[kCompactMaxSeqs / 32];
+#pragma unroll
+      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
+        const int s = it * 32 + lane;
+        lens[it] = s < p.num_seqs ? __ldg(p.context_lens + s) : 0;
+      }
       int carry = 0;
-      for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
-        const int s = s0 + lane;
+#pragma unroll
+      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
+        if (it * 32 >= p.num_seqs) break;
+        const int s = it * 32 + lane;
         int np = 0;
         if (s < p.num_seqs) {
-          const int L = __ldg(p.context_lens + s);
+          const int L = lens[it];
           if (L >= 1 && L <= max_ctx)
             np = (L + p.partition_tokens - 1) / p.partition_tokens;
           else if (blockIdx.x == 0)
@@ -553,18 +566,38 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     // Tensor path: a unit serves the sequences of an aligned window of `cap`
     // whose blocks for the (whole) partition are the same physical blocks.
     const int cap = kMma ? min(kMmaRows / p.heads_per_cta, kMaxRun) : 1;
+    const int ahead = kMma ? kClaimAheadTilesMma : kClaimAheadTiles;
     bool ok = true;
+    int staged = 0;                           // tiles of the units staged so far
     for (int k = 0;; ++k) {
-      if (k >= 1) {                           // the copy warp is far enough into unit k-1
+      if (k >= 1) {                           // wait until the staged backlog runs low
         int w = 1;
-        if (lane == 0) w = mbar_wait(sched_go, (k - 1) & 1);
+        if (lane == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (staged - ld_volatile(issued_tiles) >= ahead) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              w = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
         if (!__shfl_sync(0xffffffffu, w, 0)) {
           ok = false;
           break;
         }
       }
+      const int sb = k % kSchedSlots;
+      if (k >= kSchedSlots) {                 // the slot's previous unit has been issued
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&sched_empty[sb], ((k / kSchedSlots) & 1) ^ 1);
+        if (!__shfl_sync(0xffffffffu, w, 0) || ld_volatile(abort_flag)) {
+          ok = false;
+          break;
+        }
+      }
+      int32_t* sl = slice + sb * slice_cap;
       UnitDesc d{-1, 0, 0, 0, 1};
-      int jb0 = 0, nb = 0;
       while (true) {
         int u = 0;
         if (lane == 0) u = atomicAdd(p.counter, 1);
@@ -587,74 +620,66 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
           seq = rem / p.kv_slices;
           kvs = rem - seq * p.kv_slices;
         }
-        const int ws = seq - seq % cap, nw = min(cap, p.num_seqs - ws);
+        // One round of loads: the window's lengths, and the table entries
+        // the partition can touch (for every window member on the tensor
+        // path), written to the slot's slice before the length is known.
+        const int ws = seq - seq % cap, nw = min(cap, p.num_seqs - ws), o = seq - ws;
+        const int t_begin = part * p.partition_tokens;
+        const int need = t_begin + p.partition_tokens;    // end of a whole partition
+        const int jb0 = t_begin / B;
+        const int nb_max = min((need - 1) / B - jb0 + 1, p.max_blocks_per_seq - jb0);
         int Lm = 0;                             // lane m: length of window member m
         if (lane < nw) Lm = __ldg(p.context_lens + ws + lane);
-        const int L = __shfl_sync(0xffffffffu, Lm, seq - ws);
+        unsigned same = 0xffffffffu;            // bit m: members m-1 and m name the same blocks
+        for (int i = lane; i < nb_max; i += 32) {
+          if (kMma && cap > 1) {
+            int32_t id[kMaxRun];
+#pragma unroll
+            for (int m = 0; m < kMaxRun; ++m)
+              id[m] = m < nw ? __ldg(p.block_tables +
+                                     static_cast<int64_t>(ws + m) * p.max_blocks_per_seq + jb0 + i)
+                             : -1;
+            unsigned bits = 1u;
+            int mine = id[0];
+#pragma unroll
+            for (int m = 1; m < kMaxRun; ++m) {
+              bits |= (id[m] == id[m - 1] ? 1u : 0u) << m;
+              if (m == o) mine = id[m];
+            }
+            same &= bits;
+            sl[i] = mine;
+          } else {
+            sl[i] = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0 + i);
+          }
+        }
+        const int L = __shfl_sync(0xffffffffu, Lm, o);
         if (L < 1 || L > max_ctx) {
           if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
           continue;
         }
-        const int t_begin = part * p.partition_tokens;
         if (t_begin >= L) continue;           // this sequence has no such partition
-        const int t_end = min(L, t_begin + p.partition_tokens);
-        jb0 = t_begin / B;
-        nb = (t_end - 1) / B - jb0 + 1;
         int nrun = 1;
-        const int need = t_begin + p.partition_tokens;
         if (kMma && cap > 1 && L >= need) {
           const unsigned full =
               __ballot_sync(0xffffffffu, lane < nw && Lm >= need && Lm <= max_ctx);
-          // bit m: members m-1 and m name the same blocks over the partition
-          unsigned same = 0xffffffffu;
-          for (int i0 = 0; i0 < nb; i0 += 32) {
-            const int i = i0 + lane;
-            if (i < nb) {
-              int32_t id[kMaxRun];
-#pragma unroll
-              for (int m = 0; m < kMaxRun; ++m)
-                id[m] = m < nw ? __ldg(p.block_tables +
-                                       static_cast<int64_t>(ws + m) * p.max_blocks_per_seq + jb0 + i)
-                               : -1;
-              unsigned bits = 1u;
-#pragma unroll
-              for (int m = 1; m < kMaxRun; ++m) bits |= (id[m] == id[m - 1] ? 1u : 0u) << m;
-              same &= bits;
-            }
-          }
           same = __reduce_and_sync(0xffffffffu, same);
           const unsigned link = same & full & (full << 1);   // bit m: m-1 and m run together
-          const int o = seq - ws;
           if (o > 0 && ((link >> o) & 1u)) continue;        // served by an earlier sequence's unit
           int e = o + 1;
           while (e < nw && ((link >> e) & 1u)) ++e;
           nrun = e - o;
         }
+        const int nb = (min(L, need) - 1) / B - jb0 + 1;
+        for (int i = lane; i < nb; i += 32) {  // each lane checks the entries it wrote
+          if (sl[i] < 0 || sl[i] >= p.num_blocks) {
+            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+            sl[i] = 0;
+          }
+        }
         const int kvh = kvs / p.subs;
         d = UnitDesc{seq, kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta, part, L, nrun};
+        staged += (min(L, need) - t_begin + kTile - 1) / kTile;
         break;
-      }
-      const int sb = k & 1;
-      if (k >= 2) {
-        int w = 1;
-        if (lane == 0) w = mbar_wait(&sched_empty[sb], ((k >> 1) & 1) ^ 1);
-        if (!__shfl_sync(0xffffffffu, w, 0) || ld_volatile(abort_flag)) {
-          ok = false;
-          break;
-        }
-      }
-      if (d.seq >= 0) {
-        int32_t* sl = slice + sb * slice_cap;
-        const int32_t* row =
-            p.block_tables + static_cast<int64_t>(d.seq) * p.max_blocks_per_seq + jb0;
-        for (int i = lane; i < nb; i += 32) {
-          int32_t id = __ldg(row + i);
-          if (id < 0 || id >= p.num_blocks) {
-            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;
-          }
-          sl[i] = id;
-        }
       }
       if (lane == 0) sched[sb] = d;
       mbar_arrive(&sched_full[sb]);             // every lane: its slice entries are written
@@ -664,6 +689,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       flag_error(p.err, PKV_DEVERR_TIMEOUT);
       st_volatile(abort_flag, 1);
     }
+    // No work is left to claim: the reduce kernel may be launched now (it
+    // waits for this grid to finish).
+    if (lane == 0) griddep_launch_dependents();
     return;
   }
 
@@ -683,8 +711,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
     while (true) {
-      const int sb = k & 1;
-      if (!mbar_wait(&sched_full[sb], (k >> 1) & 1)) {
+      const int sb = k % kSchedSlots;
+      if (!mbar_wait(&sched_full[sb], (k / kSchedSlots) & 1)) {
         ok = 0;
         break;
       }
@@ -709,9 +737,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
                   p.q + (static_cast<int64_t>(d.seq + b) * p.num_heads + d.head0) * D, qbytes,
                   &q_full[qb]);
       ++k;
-      const int go_at = max(0, n_tiles - (kMma ? kClaimAheadTilesMma : kClaimAheadTiles));
       for (int i = 0; i < n_tiles; ++i, ++issued) {
-        if (i == go_at) mbar_arrive(sched_go);
         const int st = issued % kStages;
         if (issued >= kStages && !mbar_wait(&empty_bar[st], ((issued / kStages) & 1) ^ 1)) {
           ok = 0;
@@ -739,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
           }
         }
         last_issued[st] = issued;
+        st_volatile(issued_tiles, issued + 1);
       }
       if (!ok) break;
       mbar_arrive(&sched_empty[sb]);          // the slice has been read
@@ -995,6 +1022,9 @@ struct ReduceParams {
 template <int D, typename O>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(O* out, const ReduceParams p) {
   constexpr int PER = D / 32;
+  // Launched as a programmatic dependent of the partition kernel: nothing is
+  // read before that grid has completed.
+  griddep_wait();
   const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= p.num_seqs * p.num_heads) return;
@@ -1115,19 +1145,28 @@ template <int D>
 static cudaError_t launch_reduce(void* out, int out_dtype, const ReduceParams& rp,
                                  cudaStream_t s) {
   const int warps = rp.num_seqs * rp.num_heads;
-  dim3 grid((warps + 3) / 4);
+  // Programmatic dependent launch: the reduce grid is set up while the
+  // partition grid drains and waits on it with griddepcontrol.wait.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (out_dtype) {
     case PKV_F32:
-      decode_reduce_kernel<D, float><<<grid, 128, 0, s>>>(static_cast<float*>(out), rp);
-      break;
+      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, float>, static_cast<float*>(out), rp);
     case PKV_F16:
-      decode_reduce_kernel<D, __half><<<grid, 128, 0, s>>>(static_cast<__half*>(out), rp);
-      break;
+      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, __half>, static_cast<__half*>(out),
+                                rp);
     default:
-      decode_reduce_kernel<D, __nv_bfloat16>
-          <<<grid, 128, 0, s>>>(static_cast<__nv_bfloat16*>(out), rp);
+      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, __nv_bfloat16>,
+                                static_cast<__nv_bfloat16*>(out), rp);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace pkv

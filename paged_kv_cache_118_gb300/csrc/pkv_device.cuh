@@ -70,6 +70,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Programmatic dependent launch: let the grid queued after this one start
+// launching; and, in that grid, wait until the grid before it has completed
+// and its memory writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 3-D tiled TMA load global -> shared, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar,
                                             int c0, int c1, int c2, uint64_t policy) {
