@@ -336,25 +336,20 @@ struct GroupState {
 
 // Tensor-core state of one consumer warp (grouped query heads): the warp owns
 // 8 tokens of every 32-token tile. q.k and p.v run as warp-level m16n8k16 /
-// m16n8k8 products with fp32 accumulation; the query heads of the CTA are the
-// 16 rows of A (rows past heads_per_cta, and rows 8..15, are zero). Lane
-// (g = lane/4, t = lane%4) holds head g's scores of tokens 2t, 2t+1 and its
-// output columns 8j + 2t, 8j + 2t + 1. P is fed as two halves in the input
-// format (p = hi + lo), which keeps p.v at close to fp32 accuracy.
-// K and V tiles are stored by TMA with the 128-byte swizzle: token row r of
-// the tile is NH = D/64 lines of 128 bytes (64 elements each), line
-// L = r * NH + h, and the 16-byte chunk c of line L sits at chunk c ^ (L % 8).
-// ldmatrix then meets no bank conflict for d = 64 and at most two-way ones
-// for d = 128, while one TMA box moves a whole block (whole rows).
+// m16n8k8 products with fp32 accumulation; the 16 rows of A are the query
+// heads of the unit's sequences (rows past them are zero). Lane
+// (g = lane/4, t = lane%4) holds the scores of rows g and g+8 for tokens 2t,
+// 2t+1 and their output columns 8j + 2t, 8j + 2t + 1. P is fed as two halves
+// in the input format (p = hi + lo), which keeps p.v at close to fp32 accuracy.
+// K and V tiles are stored by TMA with the 128-byte swizzle, each copy of R
+// rows line-major (swizzled_chunk): the eight rows one ldmatrix reads sit in
+// eight swizzle phases, so it meets no bank conflict, while one TMA box still
+// moves whole rows of a block.
 template <int D, typename T>
 struct MmaState {
   static constexpr int KS = D / 16;               // k-steps of q.k
   static constexpr int NT = D / 8;                // 8-column tiles of the output
   static constexpr int NH = D / 64;               // 128-byte lines per token row
-  static __device__ __forceinline__ uint32_t line_addr(const uint8_t* tile, int row, int chunk) {
-    const int line = row * NH + (chunk >> 3);
-    return smem_addr(tile + line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
-  }
   // A fragments: [0] row g, k 2t..; [1] row g+8, k 2t..; [2] row g, k 2t+8..; [3] row g+8, k 2t+8..
   uint32_t qa[KS][4];
   float o[NT][4];                                 // [0..1] row g, [2..3] row g+8
@@ -378,10 +373,10 @@ struct MmaState {
     lA = lB = 0.f;
   }
 
-  // kt, vt: the stage's K and V tiles; tok0: first token of this warp in the
-  // tile; valid: tokens of the tile that exist.
+  // kt, vt: the stage's K and V tiles, filled by copies of 2^rs rows; tok0:
+  // first token of this warp in the tile; valid: tokens of the tile that exist.
   __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int tok0, int valid,
-                                       float q_scale, int lane) {
+                                       float q_scale, int lane, int rs) {
     const int t = lane & 3;
     const int r = lane & 7;                       // row this lane addresses in ldmatrix
     const int mat = lane >> 3;                    // matrix this lane addresses
@@ -390,7 +385,7 @@ struct MmaState {
 #pragma unroll
     for (int kp = 0; kp < KS / 2; ++kp) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(line_addr(kt, tok0 + r, 4 * kp + mat), b0, b1, b2, b3);
+      ldsm_x4(swizzled_chunk<NH>(kt, tok0 + r, 4 * kp + mat, rs), b0, b1, b2, b3);
       T::mma16816(s, qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
       T::mma16816(s2, qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3],
                   b2, b3);
@@ -436,7 +431,7 @@ struct MmaState {
 #pragma unroll
     for (int nq = 0; nq < NT / 4; ++nq) {
       uint32_t b[4];
-      ldsm_x4_t(line_addr(vt, tok0 + r, 4 * nq + mat), b[0], b[1], b[2], b[3]);
+      ldsm_x4_t(swizzled_chunk<NH>(vt, tok0 + r, 4 * nq + mat, rs), b[0], b[1], b[2], b[3]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) b[i] &= keep;
 #pragma unroll
@@ -756,9 +751,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
         for (int c = 0; c < copies; ++c) {
           const int z = B >= kTile ? sl[t0 / B - jb0] * B + (t0 % B) : sl[t0 / B + c - jb0] * B;
           if constexpr (kMma) {
-            // 4-D view (64 elements, D/64 lines, head, slot): whole rows, swizzled
-            tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, 0, kvh, z, policy);
-            tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, 0, kvh, z, policy);
+            // 4-D view (64 elements, slot, head, D/64 lines): whole rows, swizzled
+            tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, z, kvh, 0, policy);
+            tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, z, kvh, 0, policy);
           } else {
             tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
             tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
@@ -794,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   const int base = grp * 8;
   const unsigned gmask = 0xffu << base;
   const int heads = p.heads_per_cta;
+  const int rows_shift = 31 - __clz(p.box_rows);  // rows per copy = 2^rows_shift
   using State = typename std::conditional<kMma, MmaState<D, T>, GroupState<D, GS, T>>::type;
   State gs;
   int consumed = 0;                               // tiles consumed (ring position)
@@ -830,7 +826,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       const int valid = min(kTile, t_end - (t_begin + i * kTile));
       if constexpr (kMma) {
         const uint8_t* kt = ring + st * Lay::kStageBytes;
-        if (warp * 8 < valid) gs.tile(kt, kt + Lay::kTileBytes, warp * 8, valid, p.q_scale, lane);
+        if (warp * 8 < valid)
+          gs.tile(kt, kt + Lay::kTileBytes, warp * 8, valid, p.q_scale, lane, rows_shift);
       } else {
         const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * Lay::kStageBytes);
         const uint16_t* vs = ks + kTile * D;

@@ -70,6 +70,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Address of 16-byte chunk `chunk` of row `row` in a K or V tile filled by
+// copies of R = 2^rs rows (R >= 8) through the 4-D swizzled view. Each copy
+// holds its rows line-major ([NH lines][R rows][128 bytes]); chunk c of the
+// 128-byte line at position n from the 1024-byte aligned tile sits at
+// c ^ (n % 8), the 128-byte swizzle, and n % 8 = row % 8.
+template <int NH>
+__device__ __forceinline__ uint32_t swizzled_chunk(const uint8_t* tile, int row, int chunk, int rs) {
+  const int line = ((row >> rs) * NH + (chunk >> 3)) * (1 << rs) + (row & ((1 << rs) - 1));
+  return smem_addr(tile + line * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
 // Programmatic dependent launch: let the grid queued after this one start
 // launching; and, in that grid, wait until the grid before it has completed
 // and its memory writes are visible.

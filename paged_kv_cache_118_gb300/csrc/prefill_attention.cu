@@ -77,14 +77,6 @@ __device__ __forceinline__ void store_elem(void* out, int64_t i, float v, int dt
   else static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
 }
 
-// Address of 16-byte chunk `chunk` of key row `row` in a swizzled K or V tile
-// (row r is D/64 lines of 128 bytes; chunk c of line L sits at c ^ (L % 8)).
-template <int D>
-__device__ __forceinline__ uint32_t tile_addr(const uint8_t* tile, int row, int chunk) {
-  const int line = row * (D / 64) + (chunk >> 3);
-  return smem_addr(tile + line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
-}
-
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -92,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lay = Layout<D>;
   constexpr int KS = D / 16;           // k-steps of q.k
   constexpr int NT = D / 8;            // 8-column tiles of the output
+  const int rows_shift = 31 - __clz(p.box_rows);  // rows per TMA copy = 2^rows_shift
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -162,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           id = 0;
         }
         const int z = id * B + (B >= kTile ? t0 % B : 0);
-        tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, 0, kvh, z, policy);
-        tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, 0, kvh, z, policy);
+        tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, z, kvh, 0, policy);
+        tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, z, kvh, 0, policy);
       }
       last_issued[st] = i;
     }
@@ -224,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kp = 0; kp < KS / 2; ++kp) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(tile_addr<D>(kt, 8 * nt + r, 4 * kp + mat), b0, b1, b2, b3);
+          ldsm_x4(swizzled_chunk<D / 64>(kt, 8 * nt + r, 4 * kp + mat, rows_shift), b0, b1, b2, b3);
           T::mma16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
           T::mma16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2],
                       qa[2 * kp + 1][3], b2, b3);
@@ -290,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // matrices: (keys 0-7, d-tile 2jq), (keys 8-15, 2jq), (keys 0-7, 2jq+1), (keys 8-15, 2jq+1)
           const int krow = 16 * ks + 8 * (mat & 1) + r;
           uint32_t b[4];
-          ldsm_x4_t(tile_addr<D>(vt, krow, 2 * jq + (mat >> 1)), b[0], b[1], b[2], b[3]);
+          ldsm_x4_t(swizzled_chunk<D / 64>(vt, krow, 2 * jq + (mat >> 1), rows_shift), b[0], b[1],
+                    b[2], b[3]);
           if (kmax < kTile) {
             const int k0 = 16 * ks + 2 * t;
             const uint32_t keep0 = (k0 < kmax ? 0x0000ffffu : 0u) | (k0 + 1 < kmax ? 0xffff0000u : 0u);

@@ -42,15 +42,17 @@ bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    // 4-D view: x = 64 elements (128 bytes), y = which 64-element line of the
-    // head, z = KV head, w = slot; box 64 x D/64 x 1 x rows with the 128-byte
-    // swizzle: one copy moves whole rows of a block.
-    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64),
-                          static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(slots)};
-    cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2,
-                             static_cast<cuuint64_t>(D) * 2 * num_kv_heads};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(D / 64), 1,
-                         static_cast<cuuint32_t>(box_rows)};
+    // 4-D view: x = 64 elements (128 bytes), y = slot, z = KV head, w = which
+    // 64-element line of the head; box 64 x rows x 1 x D/64 with the 128-byte
+    // swizzle. One copy moves whole rows of a block, stored line-major: all
+    // rows' first 128 bytes, then all rows' second 128 bytes, so that eight
+    // consecutive rows of one line fall in eight different swizzle phases.
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(slots),
+                          static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(D / 64)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2 * num_kv_heads,
+                             static_cast<cuuint64_t>(D) * 2, 128};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1,
+                         static_cast<cuuint32_t>(D / 64)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
