@@ -78,12 +78,13 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(kernel_src: str, bytes_per_launch: float):
-    """DRAM bytes per decode launch, from the committed ncu summary, if it was
-    taken on the kernel source as it is now (its sha256 is recorded there).
-    The captured launch's traffic is scaled to this run's launch by the ratio
-    of algorithmic bytes (same batch, a few tokens longer or shorter)."""
-    path = os.path.join(ROOT, "profiles", "decode_partition_opt13b.md")
+def profile_traffic(config: str, kernel_src: str, bytes_per_launch: float):
+    """DRAM bytes per decode launch, from the committed ncu summary of this
+    workload, if it was taken on the kernel source as it is now (its sha256 is
+    recorded there). The captured launch's traffic is scaled to this run's
+    launch by the ratio of algorithmic bytes (same batch, a few tokens longer
+    or shorter)."""
+    path = os.path.join(ROOT, "profiles", f"decode_partition_{config}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -394,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = load_peaks()
     src = os.path.join(ROOT, "paged_kv_cache_118_gb300", "csrc", "decode_attention.cu")
-    traffic = profile_traffic(src, float(np.mean(per_call))) if args.config == "opt13b" else None
+    traffic = profile_traffic(args.config, src, float(np.mean(per_call)))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
