@@ -18,9 +18,10 @@
 //    GS query heads that share the KV head (online softmax in base 2, with the
 //    rescale taken only when the maximum grows by more than 2^8). The groups
 //    are merged at the end into one unnormalised partial (m, l, acc[d]).
-//  * decode_reduce_kernel — one warp per (sequence, query head) merges the
-//    partition partials: M = max m_p, Z = sum l_p 2^(m_p - M),
-//    o = sum acc_p 2^(m_p - M) / Z, rounded to the output type.
+//  * decode_reduce_kernel — one warp (four for rows of many partitions) per
+//    (sequence, query head) merges the partition partials: M = max m_p,
+//    Z = sum l_p 2^(m_p - M), o = sum acc_p 2^(m_p - M) / Z, rounded to the
+//    output type, with several partitions' loads in flight at once.
 // Every wait on an mbarrier has a time limit (see pkv_device.cuh); a block id
 // or context length out of range is skipped and reported through err_flag.
 
@@ -93,16 +94,20 @@ struct UnitDesc {
                               // partition are identical (shared prefix), served together
 };
 
-// A 4-stage ring; on the tensor path GS is the row capacity (kMmaRows).
+// The ring has 4 stages (5 on the tensor path, whose merge needs less room);
+// on the tensor path GS is the row capacity (kMmaRows).
 template <int D, int GS, bool kMma = false>
 struct DecodeLayout {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = kMma ? 5 : 4;
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kTile * kRowBytes;        // K (or V) of one stage
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kQBytes = GS * D * 2;                  // query rows of one unit (capacity)
-  static constexpr int kCombineFloats = kConsumerWarps * GS * (D + 2);
+  // merge area: per warp and row D + 2 floats; on the tensor path two warps'
+  // fragments, (D/8 + 1) float4s per lane
+  static constexpr int kCombineFloats =
+      kMma ? 2 * (D / 8 + 1) * 32 * 4 : kConsumerWarps * GS * (D + 2);
   static constexpr int kChunks = D / 64;                      // 16-byte pieces per lane per row
   static constexpr int kE = 8 * kChunks;                      // elements per lane per row
   // offsets (bytes) from the 1024-aligned base
@@ -110,8 +115,8 @@ struct DecodeLayout {
   static constexpr int kOffQ = kOffCombine + kCombineFloats * 4;
   static constexpr int kOffBars = kOffQ + 2 * kQBytes;        // 16-byte aligned
   // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty;
-  // tree merge of the tensor path: x_full, x_free, y_full, y_free
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 * kSchedSlots + 4;
+  // tree merge of the tensor path: x_full, x_free, y_full
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 * kSchedSlots + 3;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[2], then sched[]
   static constexpr int kOffFlag = kOffUnits + (2 + kSchedSlots) * sizeof(UnitDesc);
   static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of partitions per sequence
@@ -375,6 +380,9 @@ struct MmaState {
 
   // kt, vt: the stage's K and V tiles, filled by copies of 2^rs rows; tok0:
   // first token of this warp in the tile; valid: tokens of the tile that exist.
+  // kTwo: rows 8..15 hold query rows (a run of sequences); without them their
+  // softmax is skipped and their products stay zero.
+  template <bool kTwo>
   __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int tok0, int valid,
                                        float q_scale, int lane, int rs) {
     const int t = lane & 3;
@@ -394,14 +402,20 @@ struct MmaState {
     const bool v0 = tk < valid, v1 = tk + 1 < valid;
     const float a0 = v0 ? (s[0] + s2[0]) * q_scale : -INFINITY;
     const float a1 = v1 ? (s[1] + s2[1]) * q_scale : -INFINITY;
-    const float b0s = v0 ? (s[2] + s2[2]) * q_scale : -INFINITY;
-    const float b1s = v1 ? (s[3] + s2[3]) * q_scale : -INFINITY;
-    float tmA = fmaxf(a0, a1), tmB = fmaxf(b0s, b1s);
+    float tmA = fmaxf(a0, a1);
     tmA = fmaxf(tmA, __shfl_xor_sync(0xffffffffu, tmA, 1));
     tmA = fmaxf(tmA, __shfl_xor_sync(0xffffffffu, tmA, 2));
-    tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 1));
-    tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 2));
-    const bool needA = tmA > mA + kRescaleThreshold, needB = tmB > mB + kRescaleThreshold;
+    const bool needA = tmA > mA + kRescaleThreshold;
+    float b0s = -INFINITY, b1s = -INFINITY, tmB = -INFINITY;
+    bool needB = false;
+    if constexpr (kTwo) {
+      b0s = v0 ? (s[2] + s2[2]) * q_scale : -INFINITY;
+      b1s = v1 ? (s[3] + s2[3]) * q_scale : -INFINITY;
+      tmB = fmaxf(b0s, b1s);
+      tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 1));
+      tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 2));
+      needB = tmB > mB + kRescaleThreshold;
+    }
     if (__any_sync(0xffffffffu, needA || needB)) {
       const float cA = needA ? ex2(mA - tmA) : 1.f, cB = needB ? ex2(mB - tmB) : 1.f;
       if (needA) mA = tmA;
@@ -418,14 +432,20 @@ struct MmaState {
     }
     const float pa0 = a0 == -INFINITY ? 0.f : ex2(a0 - mA);
     const float pa1 = a1 == -INFINITY ? 0.f : ex2(a1 - mA);
-    const float pb0 = b0s == -INFINITY ? 0.f : ex2(b0s - mB);
-    const float pb1 = b1s == -INFINITY ? 0.f : ex2(b1s - mB);
     lA += pa0 + pa1;
-    lB += pb0 + pb1;
     // P as two halves in the input format: p = hi + lo
-    const uint32_t hA = T::pack(pa0, pa1), hB = T::pack(pb0, pb1);
-    const float2 fA = T::to_float2(hA), fB = T::to_float2(hB);
-    const uint32_t lAo = T::pack(pa0 - fA.x, pa1 - fA.y), lBo = T::pack(pb0 - fB.x, pb1 - fB.y);
+    const uint32_t hA = T::pack(pa0, pa1);
+    const float2 fA = T::to_float2(hA);
+    const uint32_t lAo = T::pack(pa0 - fA.x, pa1 - fA.y);
+    uint32_t hB = 0u, lBo = 0u;
+    if constexpr (kTwo) {
+      const float pb0 = b0s == -INFINITY ? 0.f : ex2(b0s - mB);
+      const float pb1 = b1s == -INFINITY ? 0.f : ex2(b1s - mB);
+      lB += pb0 + pb1;
+      hB = T::pack(pb0, pb1);
+      const float2 fB = T::to_float2(hB);
+      lBo = T::pack(pb0 - fB.x, pb1 - fB.y);
+    }
     // V rows of tokens past the tile's end may hold anything: zero their halves.
     const uint32_t keep = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
 #pragma unroll
@@ -444,8 +464,9 @@ struct MmaState {
 
 // Persistent: each CTA takes units of work — (context partition, sequence,
 // KV-head slice), partition-major — from a global counter until none is
-// left. The producer warp fetches the next unit, its slice of the block table
-// and its query rows while the consumers still work on the current one.
+// left. The scheduler and copy warps fetch the next unit, its slice of the
+// block table and its query rows while the consumers still work on the
+// current one.
 // kMma: grouped query heads on the tensor path (MmaState; K/V tiles stored
 // with 128-byte swizzle by 64-element halves; GS is then the row capacity, 16:
 // p.heads_per_cta heads of each of up to 16 / p.heads_per_cta sequences that
@@ -472,7 +493,6 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   uint64_t* x_full = sched_empty + kSchedSlots;   // tensor path: warps 2, 3 -> warps 0, 1
   uint64_t* x_free = x_full + 1;
   uint64_t* y_full = x_free + 1;              // warp 1 -> warp 0
-  uint64_t* y_free = y_full + 1;
   UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + Lay::kOffUnits);
   UnitDesc* sched = units + 2;
   int* abort_flag = reinterpret_cast<int*>(smem + Lay::kOffFlag);
@@ -502,9 +522,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       mbar_init(&sched_empty[i], 1);
     }
     mbar_init(x_full, 2);
-    mbar_init(x_free, 2);
+    mbar_init(x_free, 1);
     mbar_init(y_full, 1);
-    mbar_init(y_free, 1);
     *abort_flag = 0;
     *issued_tiles = 0;
     fence_barrier_init();
@@ -826,8 +845,14 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       const int valid = min(kTile, t_end - (t_begin + i * kTile));
       if constexpr (kMma) {
         const uint8_t* kt = ring + st * Lay::kStageBytes;
-        if (warp * 8 < valid)
-          gs.tile(kt, kt + Lay::kTileBytes, warp * 8, valid, p.q_scale, lane, rows_shift);
+        if (warp * 8 < valid) {
+          if (rows > 8)
+            gs.template tile<true>(kt, kt + Lay::kTileBytes, warp * 8, valid, p.q_scale, lane,
+                                   rows_shift);
+          else
+            gs.template tile<false>(kt, kt + Lay::kTileBytes, warp * 8, valid, p.q_scale, lane,
+                                    rows_shift);
+        }
       } else {
         const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * Lay::kStageBytes);
         const uint16_t* vs = ks + kTile * D;
@@ -844,12 +869,11 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     if constexpr (kMma) {
       // Tree merge of the four warps' states, fragment by fragment (every warp
       // holds the same rows and columns in the same registers): warps 2 and 3
-      // hand theirs to warps 0 and 1, warp 1 hands the sum to warp 0, which
-      // writes the unit's partials.
+      // hand theirs to warps 0 and 1 through two slots, warp 1 hands the sum
+      // to warp 0 through its own slot, and warp 0 writes the unit's partials.
       using M = MmaState<D, T>;
       constexpr int kFrag4 = M::NT + 1;                 // float4s per lane: o, then (mA, mB, lA, lB)
       float4* xb = reinterpret_cast<float4*>(combine);  // [2][kFrag4][32]
-      float4* yb = xb + 2 * kFrag4 * 32;                // [kFrag4][32]
       auto put = [&](float4* dst) {
 #pragma unroll
         for (int jn = 0; jn < M::NT; ++jn)
@@ -883,25 +907,22 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
         }
       };
       if (warp >= 2) {
-        if (k >= 1) wait_or_abort(x_free, (k - 1) & 1);
+        if (k >= 1) wait_or_abort(x_free, (k - 1) & 1);    // both slots read by warp 0
         put(xb + (warp - 2) * kFrag4 * 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(x_full);
       } else {
         wait_or_abort(x_full, k & 1);
         take(xb + warp * kFrag4 * 32);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(x_free);
         if (warp == 1) {
-          if (k >= 1) wait_or_abort(y_free, (k - 1) & 1);
-          put(yb);
+          put(xb + kFrag4 * 32);                  // each lane rewrites only what it read
           __syncwarp();
           if (lane == 0) mbar_arrive(y_full);
         } else {
           wait_or_abort(y_full, k & 1);
-          take(yb);
+          take(xb + kFrag4 * 32);
           __syncwarp();
-          if (lane == 0) mbar_arrive(y_free);
+          if (lane == 0) mbar_arrive(x_free);
           const int g = lane >> 2, t = lane & 3;
           float lsA = gs.lA, lsB = gs.lB;
           lsA += __shfl_xor_sync(0xffffffffu, lsA, 1);
@@ -1016,55 +1037,104 @@ struct ReduceParams {
   int max_context;
 };
 
-template <int D, typename O>
+// kWarps warps per row (1 for short contexts: four rows per CTA; 4 for long
+// ones: the partitions of a row are split round-robin over the warps and the
+// warps' sums are added in a fixed order). The order of the additions
+// depends only on kWarps and the number of partitions.
+template <int D, typename O, int kWarps>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(O* out, const ReduceParams p) {
-  constexpr int PER = D / 32;
+  constexpr int PER = D / 32;                   // output elements per lane
+  constexpr int kBatch = 4;                     // partitions whose loads a warp issues together
+  __shared__ float part_o[kWarps][PER][32];
+  __shared__ float part_z[kWarps];
+  __shared__ float part_m[kWarps];
   // Launched as a programmatic dependent of the partition kernel: nothing is
   // read before that grid has completed.
   griddep_wait();
-  const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (w >= p.num_seqs * p.num_heads) return;
+  const int wr = warp % kWarps;                 // warp within the row
+  const int w = blockIdx.x * (4 / kWarps) + warp / kWarps;   // row: (sequence, query head)
+  if (w >= p.num_seqs * p.num_heads) return;    // whole rows only: uniform across a row's warps
   const int seq = w / p.num_heads;
   O* dst = out + static_cast<int64_t>(w) * D + lane * PER;
   const int L = __ldg(p.context_lens + seq);
   if (L < 1 || L > p.max_context) {
+    if (wr == 0) {
 #pragma unroll
-    for (int k = 0; k < PER; ++k) store_out<O>(dst + k, 0.f);
+      for (int k = 0; k < PER; ++k) store_out<O>(dst + k, 0.f);
+    }
     return;
   }
   const int np = (L + p.partition_tokens - 1) / p.partition_tokens;
   const int64_t row0 = static_cast<int64_t>(w) * p.max_parts;
   float M = -INFINITY;
-  for (int i = lane; i < np; i += 32) M = fmaxf(M, p.part_ml[row0 + i].x);
+  for (int i = wr * 32 + lane; i < np; i += kWarps * 32) M = fmaxf(M, p.part_ml[row0 + i].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float Z = 0.f;
-  for (int i = lane; i < np; i += 32) {
-    const float2 ml = p.part_ml[row0 + i];
-    Z = fmaf(ml.y, ex2(ml.x - M), Z);
-  }
+  if constexpr (kWarps > 1) {
+    if (lane == 0) part_m[wr] = M;
+    __syncthreads();
+    M = part_m[0];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    for (int j = 1; j < kWarps; ++j) M = fmaxf(M, part_m[j]);
+  }
+  // This warp takes partitions wr, wr + kWarps, ... in order, kBatch of them
+  // with their loads in flight together.
   float acc[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  for (int i = 0; i < np; ++i) {
-    const float wgt = ex2(p.part_ml[row0 + i].x - M);
-    const float* src = p.part_acc + (row0 + i) * D + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] = fmaf(v.x, wgt, acc[0]);
-      acc[1] = fmaf(v.y, wgt, acc[1]);
-      acc[2] = fmaf(v.z, wgt, acc[2]);
-      acc[3] = fmaf(v.w, wgt, acc[3]);
-    } else {
+  float Z = 0.f;
+  for (int i0 = wr; i0 < np; i0 += kWarps * kBatch) {
+    float2 ml[kBatch];
+    float v[kBatch][PER];
 #pragma unroll
-      for (int k = 0; k < PER; ++k) acc[k] = fmaf(src[k], wgt, acc[k]);
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = i0 + b * kWarps;
+      ml[b] = i < np ? p.part_ml[row0 + i] : make_float2(-INFINITY, 0.f);
+      const float* src = p.part_acc + (row0 + (i < np ? i : 0)) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        v[b][0] = x.x;
+        v[b][1] = x.y;
+        v[b][2] = x.z;
+        v[b][3] = x.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < PER; ++k) v[b][k] = src[k];
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (i0 + b * kWarps < np) {
+        const float wgt = ex2(ml[b].x - M);
+        Z = fmaf(ml[b].y, wgt, Z);
+#pragma unroll
+        for (int k = 0; k < PER; ++k) acc[k] = fmaf(v[b][k], wgt, acc[k]);
+      }
     }
   }
+  if constexpr (kWarps == 1) {
 #pragma unroll
-  for (int k = 0; k < PER; ++k) store_out<O>(dst + k, acc[k] / Z);
+    for (int k = 0; k < PER; ++k) store_out<O>(dst + k, acc[k] / Z);
+  } else {
+    if (lane == 0) part_z[wr] = Z;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) part_o[wr][k][lane] = acc[k];
+    __syncthreads();
+    if (wr == 0) {
+      float Zt = part_z[0];
+#pragma unroll
+      for (int j = 1; j < kWarps; ++j) Zt += part_z[j];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        float o = part_o[0][k][lane];
+#pragma unroll
+        for (int j = 1; j < kWarps; ++j) o += part_o[j][k][lane];
+        store_out<O>(dst + k, o / Zt);
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1138,32 +1208,42 @@ static cudaError_t dispatch_gs(bool mma, int gs, const CUtensorMap& tk, const CU
   }
 }
 
+template <int D, int W>
+static cudaError_t launch_reduce_as(void* out, int out_dtype, const ReduceParams& rp,
+                                    cudaLaunchConfig_t& cfg) {
+  switch (out_dtype) {
+    case PKV_F32:
+      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, float, W>, static_cast<float*>(out),
+                                rp);
+    case PKV_F16:
+      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, __half, W>,
+                                static_cast<__half*>(out), rp);
+    default:
+      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, __nv_bfloat16, W>,
+                                static_cast<__nv_bfloat16*>(out), rp);
+  }
+}
+
 template <int D>
 static cudaError_t launch_reduce(void* out, int out_dtype, const ReduceParams& rp,
                                  cudaStream_t s) {
-  const int warps = rp.num_seqs * rp.num_heads;
+  const int rows = rp.num_seqs * rp.num_heads;
   // Programmatic dependent launch: the reduce grid is set up while the
   // partition grid drains and waits on it with griddepcontrol.wait.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.gridDim = dim3(rows);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  switch (out_dtype) {
-    case PKV_F32:
-      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, float>, static_cast<float*>(out), rp);
-    case PKV_F16:
-      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, __half>, static_cast<__half*>(out),
-                                rp);
-    default:
-      return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<D, __nv_bfloat16>,
-                                static_cast<__nv_bfloat16*>(out), rp);
-  }
+  // four warps per row once rows have many partitions
+  if (rp.max_parts > 16) return launch_reduce_as<D, 4>(out, out_dtype, rp, cfg);
+  cfg.gridDim = dim3((rows + 3) / 4);
+  return launch_reduce_as<D, 1>(out, out_dtype, rp, cfg);
 }
 
 }  // namespace pkv
