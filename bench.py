@@ -403,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": dtype_name, "data": "synthetic",
         "config": {"workload": f"{args.config}_decode", "num_seqs": S, "num_heads": H,
                    "num_kv_heads": Hkv, "head_size": D, "block_size": B, "layers": layers,
-                   "context_tokens_first_step": int(L0.sum()), "partition_tokens": pt or 512,
+                   "context_tokens_first_step": int(L0.sum()), "partition_tokens": pk.pkv_decode_partition_tokens(width, B, pt),
                    "num_blocks": num_blocks, "seed": args.seed,
                    "l2": "inputs larger than L2 (each step reads every layer's pool)",
                    **({"groups": st["groups"], "beams": st["beams"],

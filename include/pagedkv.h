@@ -71,10 +71,11 @@ const char* pkv_version(void);
  * h / (num_heads / num_kv_heads).
  *
  * The context is processed in partitions of `partition_tokens` tokens (0 picks
- * 512; otherwise a positive multiple of 32, at most 4096): one CTA per
- * (sequence, KV head, partition) produces an unnormalised partial, and a second
- * kernel merges the partials of each (sequence, head) with the global
- * denominator.
+ * 512, or 1024 when max_blocks_per_seq * block_size >= 32768, see
+ * pkv_decode_partition_tokens; otherwise a positive multiple of 32, at most
+ * 4096): each (sequence, KV head, partition) produces an unnormalised partial,
+ * and a second kernel merges the partials of each (sequence, head) with the
+ * global denominator.
  *
  *   out          device, [num_seqs][num_heads][head_size] of out_dtype (F16, BF16 or F32)
  *   q            device, [num_seqs][num_heads][head_size] of kv_dtype
@@ -97,6 +98,11 @@ const char* pkv_version(void);
  * ------------------------------------------------------------------------ */
 size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_size,
                                  int max_blocks_per_seq, int block_size, int partition_tokens);
+
+/* The partition size a decode call with these arguments uses: partition_tokens
+ * itself when nonzero, else 512, or 1024 when the tables can hold 32768 tokens
+ * or more (long contexts then produce half as many partials). Never fails. */
+int pkv_decode_partition_tokens(int max_blocks_per_seq, int block_size, int partition_tokens);
 
 pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
                                       const void* k_cache, const void* v_cache, int kv_dtype,

@@ -34,6 +34,7 @@ SIGNATURES = {
     "pkv_status_string": (ctypes.c_char_p, [_c_int]),
     "pkv_version": (ctypes.c_char_p, []),
     "pkv_decode_workspace_size": (_c_sz, [_c_int] * 6),
+    "pkv_decode_partition_tokens": (_c_int, [_c_int] * 3),
     "pkv_paged_attention_decode": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                             _c_int, _c_f, _c_int, _vp, _c_sz, _vp, _vp]),
@@ -110,6 +111,12 @@ def _need_cuda(*ts):
 
 
 # ---------------------------------------------------------------- kernels
+
+def pkv_decode_partition_tokens(max_blocks_per_seq: int, block_size: int,
+                                partition_tokens: int = 0) -> int:
+    """The partition size a decode call with these arguments uses (0 = the default)."""
+    return int(lib.pkv_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens))
+
 
 def pkv_decode_workspace_size(num_seqs: int, num_heads: int, head_size: int,
                               max_blocks_per_seq: int, block_size: int,

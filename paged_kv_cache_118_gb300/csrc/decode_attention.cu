@@ -1250,8 +1250,17 @@ static cudaError_t launch_reduce(void* out, int out_dtype, const ReduceParams& r
 
 using namespace pkv;
 
-static int effective_partition(int partition_tokens) {
-  return partition_tokens == 0 ? 512 : partition_tokens;
+// 0 picks 512 tokens, or 1024 when the tables can hold 32K tokens or more: long
+// contexts then pay for half as many units and partials.
+static int effective_partition(int partition_tokens, int max_blocks_per_seq, int block_size) {
+  if (partition_tokens != 0) return partition_tokens;
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+  return max_ctx >= 32768 ? 1024 : 512;
+}
+
+extern "C" int pkv_decode_partition_tokens(int max_blocks_per_seq, int block_size,
+                                           int partition_tokens) {
+  return effective_partition(partition_tokens, max_blocks_per_seq, block_size);
 }
 
 // A 32-token tile is a whole number of blocks, or a whole number of tiles is a block.
@@ -1260,7 +1269,7 @@ static bool block_size_ok(int b) { return b >= 1 && b <= 256 && (b & (b - 1)) ==
 extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_size,
                                             int max_blocks_per_seq, int block_size,
                                             int partition_tokens) {
-  const int pt = effective_partition(partition_tokens);
+  const int pt = effective_partition(partition_tokens, max_blocks_per_seq, block_size);
   if (num_seqs < 0 || num_heads < 1 || head_size < 1 || max_blocks_per_seq < 1 ||
       block_size < 1 || pt < 1)
     return 0;
@@ -1276,7 +1285,7 @@ extern "C" pkv_status pkv_paged_attention_decode(
     int num_heads, int num_kv_heads, int head_size, int num_blocks, int block_size,
     int max_blocks_per_seq, float scale, int partition_tokens, void* workspace,
     size_t workspace_bytes, int32_t* err_flag, void* stream) {
-  const int pt = effective_partition(partition_tokens);
+  const int pt = effective_partition(partition_tokens, max_blocks_per_seq, block_size);
   if (num_seqs < 0 || num_seqs > 65535) return PKV_EINVAL;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)

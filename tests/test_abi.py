@@ -38,8 +38,10 @@ def test_workspace_size_formula():
     # rows = S * H * ceil(max_blocks * B / partition); each row holds D floats and an
     # (m, l) pair (the pairs padded to 16 bytes), then a 16-byte work counter
     for S, H, D, mb, B, pt in [(64, 40, 128, 128, 16, 512), (8, 32, 128, 8192, 16, 512),
-                               (3, 4, 64, 5, 4, 32), (1, 1, 64, 1, 8, 0)]:
-        parts = -(-(mb * B) // (pt or 512))
+                               (3, 4, 64, 5, 4, 32), (1, 1, 64, 1, 8, 0), (8, 32, 128, 8192, 16, 0)]:
+        eff = pt or (1024 if mb * B >= 32768 else 512)
+        assert pk.pkv_decode_partition_tokens(mb, B, pt) == eff
+        parts = -(-(mb * B) // eff)
         rows = S * H * parts
         assert pk.pkv_decode_workspace_size(S, H, D, mb, B, pt) == rows * D * 4 + -(-rows * 8 // 16) * 16 + 16
 

@@ -69,9 +69,11 @@ def test_refuses_batches_beyond_the_built_in_scratch():
     batch, cache, tables, ctx = _case((64,), 8, 8, 16, "f16", 3)
     q = dev(batch.q, "f16")
     out = torch.zeros_like(q)
-    # a table wide enough that the partials would not fit: rows of 128 floats + (m, l)
+    # a table wide enough that the partials would not fit: rows of 128 floats + (m, l),
+    # in partitions of the default size for so wide a table (1024 tokens)
     parts = pk.NOALLOC_SCRATCH_BYTES // (8 * (128 * 4 + 8)) + 1
-    width = parts * 512 // 16
+    width = parts * 1024 // 16
+    assert pk.pkv_decode_partition_tokens(width, 16) == 1024
     wide = torch.full((1, width), -1, dtype=torch.int32, device="cuda")
     wide[0, :tables.shape[1]] = tables[0]
     assert pk.pkv_decode_workspace_size(1, 8, 128, width, 16) > pk.NOALLOC_SCRATCH_BYTES
