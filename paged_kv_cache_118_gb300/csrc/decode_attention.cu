@@ -56,8 +56,8 @@ constexpr int kMaxRun = 8;                  // sequences one tensor-path unit se
 // staged units are left to issue: enough to hide the claims (several short
 // units may be staged at once), few enough to keep the end of the work list
 // balanced across CTAs.
-constexpr int kClaimAheadTiles = 4;
-constexpr int kClaimAheadTilesMma = 8;
+constexpr int kClaimAheadTiles = 2;
+constexpr int kClaimAheadTilesMma = 16;
 constexpr int kSchedSlots = 4;              // staged units (descriptor + table slice)
 
 struct DecodeParams {
