@@ -52,6 +52,7 @@ constexpr int kCompactMaxSeqs = 1024;       // batches up to this size get a com
 constexpr int kMmaHeads = 8;                // query heads of one KV head a tensor-path CTA serves
 constexpr int kMmaRows = 16;                // rows of its products: heads x sequences of a run
 constexpr int kMaxRun = 8;                  // sequences one tensor-path unit serves at most
+constexpr int kMaxGroupParts = 4095;        // group claims need F < 2^12 (packed with flags)
 // The scheduler claims another unit whenever fewer than this many tiles of
 // staged units are left to issue: enough to hide the claims (several short
 // units may be staged at once), few enough to keep the end of the work list
@@ -113,14 +114,16 @@ struct DecodeLayout {
   // offsets (bytes) from the 1024-aligned base
   static constexpr int kOffCombine = kRingBytes;
   static constexpr int kOffQ = kOffCombine + kCombineFloats * 4;
-  static constexpr int kOffBars = kOffQ + 2 * kQBytes;        // 16-byte aligned
-  // full, empty (ring); q_full, q_empty; merge; sched_full, sched_empty;
+  static constexpr int kOffBars = kOffQ + kQBytes;            // 16-byte aligned
+  // full, empty (ring); q_full, q_empty (one query buffer: the consumers
+  // copy it to registers when a unit starts); merge; sched_full, sched_empty;
   // tree merge of the tensor path: x_full, x_free, y_full
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 * kSchedSlots + 3;
-  static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[2], then sched[]
-  static constexpr int kOffFlag = kOffUnits + (2 + kSchedSlots) * sizeof(UnitDesc);
+  static constexpr int kNumBars = 2 * kStages + 1 + 1 + 2 + 2 * kSchedSlots + 3;
+  static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[1], then sched[]
+  static constexpr int kOffFlag = kOffUnits + (1 + kSchedSlots) * sizeof(UnitDesc);
   static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of partitions per sequence
-  static constexpr int kOffSlice = kOffPref + ((kCompactMaxSeqs + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kOffGroup = kOffPref + ((kCompactMaxSeqs + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kOffSlice = kOffGroup + (kCompactMaxSeqs * 2 + 15) / 16 * 16;  // after group info
   // table_slice: entries of one unit's block-table slice; kSchedSlots are staged
   static int smem_bytes(int table_slice) {
     return 1024 /*alignment slack*/ + kOffSlice + ((kSchedSlots * table_slice * 4 + 15) / 16) * 16;
@@ -486,18 +489,19 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* q_full = empty_bar + kStages;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* merge_bar = q_empty + 2;          // [0]: partials written, [1]: partials read
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* merge_bar = q_empty + 1;          // [0]: partials written, [1]: partials read
   uint64_t* sched_full = merge_bar + 2;       // scheduler -> copy warp, per staged unit
   uint64_t* sched_empty = sched_full + kSchedSlots;
   uint64_t* x_full = sched_empty + kSchedSlots;   // tensor path: warps 2, 3 -> warps 0, 1
   uint64_t* x_free = x_full + 1;
   uint64_t* y_full = x_free + 1;              // warp 1 -> warp 0
   UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + Lay::kOffUnits);
-  UnitDesc* sched = units + 2;
+  UnitDesc* sched = units + 1;
   int* abort_flag = reinterpret_cast<int*>(smem + Lay::kOffFlag);
   int* issued_tiles = abort_flag + 1;         // copy warp's tile count, read by the scheduler
   int* pref = reinterpret_cast<int*>(smem + Lay::kOffPref);
+  uint16_t* ginfo = reinterpret_cast<uint16_t*>(smem + Lay::kOffGroup);
   int32_t* slice = reinterpret_cast<int32_t*>(smem + Lay::kOffSlice);
 
   const int warp = threadIdx.x >> 5;
@@ -512,11 +516,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], kConsumerWarps);
-      mbar_init(&merge_bar[i], kConsumerWarps);
-    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, kConsumerWarps);
+    for (int i = 0; i < 2; ++i) mbar_init(&merge_bar[i], kConsumerWarps);
     for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sched_full[i], 32);
       mbar_init(&sched_empty[i], 1);
@@ -533,38 +535,81 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   // ------------------------------------------------------------ scheduler warp
   // Claims units from the global counter, resolves each one (sequence,
   // partition, head slice; on the tensor path the run of sequences that share
-  // the partition's blocks) and stages its block-table slice, one unit ahead of
-  // the copy warp, so that none of this latency falls between two units of the
-  // copy stream.
+  // the partition's blocks) and stages its block-table slice ahead of the copy
+  // warp, so that none of this latency falls between two units of the copy
+  // stream.
   if (warp == kConsumerWarps + 1) {
-    // The work list. For batches of up to kCompactMaxSeqs sequences only the
-    // units that exist are numbered, sequence-major (a prefix sum of each
-    // sequence's partition count, then a binary search per unit); larger
-    // batches number every (partition, sequence, slice) and skip the empty ones.
     const bool compact = p.num_seqs <= kCompactMaxSeqs;
+    // Tensor path: the sequences of an aligned window of `cap` (a power of two)
+    // may be served together.
+    int cap = 1;
+    if (kMma) {
+      const int c = min(kMmaRows / p.heads_per_cta, kMaxRun);
+      cap = 1 << (31 - __clz(c));
+    }
+    const bool grouping = kMma && cap > 1 && compact && p.max_parts <= kMaxGroupParts;
+    // The work list. For batches of up to kCompactMaxSeqs sequences only the
+    // units that exist are numbered, sequence-major (a prefix sum of claims
+    // per sequence, then a binary search per claim); larger batches number
+    // every (partition, sequence, slice) and skip the empty ones.
+    //
+    // Groups (tensor path): consecutive sequences of a window whose first
+    // blocks are the same physical block (a shared prefix) form a group. The
+    // partitions that are whole for every member, F of them, are claimed once
+    // for the group by its first sequence; each member claims only its own
+    // partitions from F on. A group claim checks the members' table entries
+    // for that partition and serves the runs of identical ones (normally one
+    // run: the whole group) as units.
     int total = p.total_units;
     if (compact) {
-      // all lengths in one round of loads, then the scan
-      int lens[kCompactMaxSeqs / 32];
+      // all lengths (and first blocks) in one round of loads, then the scan
+      int lens[kCompactMaxSeqs / 32], fblk[kCompactMaxSeqs / 32];
 #pragma unroll
       for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
         const int s = it * 32 + lane;
         lens[it] = s < p.num_seqs ? __ldg(p.context_lens + s) : 0;
+        fblk[it] = (grouping && s < p.num_seqs)
+                       ? __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq)
+                       : -1;
       }
       int carry = 0;
 #pragma unroll
       for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
         if (it * 32 >= p.num_seqs) break;
         const int s = it * 32 + lane;
-        int np = 0;
-        if (s < p.num_seqs) {
-          const int L = lens[it];
-          if (L >= 1 && L <= max_ctx)
-            np = (L + p.partition_tokens - 1) / p.partition_tokens;
-          else if (blockIdx.x == 0)
-            flag_error(p.err, PKV_DEVERR_CONTEXT);
+        const int L = lens[it];
+        const bool valid = s < p.num_seqs && L >= 1 && L <= max_ctx;
+        if (s < p.num_seqs && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+        const int np = valid ? (L + p.partition_tokens - 1) / p.partition_tokens : 0;
+        int c = np;                           // claims of this sequence, in partitions
+        if (grouping) {
+          const int whole = valid ? L / p.partition_tokens : 0;
+          const int fb = fblk[it];
+          const int fb_prev = __shfl_up_sync(0xffffffffu, fb, 1);
+          const int valid_prev = __shfl_up_sync(0xffffffffu, valid ? 1 : 0, 1);
+          // windows never straddle the 32 lanes: cap divides 32
+          const bool link = valid && valid_prev && (s & (cap - 1)) != 0 && fb >= 0 && fb == fb_prev;
+          const unsigned starts = __ballot_sync(0xffffffffu, !link);
+          const int hd = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // group's first lane
+          const int wb = lane & ~(cap - 1);
+          const unsigned later = starts & ~(0xffffffffu >> (31 - hd));
+          const int nx = later ? min(__ffs(later) - 1, wb + cap) : wb + cap;  // past the group
+          int fmin = whole;
+#pragma unroll
+          for (int j = 0; j < kMaxRun; ++j) {
+            const int lj = (wb + j) & 31;
+            const int v = __shfl_sync(0xffffffffu, whole, lj);
+            if (j < cap && wb + j >= hd && wb + j < nx) fmin = min(fmin, v);
+          }
+          uint16_t gi = 0;
+          if (nx - hd > 1) {
+            const bool member = lane != hd;
+            if (member) c = np - fmin;
+            gi = static_cast<uint16_t>((fmin << 4) | ((nx - hd - 1) << 1) | (member ? 1 : 0));
+          }
+          if (s < p.num_seqs) ginfo[s] = gi;
         }
-        int x = np;
+        int x = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -577,12 +622,12 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       __syncwarp();
       total = carry * p.kv_slices;
     }
-    // Tensor path: a unit serves the sequences of an aligned window of `cap`
-    // whose blocks for the (whole) partition are the same physical blocks.
-    const int cap = kMma ? min(kMmaRows / p.heads_per_cta, kMaxRun) : 1;
     const int ahead = kMma ? kClaimAheadTilesMma : kClaimAheadTiles;
     bool ok = true;
     int staged = 0;                           // tiles of the units staged so far
+    // runs of the last group claim still to be staged
+    unsigned pend = 0, plink = 0;
+    int pseq = 0, ppart = 0, pkvs = 0, pLm = 0, pgs = 0;
     for (int k = 0;; ++k) {
       if (k >= 1) {                           // wait until the staged backlog runs low
         int w = 1;
@@ -611,89 +656,126 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
         }
       }
       int32_t* sl = slice + sb * slice_cap;
-      UnitDesc d{-1, 0, 0, 0, 1};
-      while (true) {
-        int u = 0;
-        if (lane == 0) u = atomicAdd(p.counter, 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
-        if (u >= total) break;
-        int part, seq, kvs;
-        if (compact) {
-          int lo = 0, hi = p.num_seqs;        // largest lo with pref[lo] * slices <= u
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (pref[mid] * p.kv_slices <= u) lo = mid; else hi = mid;
-          }
-          seq = lo;
-          const int rem = u - pref[lo] * p.kv_slices;
-          part = rem / p.kv_slices;
-          kvs = rem - part * p.kv_slices;
-        } else {
-          part = u / per_part;
-          const int rem = u - part * per_part;
-          seq = rem / p.kv_slices;
-          kvs = rem - seq * p.kv_slices;
-        }
-        // One round of loads: the window's lengths, and the table entries
-        // the partition can touch (for every window member on the tensor
-        // path), written to the slot's slice before the length is known.
-        const int ws = seq - seq % cap, nw = min(cap, p.num_seqs - ws), o = seq - ws;
-        const int t_begin = part * p.partition_tokens;
-        const int need = t_begin + p.partition_tokens;    // end of a whole partition
-        const int jb0 = t_begin / B;
-        const int nb_max = min((need - 1) / B - jb0 + 1, p.max_blocks_per_seq - jb0);
-        int Lm = 0;                             // lane m: length of window member m
-        if (lane < nw) Lm = __ldg(p.context_lens + ws + lane);
-        unsigned same = 0xffffffffu;            // bit m: members m-1 and m name the same blocks
-        for (int i = lane; i < nb_max; i += 32) {
-          if (kMma && cap > 1) {
-            int32_t id[kMaxRun];
-#pragma unroll
-            for (int m = 0; m < kMaxRun; ++m)
-              id[m] = m < nw ? __ldg(p.block_tables +
-                                     static_cast<int64_t>(ws + m) * p.max_blocks_per_seq + jb0 + i)
-                             : -1;
-            unsigned bits = 1u;
-            int mine = id[0];
-#pragma unroll
-            for (int m = 1; m < kMaxRun; ++m) {
-              bits |= (id[m] == id[m - 1] ? 1u : 0u) << m;
-              if (m == o) mine = id[m];
-            }
-            same &= bits;
-            sl[i] = mine;
-          } else {
-            sl[i] = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0 + i);
-          }
-        }
-        const int L = __shfl_sync(0xffffffffu, Lm, o);
-        if (L < 1 || L > max_ctx) {
-          if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-          continue;
-        }
-        if (t_begin >= L) continue;           // this sequence has no such partition
-        int nrun = 1;
-        if (kMma && cap > 1 && L >= need) {
-          const unsigned full =
-              __ballot_sync(0xffffffffu, lane < nw && Lm >= need && Lm <= max_ctx);
-          same = __reduce_and_sync(0xffffffffu, same);
-          const unsigned link = same & full & (full << 1);   // bit m: m-1 and m run together
-          if (o > 0 && ((link >> o) & 1u)) continue;        // served by an earlier sequence's unit
-          int e = o + 1;
-          while (e < nw && ((link >> e) & 1u)) ++e;
-          nrun = e - o;
-        }
-        const int nb = (min(L, need) - 1) / B - jb0 + 1;
-        for (int i = lane; i < nb; i += 32) {  // each lane checks the entries it wrote
-          if (sl[i] < 0 || sl[i] >= p.num_blocks) {
+      // Writes this unit's slice (entries of `seq`'s table from jb0), checking ids.
+      auto load_slice = [&](int seq, int jb0, int nb) {
+        const int32_t* row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + jb0;
+        for (int i = lane; i < nb; i += 32) {
+          int32_t id = __ldg(row + i);
+          if (id < 0 || id >= p.num_blocks) {
             flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            sl[i] = 0;
+            id = 0;
           }
+          sl[i] = id;
         }
-        const int kvh = kvs / p.subs;
-        d = UnitDesc{seq, kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta, part, L, nrun};
-        staged += (min(L, need) - t_begin + kTile - 1) / kTile;
-        break;
+      };
+      UnitDesc d{-1, 0, 0, 0, 1};
+      if (pend) {
+        // the next run of the last group claim
+        const int o = __ffs(pend) - 1;
+        pend &= pend - 1;
+        int e = o + 1;
+        while (e < pgs && ((plink >> e) & 1u)) ++e;
+        const int t_begin = ppart * p.partition_tokens;
+        const int jb0 = t_begin / B;
+        load_slice(pseq + o, jb0, (t_begin + p.partition_tokens - 1) / B - jb0 + 1);
+        const int L = __shfl_sync(0xffffffffu, pLm, o);
+        const int kvh = pkvs / p.subs;
+        d = UnitDesc{pseq + o, kvh * p.group + (pkvs - kvh * p.subs) * p.heads_per_cta, ppart, L,
+                     e - o};
+        staged += p.partition_tokens / kTile;
+      } else {
+        while (true) {
+          int u = 0;
+          if (lane == 0) u = atomicAdd(p.counter, 1);
+          u = __shfl_sync(0xffffffffu, u, 0);
+          if (u >= total) break;
+          int part, seq, kvs;
+          int F = 0, gs = 1;
+          bool member = false;
+          if (compact) {
+            int lo = 0, hi = p.num_seqs;      // largest lo with pref[lo] * slices <= u
+            while (hi - lo > 1) {
+              const int mid = (lo + hi) >> 1;
+              if (pref[mid] * p.kv_slices <= u) lo = mid; else hi = mid;
+            }
+            seq = lo;
+            const int rem = u - pref[lo] * p.kv_slices;
+            part = rem / p.kv_slices;
+            kvs = rem - part * p.kv_slices;
+            if (grouping) {
+              const int gi = ginfo[seq];
+              F = gi >> 4;
+              gs = ((gi >> 1) & 7) + 1;
+              member = gi & 1;
+              if (member) part += F;
+            }
+          } else {
+            part = u / per_part;
+            const int rem = u - part * per_part;
+            seq = rem / p.kv_slices;
+            kvs = rem - seq * p.kv_slices;
+          }
+          const int t_begin = part * p.partition_tokens;
+          const int need = t_begin + p.partition_tokens;    // end of a whole partition
+          const int jb0 = t_begin / B;
+          const int kvh = kvs / p.subs;
+          const int head0 = kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta;
+          if (!member && gs > 1 && part < F) {
+            // Group claim: every member's partition is whole. One round of
+            // loads: the members' lengths and table entries; the first run's
+            // slice (the first member's entries) goes straight to the slot.
+            const int nbw = (need - 1) / B - jb0 + 1;
+            const int Lm = lane < gs ? __ldg(p.context_lens + seq + lane) : 0;
+            unsigned same = 0xffffffffu;      // bit m: members m-1 and m name the same blocks
+            for (int i = lane; i < nbw; i += 32) {
+              int32_t id[kMaxRun];
+#pragma unroll
+              for (int m = 0; m < kMaxRun; ++m)
+                id[m] = m < gs ? __ldg(p.block_tables +
+                                       static_cast<int64_t>(seq + m) * p.max_blocks_per_seq + jb0 + i)
+                               : -1;
+              unsigned bits = 1u;
+#pragma unroll
+              for (int m = 1; m < kMaxRun; ++m) bits |= (id[m] == id[m - 1] ? 1u : 0u) << m;
+              same &= bits;
+              int32_t v = id[0];
+              if (v < 0 || v >= p.num_blocks) {
+                flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+                v = 0;
+              }
+              sl[i] = v;
+            }
+            same = __reduce_and_sync(0xffffffffu, same);
+            const unsigned full =
+                __ballot_sync(0xffffffffu, lane < gs && Lm >= need && Lm <= max_ctx);
+            const unsigned link = same & full & (full << 1);
+            int e = 1;
+            while (e < gs && ((link >> e) & 1u)) ++e;
+            // later runs start where the chain breaks
+            pend = ~link & ((1u << gs) - 1u) & ~((1u << e) - 1u);
+            plink = link;
+            pseq = seq;
+            ppart = part;
+            pkvs = kvs;
+            pLm = Lm;
+            pgs = gs;
+            d = UnitDesc{seq, head0, part, __shfl_sync(0xffffffffu, Lm, 0), e};
+            staged += p.partition_tokens / kTile;
+            break;
+          }
+          // A unit of one sequence.
+          const int L = __ldg(p.context_lens + seq);
+          if (L < 1 || L > max_ctx) {
+            if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+            continue;
+          }
+          if (t_begin >= L) continue;         // this sequence has no such partition
+          const int t_end = min(L, need);
+          load_slice(seq, jb0, (t_end - 1) / B - jb0 + 1);
+          d = UnitDesc{seq, head0, part, L, 1};
+          staged += (t_end - t_begin + kTile - 1) / kTile;
+          break;
+        }
       }
       if (lane == 0) sched[sb] = d;
       mbar_arrive(&sched_full[sb]);             // every lane: its slice entries are written
@@ -738,8 +820,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       const int jb0 = t_begin / B;
       const int kvh = d.head0 / p.group;
       const int32_t* sl = slice + sb * slice_cap;
-      const int qb = k & 1;
-      if (k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) {
+      const int qb = 0;                       // one query buffer
+      if (k >= 1 && !mbar_wait(&q_empty[qb], (k - 1) & 1)) {
         ok = 0;
         break;
       }
@@ -785,8 +867,8 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       mbar_arrive(&sched_empty[sb]);          // the slice has been read
     }
     // Publish the end of the work (or the abort) to the consumers.
-    const int qb = k & 1;
-    if (ok && k >= 2 && !mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1)) ok = 0;
+    const int qb = 0;
+    if (ok && k >= 1 && !mbar_wait(&q_empty[qb], (k - 1) & 1)) ok = 0;
     if (!ok) {
       flag_error(p.err, PKV_DEVERR_TIMEOUT);
       st_volatile(abort_flag, 1);
@@ -813,9 +895,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   State gs;
   int consumed = 0;                               // tiles consumed (ring position)
   for (int k = 0;; ++k) {
-    const int qb = k & 1;
+    const int qb = 0;
     UnitDesc ud{-2, 0, 0, 0, 1};
-    if (!ld_volatile(abort_flag) && mbar_wait(&q_full[qb], (k >> 1) & 1)) ud = units[qb];
+    if (!ld_volatile(abort_flag) && mbar_wait(&q_full[qb], k & 1)) ud = units[qb];
     if (ud.seq == -1) break;                      // all work done
     if (ud.seq == -2) {                           // abort: nothing more is coming
       if (lane == 0) {
