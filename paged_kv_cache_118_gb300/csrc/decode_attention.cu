@@ -1399,8 +1399,9 @@ extern "C" pkv_status pkv_paged_attention_decode(
   const int box_rows = std::min(block_size, kTile);
   CUtensorMap tk, tv;
   const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
-  if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, mma) ||
-      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, mma))
+  const CacheView view = mma ? kRowsSwizzled : kRowsPlain;
+  if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, view) ||
+      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, view))
     return PKV_ECUDA;
 
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_heads * parts;

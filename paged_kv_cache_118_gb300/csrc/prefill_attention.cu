@@ -1,4 +1,5 @@
-// Paged chunked-prefill attention for sm_103a.
+// Paged chunked-prefill attention for sm_103a on the 5th-generation tensor
+// cores.
 //
 // What is computed: a sequence with L tokens in its cache receives a chunk of
 // C query tokens, its last C positions (their keys and values already
@@ -8,18 +9,24 @@
 // follow their position; "079｜vLLM 与 PagedAttention" §2 for the single global
 // denominator). Decode is the case C = 1.
 //
-// How (FlashAttention-2 structure over a paged cache, warp-level tensor cores):
-//  * one CTA per (tile of 64 rows, KV head, sequence); a row is one (query
-//    token, query head of the KV head's group), so 64/G tokens per tile;
-//  * a producer warp streams 32-key tiles of K and V over the causal range
-//    only, one 4-D TMA box per physical block with the 128-byte swizzle, into
-//    a 4-stage ring completing on mbarriers (bounded waits);
-//  * each of four consumer warps owns 16 rows and every key: S = Q K^T with
-//    mma.m16n8k16 (Q fragments in registers), causal mask and online softmax
-//    (base 2, lazy rescale) in the accumulator layout, P fed straight from
-//    the score fragments into P V with mma.m16n8k16 (bfloat16 P as hi + lo
-//    halves), fp32 accumulation; a warp skips tiles past its last query.
-// A chunk or context length out of range is skipped and reported.
+// How (one CTA per tile of 128 query rows, KV head and sequence; a row is one
+// (query token, query head of the KV head's group), so 128/G tokens per tile):
+//  * warp 0 streams 64-key tiles of K and V over the causal range only, one
+//    TMA copy per physical block and 128-byte line (128-byte swizzle), into a
+//    3-stage ring completing on mbarriers;
+//  * warp 1 owns the tensor memory (256 columns: two 64-column score buffers
+//    and the D-column output) and issues, from one thread, S = Q K^T
+//    (M = 128, N = 64, K = D) into a score buffer and O += P V (M = 128,
+//    N = D, K = 64) into the output, each followed by a commit to an mbarrier;
+//    the next tile's S is issued before this tile's P V;
+//  * warps 4-7 run the softmax, one thread per query row (its TMEM lane): the
+//    row's 64 scores come out of TMEM, the causal mask and a base-2 online
+//    softmax with lazy rescale (the output row in TMEM is rescaled only when
+//    the running maximum grows by more than 2^8) give P, which is written to
+//    shared memory in the layout the P V product reads; the output row is
+//    divided by the row sum at the end.
+// Every wait is bounded; a chunk or context length out of range is skipped
+// and reported.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -37,11 +44,12 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int kTile = 32;              // keys per pipeline stage
-constexpr int kRows = 64;              // query rows per CTA (16 per consumer warp)
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;
+constexpr int kRows = 128;             // query rows per CTA: the TMEM lanes
+constexpr int kKeys = 64;              // keys per tile
+constexpr int kStages = 3;
+constexpr int kThreads = 256;          // warp 0: copies; warp 1: MMA; warps 4-7: softmax
+constexpr int kSoftmaxWarp0 = 4;
+constexpr uint32_t kTmemCols = 256;    // S0 [0, 64), S1 [64, 128), O [128, 128 + D)
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -59,22 +67,59 @@ struct Params {
   int block_size;
   int max_blocks_per_seq;
   int max_query_len;
-  int box_rows;                        // min(block_size, kTile)
+  int box_rows;                        // rows per TMA copy: min(block_size, kKeys)
   float q_scale;                       // scale * log2(e)
 };
 
+// Shared memory, from a 1024-byte aligned base. Every operand is stored as
+// 128-byte rows with the 128-byte swizzle (16-byte chunk c of the row at
+// position n sits at c ^ (n % 8)), 8-row groups 1024 bytes apart:
+//  Q: D/64 column blocks of 128 rows (A of S, K-major);
+//  each stage: K then V, each D/64 line blocks of 64 key rows (B of S,
+//  K-major; B of P V, MN-major with the next 64 columns one line block on);
+//  P: two buffers of 128 rows x 64 keys (A of P V, K-major).
 template <int D>
 struct Layout {
-  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int NH = D / 64;
+  static constexpr int kQBytes = kRows * D * 2;
+  static constexpr int kLineBytes = kKeys * 128;          // one line block of a K or V tile
+  static constexpr int kTileBytes = NH * kLineBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kSmem = 1024 + kRingBytes + 2 * kStages * 8;
+  static constexpr int kPBytes = kRows * kKeys * 2;
+  static constexpr int kOffStages = kQBytes;
+  static constexpr int kOffP = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffBars = kOffP + 2 * kPBytes;
+  // stage_full[S], stage_empty[S], q_full, s_full[2], s_free[2], p_full[2], pv_done[2], drain
+  static constexpr int kNumBars = 2 * kStages + 1 + 8 + 1;
+  static constexpr int kOffTmem = kOffBars + kNumBars * 8;
+  static constexpr int kSmem = 1024 + kOffTmem + 16;
 };
 
-__device__ __forceinline__ void store_elem(void* out, int64_t i, float v, int dtype) {
-  if (dtype == PKV_F32) static_cast<float*>(out)[i] = v;
-  else if (dtype == PKV_F16) static_cast<__half*>(out)[i] = __float2half_rn(v);
-  else static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+template <typename T>
+__device__ __forceinline__ void store_row(void* out, int out_dtype, int64_t base, const float* v,
+                                          int n) {
+  // n values of one output row, 16 bytes at a time
+  if (out_dtype == PKV_F32) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
+    for (int i = 0; i < n / 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + base);
+    for (int i = 0; i < n / 8; ++i) {
+      uint4 w;
+      if (out_dtype == PKV_F16) {
+        w.x = F16::pack(v[8 * i], v[8 * i + 1]);
+        w.y = F16::pack(v[8 * i + 2], v[8 * i + 3]);
+        w.z = F16::pack(v[8 * i + 4], v[8 * i + 5]);
+        w.w = F16::pack(v[8 * i + 6], v[8 * i + 7]);
+      } else {
+        w.x = BF16::pack(v[8 * i], v[8 * i + 1]);
+        w.y = BF16::pack(v[8 * i + 2], v[8 * i + 3]);
+        w.z = BF16::pack(v[8 * i + 4], v[8 * i + 5]);
+        w.w = BF16::pack(v[8 * i + 6], v[8 * i + 7]);
+      }
+      d[i] = w;
+    }
+  }
 }
 
 template <int D, typename T>
@@ -82,15 +127,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params p) {
   using Lay = Layout<D>;
-  constexpr int KS = D / 16;           // k-steps of q.k
-  constexpr int NT = D / 8;            // 8-column tiles of the output
-  const int rows_shift = 31 - __clz(p.box_rows);  // rows per TMA copy = 2^rows_shift
+  constexpr int NH = Lay::NH;
+  constexpr bool kBF16 = std::is_same<T, BF16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* ring = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::kRingBytes);
-  uint64_t* empty_bar = full_bar + kStages;
+  uint8_t* qtile = smem;
+  uint8_t* stages = smem + Lay::kOffStages;
+  uint8_t* pbuf = smem + Lay::kOffP;
+  uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
+  uint64_t* stage_empty = stage_full + kStages;
+  uint64_t* q_full = stage_empty + kStages;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* drain = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -112,219 +165,263 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tok0 >= C) return;
   const int tok_end = min(C, tok0 + tokens_per_tile);
   const int kv_end = L - C + tok_end;                      // keys this tile can see
-  const int n_tiles = (kv_end + kTile - 1) / kTile;
+  const int n_tiles = (kv_end + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], kConsumerWarps);
+      mbar_init(&stage_full[i], 1);
+      mbar_init(&stage_empty[i], 1);
     }
+    mbar_init(q_full, kRows);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], kRows);
+      mbar_init(&p_full[i], kRows);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(drain, 1);
     fence_barrier_init();
   }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
 
-  // ------------------------------------------------------------ producer
-  if (warp == kConsumerWarps) {
-    if (lane != 0) return;
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-    const uint64_t policy = l2_evict_first_policy();
-    const uint32_t copy_bytes = static_cast<uint32_t>(p.box_rows) * D * 2;
-    const int32_t* row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
-    int last_issued[kStages];
+  if (warp == 0) {
+    // ---------------------------------------------------------- copies
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const uint64_t policy = l2_evict_first_policy();
+      const int R = p.box_rows;
+      const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
+      const int32_t* row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
+      int last_issued[kStages];
 #pragma unroll
-    for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
+      for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !mbar_wait(&stage_empty[st], ((j / kStages) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        const int t0 = j * kKeys;
+        const int valid = min(kKeys, kv_end - t0);
+        const int copies = (valid + R - 1) / R;            // copies of R rows cover the keys
+        uint8_t* kdst = stages + st * Lay::kStageBytes;
+        uint8_t* vdst = kdst + Lay::kTileBytes;
+        mbar_arrive_expect_tx(&stage_full[st], 2u * NH * copies * copy_bytes);
+        for (int c = 0; c < copies; ++c) {
+          const int tk = t0 + c * R;                        // first key of the copy
+          int32_t id = __ldg(row + tk / B);
+          if (id < 0 || id >= p.num_blocks) {
+            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+            id = 0;
+          }
+          const int z = id * B + tk % B;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            tma_load_4d(kdst + h * Lay::kLineBytes + c * copy_bytes, &tm_k, &stage_full[st], 0, z,
+                        kvh, h, policy);
+            tma_load_4d(vdst + h * Lay::kLineBytes + c * copy_bytes, &tm_v, &stage_full[st], 0, z,
+                        kvh, h, policy);
+          }
+        }
+        last_issued[st] = j;
+      }
+      if (!ok) {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        for (int st = 0; st < kStages; ++st)
+          if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = mma_idesc_f16(kBF16, kRows, kKeys, false);
+      constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
+      bool ok = mbar_wait(q_full, 0);
+      tc_fence_after();
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kStages, b = j & 1;
+        if (!mbar_wait(&stage_full[st], (j / kStages) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&s_free[b], ((j - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint8_t* kt = stages + st * Lay::kStageBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int h = ks >> 2, off = (ks & 3) * 32;      // 64-element column block, 16 of them
+          const uint64_t ad = smem_desc_sw128(qtile + h * kRows * 128 + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kt + h * Lay::kLineBytes + off, 16, 1024);
+          tc_mma_f16(tbase + b * kKeys, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[b]);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j % kStages, b = j & 1;
+        if (!mbar_wait(&p_full[b], (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint8_t* vt = stages + st * Lay::kStageBytes + Lay::kTileBytes;
+        const uint8_t* pt = pbuf + b * Lay::kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(pt + kk * 32, 16, 1024);
+          // V as B, MN-major: 16 keys are two 8-row groups; the next 64 columns
+          // of D are one line block (kLineBytes) on
+          const uint64_t bd = smem_desc_sw128(vt + kk * 16 * 128, Lay::kLineBytes, 1024);
+          tc_mma_f16(tbase + 128, ad, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[b]);
+        tc_commit(&stage_empty[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) ok = issue_s(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
+      if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      // everything issued has completed before the columns are freed
+      tc_commit(drain);
+      mbar_wait(drain, 0);
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ---------------------------------------------------------- softmax
+    const int r = (warp - kSoftmaxWarp0) * 32 + lane;      // query row = TMEM lane
+    const uint32_t tl = tbase + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    const int tok = tok0 + r / G;
+    const int head = kvh * G + r % G;
+    const bool live = tok < C;
+    const int pos = L - C + tok;
+    // this row of Q into the A layout of S (zeros past the chunk)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<int64_t>(qs + (live ? tok : 0)) * p.num_heads + head) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const int h = c >> 3, cc = c & 7;
+        uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(qtile + h * kRows * 128 + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kStages;
-      if (i >= kStages && !mbar_wait(&empty_bar[st], ((i / kStages) & 1) ^ 1)) {
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&s_full[b], (j >> 1) & 1)) {
         ok = false;
         break;
       }
-      const int t0 = i * kTile;
-      const int valid = min(kTile, kv_end - t0);
-      const int copies = B >= kTile ? 1 : (valid + B - 1) / B;
-      uint8_t* kdst = ring + st * Lay::kStageBytes;
-      uint8_t* vdst = kdst + Lay::kTileBytes;
-      mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
-      for (int c = 0; c < copies; ++c) {
-        const int j = B >= kTile ? t0 / B : t0 / B + c;
-        int32_t id = __ldg(row + j);
-        if (id < 0 || id >= p.num_blocks) {
-          flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-          id = 0;
-        }
-        const int z = id * B + (B >= kTile ? t0 % B : 0);
-        tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, z, kvh, 0, policy);
-        tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, z, kvh, 0, policy);
+      tc_fence_after();
+      float s[kKeys];
+#pragma unroll
+      for (int h = 0; h < kKeys / 32; ++h) {
+        uint32_t raw[32];
+        tmem_ld32(tl + b * kKeys + h * 32, raw);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[h * 32 + i] = __uint_as_float(raw[i]);
       }
-      last_issued[st] = i;
-    }
-    if (!ok) {
-      flag_error(p.err, PKV_DEVERR_TIMEOUT);
-      for (int st = 0; st < kStages; ++st)
-        if (last_issued[st] >= 0) mbar_wait(&full_bar[st], (last_issued[st] / kStages) & 1);
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  const int g = lane >> 2, t = lane & 3;
-  const int r0 = warp * 16;            // this warp's first row of the tile
-  // rows r0 + g and r0 + g + 8: (token, head) and their query positions
-  int tokA = tok0 + (r0 + g) / G, tokB = tok0 + (r0 + g + 8) / G;
-  const int headA = kvh * G + (r0 + g) % G, headB = kvh * G + (r0 + g + 8) % G;
-  const bool liveA = tokA < C, liveB = tokB < C;
-  const int posA = L - C + tokA, posB = L - C + tokB;
-  // the warp's last query position: tiles past it are skipped
-  const int warp_last_tok = min(C - 1, tok0 + (r0 + 15) / G);
-  const int warp_kv_end = L - C + warp_last_tok + 1;
-
-  uint32_t qa[KS][4];
-  {
-    const uint16_t* qrA = p.q + (static_cast<int64_t>(qs + (liveA ? tokA : 0)) * p.num_heads + headA) * D;
-    const uint16_t* qrB = p.q + (static_cast<int64_t>(qs + (liveB ? tokB : 0)) * p.num_heads + headB) * D;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = liveA ? __ldg(reinterpret_cast<const uint32_t*>(qrA + 16 * ks + 2 * t)) : 0u;
-      qa[ks][1] = liveB ? __ldg(reinterpret_cast<const uint32_t*>(qrB + 16 * ks + 2 * t)) : 0u;
-      qa[ks][2] = liveA ? __ldg(reinterpret_cast<const uint32_t*>(qrA + 16 * ks + 8 + 2 * t)) : 0u;
-      qa[ks][3] = liveB ? __ldg(reinterpret_cast<const uint32_t*>(qrB + 16 * ks + 8 + 2 * t)) : 0u;
-    }
-  }
-  float o[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-  const int r = lane & 7, mat = lane >> 3;
-
-  bool ok = true;
-  for (int i = 0; i < n_tiles; ++i) {
-    const int st = i % kStages;
-    if (!mbar_wait(&full_bar[st], (i / kStages) & 1)) {
-      ok = false;
-      break;
-    }
-    const int t0 = i * kTile;
-    if (t0 < warp_kv_end) {
-      const uint8_t* kt = ring + st * Lay::kStageBytes;
-      const uint8_t* vt = kt + Lay::kTileBytes;
-      // S = Q K^T for 4 groups of 8 keys
-      float s[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int kp = 0; kp < KS / 2; ++kp) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(swizzled_chunk<D / 64>(kt, 8 * nt + r, 4 * kp + mat, rows_shift), b0, b1, b2, b3);
-          T::mma16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
-          T::mma16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2],
-                      qa[2 * kp + 1][3], b2, b3);
-        }
-      }
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);
       // causal mask (also hides keys past the context and rows past the chunk)
-      float tmA = -INFINITY, tmB = -INFINITY;
+      const int key0 = j * kKeys;
+      float mt = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = t0 + 8 * nt + 2 * t + e;
-          s[nt][e] = (liveA && key <= posA) ? s[nt][e] * p.q_scale : -INFINITY;
-          s[nt][2 + e] = (liveB && key <= posB) ? s[nt][2 + e] * p.q_scale : -INFINITY;
-          tmA = fmaxf(tmA, s[nt][e]);
-          tmB = fmaxf(tmB, s[nt][2 + e]);
-        }
-      tmA = fmaxf(tmA, __shfl_xor_sync(0xffffffffu, tmA, 1));
-      tmA = fmaxf(tmA, __shfl_xor_sync(0xffffffffu, tmA, 2));
-      tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 1));
-      tmB = fmaxf(tmB, __shfl_xor_sync(0xffffffffu, tmB, 2));
-      const bool needA = tmA > mA + kRescaleThreshold, needB = tmB > mB + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, needA || needB)) {
-        const float cA = needA ? ex2(mA - tmA) : 1.f, cB = needB ? ex2(mB - tmB) : 1.f;
-        if (needA) mA = tmA;
-        if (needB) mB = tmB;
-        lA *= cA;
-        lB *= cB;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          o[j][0] *= cA;
-          o[j][1] *= cA;
-          o[j][2] *= cB;
-          o[j][3] *= cB;
-        }
+      for (int i = 0; i < kKeys; ++i) {
+        s[i] = (live && key0 + i <= pos) ? s[i] * p.q_scale : -INFINITY;
+        mt = fmaxf(mt, s[i]);
       }
-      // probabilities, and the P fragments of the two 16-key k-steps
-      uint32_t ph[2][4], pl[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const float p0 = s[nt][0] == -INFINITY ? 0.f : ex2(s[nt][0] - mA);
-        const float p1 = s[nt][1] == -INFINITY ? 0.f : ex2(s[nt][1] - mA);
-        const float p2 = s[nt][2] == -INFINITY ? 0.f : ex2(s[nt][2] - mB);
-        const float p3 = s[nt][3] == -INFINITY ? 0.f : ex2(s[nt][3] - mB);
-        lA += p0 + p1;
-        lB += p2 + p3;
-        const int ks = nt >> 1, hi = (nt & 1) * 2;   // A regs: [row g | row g+8] x [k lo | k hi]
-        const uint32_t hA = T::pack(p0, p1), hB = T::pack(p2, p3);
-        ph[ks][hi] = hA;
-        ph[ks][hi + 1] = hB;
-        if constexpr (std::is_same<T, BF16>::value) {
-          const float2 fa = T::to_float2(hA), fb = T::to_float2(hB);
-          pl[ks][hi] = T::pack(p0 - fa.x, p1 - fa.y);
-          pl[ks][hi + 1] = T::pack(p2 - fb.x, p3 - fb.y);
-        }
-      }
-      // keys past the context: their V rows may hold anything
-      const int kmax = kv_end - t0;                     // keys of this tile that exist
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-        for (int jq = 0; jq < NT / 2; ++jq) {          // two output tiles per ldmatrix
-          // matrices: (keys 0-7, d-tile 2jq), (keys 8-15, 2jq), (keys 0-7, 2jq+1), (keys 8-15, 2jq+1)
-          const int krow = 16 * ks + 8 * (mat & 1) + r;
-          uint32_t b[4];
-          ldsm_x4_t(swizzled_chunk<D / 64>(vt, krow, 2 * jq + (mat >> 1), rows_shift), b[0], b[1],
-                    b[2], b[3]);
-          if (kmax < kTile) {
-            const int k0 = 16 * ks + 2 * t;
-            const uint32_t keep0 = (k0 < kmax ? 0x0000ffffu : 0u) | (k0 + 1 < kmax ? 0xffff0000u : 0u);
-            const uint32_t keep1 = (k0 + 8 < kmax ? 0x0000ffffu : 0u) | (k0 + 9 < kmax ? 0xffff0000u : 0u);
-            b[0] &= keep0; b[2] &= keep0;
-            b[1] &= keep1; b[3] &= keep1;
+      if (mt > m + kRescaleThreshold) {
+        if (m != -INFINITY) {
+          // the output row holds earlier tiles: rescale it once their P V is done
+          if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+            ok = false;
+            break;
           }
-          T::mma16816(o[2 * jq], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], b[0], b[1]);
-          T::mma16816(o[2 * jq + 1], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], b[2], b[3]);
-          if constexpr (std::is_same<T, BF16>::value) {
-            T::mma16816(o[2 * jq], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b[0], b[1]);
-            T::mma16816(o[2 * jq + 1], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b[2], b[3]);
+          tc_fence_after();
+          const float c = ex2(m - mt);
+#pragma unroll
+          for (int h = 0; h < D / 32; ++h) {
+            uint32_t raw[32];
+            tmem_ld32(tl + 128 + h * 32, raw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * c);
+            tmem_st32(tl + 128 + h * 32, raw);
+          }
+          l *= c;
+        }
+        m = mt;
+      }
+      // this P buffer was read by the P V product two tiles back
+      if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = pbuf + b * Lay::kPBytes + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < kKeys / 8; ++cc) {
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float x = s[cc * 8 + i];
+          e[i] = x == -INFINITY ? 0.f : ex2(x - m);
+          l += e[i];
+        }
+        uint4 w;
+        w.x = T::pack(e[0], e[1]);
+        w.y = T::pack(e[2], e[3]);
+        w.z = T::pack(e[4], e[5]);
+        w.w = T::pack(e[6], e[7]);
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w;
+      }
+      if (j == n_tiles - 1 && kv_end - key0 < kKeys) {
+        // V rows past the last key may hold anything (0 x NaN is NaN): zero them
+        uint8_t* vt = stages + (j % kStages) * Lay::kStageBytes + Lay::kTileBytes;
+        const int valid = kv_end - key0;
+        for (int idx = r; idx < NH * kKeys; idx += kRows) {
+          const int kr = idx % kKeys, h = idx / kKeys;
+          if (kr >= valid) {
+            uint4* d = reinterpret_cast<uint4*>(vt + h * Lay::kLineBytes + kr * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[b]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[st]);
-  }
-  if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
-
-  lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-  lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-  lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-  lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-  if (liveA) {
-    const int64_t base = (static_cast<int64_t>(qs + tokA) * p.num_heads + headA) * D;
+    if (ok && mbar_wait(&pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1)) {
+      tc_fence_after();
+      float o[D];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      store_elem(p.out, base + 8 * j + 2 * t, o[j][0] / lA, p.out_dtype);
-      store_elem(p.out, base + 8 * j + 2 * t + 1, o[j][1] / lA, p.out_dtype);
+      for (int h = 0; h < D / 32; ++h) {
+        uint32_t raw[32];
+        tmem_ld32(tl + 128 + h * 32, raw);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[h * 32 + i] = __uint_as_float(raw[i]);
+      }
+      if (live) {
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int i = 0; i < D; ++i) o[i] *= inv;
+        store_row<T>(p.out, p.out_dtype,
+                     (static_cast<int64_t>(qs + tok) * p.num_heads + head) * D, o, D);
+      }
+    } else {
+      flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
   }
-  if (liveB) {
-    const int64_t base = (static_cast<int64_t>(qs + tokB) * p.num_heads + headB) * D;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      store_elem(p.out, base + 8 * j + 2 * t, o[j][2] / lB, p.out_dtype);
-      store_elem(p.out, base + 8 * j + 2 * t + 1, o[j][3] / lB, p.out_dtype);
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
   }
 }
 
@@ -377,11 +474,11 @@ extern "C" pkv_status pkv_paged_attention_prefill(
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_EINVAL;
 
-  const int box_rows = std::min(block_size, prefill::kTile);
+  const int box_rows = std::min(block_size, prefill::kKeys);
   CUtensorMap tk, tv;
   const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
-  if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, true) ||
-      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, true))
+  if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, kLineSwizzled) ||
+      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, kLineSwizzled))
     return PKV_ECUDA;
   prefill::Params p{};
   p.out = out;

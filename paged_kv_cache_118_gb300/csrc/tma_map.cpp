@@ -26,11 +26,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads,
-                             int64_t slots, int box_rows, bool swizzled) {
+                             int64_t slots, int box_rows, CacheView view) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   CUresult r;
-  if (!swizzled) {
+  if (view == kRowsPlain) {
     // 3-D view: x = element within the head (D), y = KV head, z = slot; box D x 1 x rows.
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_kv_heads),
                           static_cast<cuuint64_t>(slots)};
@@ -52,7 +52,7 @@ bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2 * num_kv_heads,
                              static_cast<cuuint64_t>(D) * 2, 128};
     cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1,
-                         static_cast<cuuint32_t>(D / 64)};
+                         static_cast<cuuint32_t>(view == kLineSwizzled ? 1 : D / 64)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
