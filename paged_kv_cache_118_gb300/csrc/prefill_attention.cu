@@ -44,12 +44,14 @@
 namespace pkv {
 namespace prefill {
 
-constexpr int kRows = 128;             // query rows per CTA: the TMEM lanes
+constexpr int kRows = 128;             // query rows of one query tile: the TMEM lanes
+constexpr int kQTiles = 2;             // query tiles per CTA, sharing every K/V tile
 constexpr int kKeys = 64;              // keys per tile
 constexpr int kStages = 3;
-constexpr int kThreads = 256;          // warp 0: copies; warp 1: MMA; warps 4-7: softmax
+constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: copies; warp 1: MMA; 4 warps per query tile
 constexpr int kSoftmaxWarp0 = 4;
-constexpr uint32_t kTmemCols = 256;    // S0 [0, 64), S1 [64, 128), O [128, 128 + D)
+// per query tile t, from column 256 t: S0 [0, 64), S1 [64, 128), O [128, 128 + D)
+constexpr uint32_t kTmemCols = 256 * kQTiles;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -74,10 +76,10 @@ struct Params {
 // Shared memory, from a 1024-byte aligned base. Every operand is stored as
 // 128-byte rows with the 128-byte swizzle (16-byte chunk c of the row at
 // position n sits at c ^ (n % 8)), 8-row groups 1024 bytes apart:
-//  Q: D/64 column blocks of 128 rows (A of S, K-major);
+//  Q, per query tile: D/64 column blocks of 128 rows (A of S, K-major);
 //  each stage: K then V, each D/64 line blocks of 64 key rows (B of S,
 //  K-major; B of P V, MN-major with the next 64 columns one line block on);
-//  P: two buffers of 128 rows x 64 keys (A of P V, K-major).
+//  P, per query tile: two buffers of 128 rows x 64 keys (A of P V, K-major).
 template <int D>
 struct Layout {
   static constexpr int NH = D / 64;
@@ -86,11 +88,12 @@ struct Layout {
   static constexpr int kTileBytes = NH * kLineBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kPBytes = kRows * kKeys * 2;
-  static constexpr int kOffStages = kQBytes;
+  static constexpr int kOffStages = kQTiles * kQBytes;
   static constexpr int kOffP = kOffStages + kStages * kStageBytes;
-  static constexpr int kOffBars = kOffP + 2 * kPBytes;
-  // stage_full[S], stage_empty[S], q_full, s_full[2], s_free[2], p_full[2], pv_done[2], drain
-  static constexpr int kNumBars = 2 * kStages + 1 + 8 + 1;
+  static constexpr int kOffBars = kOffP + kQTiles * 2 * kPBytes;
+  // stage_full[S], stage_empty[S], q_full, per query tile s_full[2], s_free[2],
+  // p_full[2], pv_done[2]; drain, tail (V rows past the last key zeroed)
+  static constexpr int kNumBars = 2 * kStages + 1 + 8 * kQTiles + 2;
   static constexpr int kOffTmem = kOffBars + kNumBars * 8;
   static constexpr int kSmem = 1024 + kOffTmem + 16;
 };
@@ -132,17 +135,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* qtile = smem;
+  uint8_t* qtiles = smem;
   uint8_t* stages = smem + Lay::kOffStages;
-  uint8_t* pbuf = smem + Lay::kOffP;
+  uint8_t* pbufs = smem + Lay::kOffP;
   uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* stage_empty = stage_full + kStages;
   uint64_t* q_full = stage_empty + kStages;
-  uint64_t* s_full = q_full + 1;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* drain = pv_done + 2;
+  uint64_t* tbars = q_full + 1;                 // per query tile: s_full[2], s_free[2], p_full[2], pv_done[2]
+  uint64_t* drain = tbars + 8 * kQTiles;
+  uint64_t* tail = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
 
   const int warp = threadIdx.x >> 5;
@@ -150,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int seq = blockIdx.z;
   const int kvh = blockIdx.y;
   const int G = p.group;
-  const int tokens_per_tile = kRows / G;
-  const int tok0 = blockIdx.x * tokens_per_tile;          // first chunk token of the tile
+  const int tok_per_qt = kRows / G;                        // chunk tokens per query tile
+  const int tok0 = blockIdx.x * kQTiles * tok_per_qt;      // first chunk token of the CTA
   const int B = p.block_size;
 
   const int qs = __ldg(p.query_start + seq);
@@ -163,23 +164,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   if (tok0 >= C) return;
-  const int tok_end = min(C, tok0 + tokens_per_tile);
-  const int kv_end = L - C + tok_end;                      // keys this tile can see
+  // key tiles each query tile reads (0 for a tile wholly past the chunk)
+  int nt[kQTiles];
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    const int first = tok0 + t * tok_per_qt;
+    const int kv_end_t = L - C + min(C, first + tok_per_qt);
+    nt[t] = first < C ? (kv_end_t + kKeys - 1) / kKeys : 0;
+  }
+  const int kv_end = L - C + min(C, tok0 + kQTiles * tok_per_qt);   // keys the CTA reads
   const int n_tiles = (kv_end + kKeys - 1) / kKeys;
+  // the lowest query tile that reads the last key tile zeroes its V rows past kv_end
+  int zt = 0;
+  while (nt[zt] != n_tiles) ++zt;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&stage_full[i], 1);
       mbar_init(&stage_empty[i], 1);
     }
-    mbar_init(q_full, kRows);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kRows);
-      mbar_init(&p_full[i], kRows);
-      mbar_init(&pv_done[i], 1);
-    }
+    mbar_init(q_full, kQTiles * kRows);
+    for (int t = 0; t < kQTiles; ++t)
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&tbars[8 * t + i], 1);              // s_full
+        mbar_init(&tbars[8 * t + 2 + i], kRows);      // s_free
+        mbar_init(&tbars[8 * t + 4 + i], kRows);      // p_full
+        mbar_init(&tbars[8 * t + 6 + i], 1);          // pv_done
+      }
     mbar_init(drain, 1);
+    mbar_init(tail, kRows);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -244,44 +257,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
       bool ok = mbar_wait(q_full, 0);
       tc_fence_after();
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages, b = j & 1;
-        if (!mbar_wait(&stage_full[st], (j / kStages) & 1)) return false;
+      // S of query tile t for key tile j, into its score buffer j % 2
+      auto issue_s = [&](int t, int j) -> bool {
+        const int b = j & 1;
+        uint64_t* s_free = &tbars[8 * t + 2];
         if (j >= 2 && !mbar_wait(&s_free[b], ((j - 2) >> 1) & 1)) return false;
         tc_fence_after();
-        const uint8_t* kt = stages + st * Lay::kStageBytes;
+        const uint8_t* kt = stages + (j % kStages) * Lay::kStageBytes;
+        const uint8_t* qt = qtiles + t * Lay::kQBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int h = ks >> 2, off = (ks & 3) * 32;      // 64-element column block, 16 of them
-          const uint64_t ad = smem_desc_sw128(qtile + h * kRows * 128 + off, 16, 1024);
+          const uint64_t ad = smem_desc_sw128(qt + h * kRows * 128 + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(kt + h * Lay::kLineBytes + off, 16, 1024);
-          tc_mma_f16(tbase + b * kKeys, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
+          tc_mma_f16(tbase + 256 * t + b * kKeys, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[b]);
+        tc_commit(&tbars[8 * t + b]);                       // s_full
         return true;
       };
-      auto issue_pv = [&](int j) -> bool {
-        const int st = j % kStages, b = j & 1;
-        if (!mbar_wait(&p_full[b], (j >> 1) & 1)) return false;
+      // O of query tile t += P V for key tile j
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int b = j & 1;
+        if (!mbar_wait(&tbars[8 * t + 4 + b], (j >> 1) & 1)) return false;   // p_full
         tc_fence_after();
-        const uint8_t* vt = stages + st * Lay::kStageBytes + Lay::kTileBytes;
-        const uint8_t* pt = pbuf + b * Lay::kPBytes;
+        const uint8_t* vt = stages + (j % kStages) * Lay::kStageBytes + Lay::kTileBytes;
+        const uint8_t* pt = pbufs + (2 * t + b) * Lay::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128(pt + kk * 32, 16, 1024);
           // V as B, MN-major: 16 keys are two 8-row groups; the next 64 columns
           // of D are one line block (kLineBytes) on
           const uint64_t bd = smem_desc_sw128(vt + kk * 16 * 128, Lay::kLineBytes, 1024);
-          tc_mma_f16(tbase + 128, ad, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tbase + 256 * t + 128, ad, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&pv_done[b]);
-        tc_commit(&stage_empty[st]);
+        tc_commit(&tbars[8 * t + 6 + b]);                   // pv_done
         return true;
       };
-      if (ok) ok = issue_s(0);
+      auto issue_s_all = [&](int j) -> bool {
+        if (!mbar_wait(&stage_full[j % kStages], (j / kStages) & 1)) return false;
+        for (int t = 0; t < kQTiles; ++t)
+          if (j < nt[t] && !issue_s(t, j)) return false;
+        return true;
+      };
+      if (ok) ok = issue_s_all(0);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) ok = issue_s(j + 1);
-        if (ok) ok = issue_pv(j);
+        if (j + 1 < n_tiles) ok = issue_s_all(j + 1);
+        for (int t = 0; ok && t < kQTiles; ++t)
+          if (j < nt[t]) ok = issue_pv(t, j);
+        if (ok) tc_commit(&stage_empty[j % kStages]);       // K and V of tile j are read
       }
       if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
       // everything issued has completed before the columns are freed
@@ -290,9 +313,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- softmax
-    const int r = (warp - kSoftmaxWarp0) * 32 + lane;      // query row = TMEM lane
-    const uint32_t tl = tbase + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
-    const int tok = tok0 + r / G;
+    const int t = (warp - kSoftmaxWarp0) >> 2;             // query tile
+    const int r = ((warp - kSoftmaxWarp0) & 3) * 32 + lane;   // row of the tile = TMEM lane
+    const uint32_t tl = tbase + 256 * t + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    uint64_t* s_full = &tbars[8 * t];
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_full + 4;
+    uint64_t* pv_done = s_full + 6;
+    uint8_t* qtile = qtiles + t * Lay::kQBytes;
+    uint8_t* pbuf = pbufs + 2 * t * Lay::kPBytes;
+    const int n_my = nt[t];
+    const int tok = tok0 + t * tok_per_qt + r / G;
     const int head = kvh * G + r % G;
     const bool live = tok < C;
     const int pos = L - C + tok;
@@ -311,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; j < n_my; ++j) {
       const int b = j & 1;
       if (!mbar_wait(&s_full[b], (j >> 1) & 1)) {
         ok = false;
@@ -380,41 +411,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w;
       }
       if (j == n_tiles - 1 && kv_end - key0 < kKeys) {
-        // V rows past the last key may hold anything (0 x NaN is NaN): zero them
-        uint8_t* vt = stages + (j % kStages) * Lay::kStageBytes + Lay::kTileBytes;
-        const int valid = kv_end - key0;
-        for (int idx = r; idx < NH * kKeys; idx += kRows) {
-          const int kr = idx % kKeys, h = idx / kKeys;
-          if (kr >= valid) {
-            uint4* d = reinterpret_cast<uint4*>(vt + h * Lay::kLineBytes + kr * 128);
+        if (t == zt) {
+          // V rows past the last key may hold anything (0 x NaN is NaN): zero them
+          uint8_t* vt = stages + (j % kStages) * Lay::kStageBytes + Lay::kTileBytes;
+          const int valid = kv_end - key0;
+          for (int idx = r; idx < NH * kKeys; idx += kRows) {
+            const int kr = idx % kKeys, h = idx / kKeys;
+            if (kr >= valid) {
+              uint4* d = reinterpret_cast<uint4*>(vt + h * Lay::kLineBytes + kr * 128);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+              for (int i = 0; i < 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
           }
+          fence_proxy_async_smem();
+          mbar_arrive(tail);
+        } else if (!mbar_wait(tail, 0)) {                   // a lower query tile zeroes them
+          ok = false;
+          break;
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
-    if (ok && mbar_wait(&pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1)) {
-      tc_fence_after();
-      float o[D];
+    if (n_my > 0) {
+      if (ok && mbar_wait(&pv_done[(n_my - 1) & 1], ((n_my - 1) >> 1) & 1)) {
+        tc_fence_after();
+        float o[D];
 #pragma unroll
-      for (int h = 0; h < D / 32; ++h) {
-        uint32_t raw[32];
-        tmem_ld32(tl + 128 + h * 32, raw);
+        for (int h = 0; h < D / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(tl + 128 + h * 32, raw);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[h * 32 + i] = __uint_as_float(raw[i]);
+          for (int i = 0; i < 32; ++i) o[h * 32 + i] = __uint_as_float(raw[i]);
+        }
+        if (live) {
+          const float inv = 1.f / l;
+#pragma unroll
+          for (int i = 0; i < D; ++i) o[i] *= inv;
+          store_row<T>(p.out, p.out_dtype,
+                       (static_cast<int64_t>(qs + tok) * p.num_heads + head) * D, o, D);
+        }
+      } else {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
       }
-      if (live) {
-        const float inv = 1.f / l;
-#pragma unroll
-        for (int i = 0; i < D; ++i) o[i] *= inv;
-        store_row<T>(p.out, p.out_dtype,
-                     (static_cast<int64_t>(qs + tok) * p.num_heads + head) * D, o, D);
-      }
-    } else {
-      flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
   }
   tc_fence_before();
@@ -436,7 +476,7 @@ static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Pa
                                 Layout<D>::kSmem);
   });
   if (attr != cudaSuccess) return attr;
-  const int tiles = (p.max_query_len * p.group + kRows - 1) / kRows;
+  const int tiles = (p.max_query_len * p.group + kQTiles * kRows - 1) / (kQTiles * kRows);
   dim3 grid(tiles, num_kv_heads, num_seqs);
   kern<<<grid, kThreads, Layout<D>::kSmem, s>>>(tk, tv, p);
   return cudaGetLastError();
