@@ -167,7 +167,7 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, int out_dtype, const vo
  *   query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
  *   max_query_len host int >= every C (sizes the grid)
  *   head_size 64 or 128; block_size a power of two from 8 to 256;
- *   64 % (num_heads / num_kv_heads) == 0
+ *   128 % (num_heads / num_kv_heads) == 0; scale > 0
  * Device checks: 0 <= C <= min(L, max_query_len) and L <= max_blocks_per_seq *
  * block_size, else the sequence is skipped (its rows untouched) and
  * PKV_DEVERR_CONTEXT set; bad block ids as for decode. Needs no workspace.

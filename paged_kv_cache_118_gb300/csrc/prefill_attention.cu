@@ -359,14 +359,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&s_free[b]);
-      // causal mask (also hides keys past the context and rows past the chunk)
+      // causal mask (also hides keys past the context and rows past the chunk);
+      // the row maximum is taken on unscaled scores (the scale is positive)
       const int key0 = j * kKeys;
-      float mt = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (live && key0 + kKeys - 1 <= pos) {              // every key of the tile is visible
 #pragma unroll
-      for (int i = 0; i < kKeys; ++i) {
-        s[i] = (live && key0 + i <= pos) ? s[i] * p.q_scale : -INFINITY;
-        mt = fmaxf(mt, s[i]);
+        for (int i = 0; i < kKeys; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+          s[i] = (live && key0 + i <= pos) ? s[i] : -INFINITY;
+          mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+        }
       }
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.q_scale;
       if (mt > m + kRescaleThreshold) {
         if (m != -INFINITY) {
           // the output row holds earlier tiles: rescale it once their P V is done
@@ -394,14 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       uint8_t* prow = pbuf + b * Lay::kPBytes + r * 128;
+      // p = 2^(scale s - m): a masked score is -inf and gives 0 (m is finite
+      // on a live row from its first tile on; a row past the chunk writes 0)
+      const float nm = live ? -m : 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < kKeys / 8; ++cc) {
         float e[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float x = s[cc * 8 + i];
-          e[i] = x == -INFINITY ? 0.f : ex2(x - m);
-          l += e[i];
+          e[i] = live ? ex2(fmaf(s[cc * 8 + i], p.q_scale, nm)) : 0.f;
+          ls[i & 3] += e[i];
         }
         uint4 w;
         w.x = T::pack(e[0], e[1]);
@@ -410,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         w.w = T::pack(e[6], e[7]);
         *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w;
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (j == n_tiles - 1 && kv_end - key0 < kKeys) {
         if (t == zt) {
           // V rows past the last key may hold anything (0 x NaN is NaN): zero them
@@ -510,7 +521,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(
   if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EINVAL;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT32_MAX / 2) return PKV_EINVAL;
   if (static_cast<int64_t>(max_query_len) * group / prefill::kRows > 65535) return PKV_EINVAL;
-  if (!std::isfinite(scale)) return PKV_EINVAL;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PKV_EINVAL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_EINVAL;
 
