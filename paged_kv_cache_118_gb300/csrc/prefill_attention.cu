@@ -257,20 +257,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
       bool ok = mbar_wait(q_full, 0);
       tc_fence_after();
+      // Descriptors are built once; a k-step or another buffer only moves the
+      // start address (bits 0-13, in 16-byte units), so it is an addition.
+      const uint64_t dq0 = smem_desc_sw128(qtiles, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(stages, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(stages + Lay::kTileBytes, Lay::kLineBytes, 1024);
+      const uint64_t dp0 = smem_desc_sw128(pbufs, 16, 1024);
       // S of query tile t for key tile j, into its score buffer j % 2
       auto issue_s = [&](int t, int j) -> bool {
         const int b = j & 1;
         uint64_t* s_free = &tbars[8 * t + 2];
         if (j >= 2 && !mbar_wait(&s_free[b], ((j - 2) >> 1) & 1)) return false;
         tc_fence_after();
-        const uint8_t* kt = stages + (j % kStages) * Lay::kStageBytes;
-        const uint8_t* qt = qtiles + t * Lay::kQBytes;
+        const uint64_t dq = dq0 + (t * Lay::kQBytes >> 4);
+        const uint64_t dk = dk0 + ((j % kStages) * Lay::kStageBytes >> 4);
+        const uint32_t d = tbase + 256 * t + b * kKeys;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int h = ks >> 2, off = (ks & 3) * 32;      // 64-element column block, 16 of them
-          const uint64_t ad = smem_desc_sw128(qt + h * kRows * 128 + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kt + h * Lay::kLineBytes + off, 16, 1024);
-          tc_mma_f16(tbase + 256 * t + b * kKeys, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
+          // 64-element column block ks / 4, 32 bytes per k-step inside it
+          const uint32_t qo = ((ks >> 2) * kRows * 128 + (ks & 3) * 32) >> 4;
+          const uint32_t ko = ((ks >> 2) * Lay::kLineBytes + (ks & 3) * 32) >> 4;
+          tc_mma_f16(d, dq + qo, dk + ko, kIdescS, ks > 0 ? 1u : 0u);
         }
         tc_commit(&tbars[8 * t + b]);                       // s_full
         return true;
@@ -280,16 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1;
         if (!mbar_wait(&tbars[8 * t + 4 + b], (j >> 1) & 1)) return false;   // p_full
         tc_fence_after();
-        const uint8_t* vt = stages + (j % kStages) * Lay::kStageBytes + Lay::kTileBytes;
-        const uint8_t* pt = pbufs + (2 * t + b) * Lay::kPBytes;
+        // V as B, MN-major: 16 keys are two 8-row groups; the next 64 columns
+        // of D are one line block (kLineBytes) on
+        const uint64_t dv = dv0 + ((j % kStages) * Lay::kStageBytes >> 4);
+        const uint64_t dp = dp0 + ((2 * t + b) * Lay::kPBytes >> 4);
+        const uint32_t d = tbase + 256 * t + 128;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(pt + kk * 32, 16, 1024);
-          // V as B, MN-major: 16 keys are two 8-row groups; the next 64 columns
-          // of D are one line block (kLineBytes) on
-          const uint64_t bd = smem_desc_sw128(vt + kk * 16 * 128, Lay::kLineBytes, 1024);
-          tc_mma_f16(tbase + 256 * t + 128, ad, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc_mma_f16(d, dp + ((kk * 32) >> 4), dv + ((kk * 16 * 128) >> 4), kIdescO,
+                     (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&tbars[8 * t + 6 + b]);                   // pv_done
         return true;
       };
