@@ -9,22 +9,24 @@
 // follow their position; "079｜vLLM 与 PagedAttention" §2 for the single global
 // denominator). Decode is the case C = 1.
 //
-// How (one CTA per tile of 128 query rows, KV head and sequence; a row is one
-// (query token, query head of the KV head's group), so 128/G tokens per tile):
+// How (one CTA per 256 query rows, KV head and sequence: two query tiles of
+// 128 rows; a row is one (query token, query head of the KV head's group), so
+// 128/G tokens per query tile):
 //  * warp 0 streams 64-key tiles of K and V over the causal range only, one
 //    TMA copy per physical block and 128-byte line (128-byte swizzle), into a
-//    3-stage ring completing on mbarriers;
-//  * warp 1 owns the tensor memory (256 columns: two 64-column score buffers
-//    and the D-column output) and issues, from one thread, S = Q K^T
+//    3-stage ring completing on mbarriers; both query tiles use each K/V tile;
+//  * warp 1 owns the tensor memory (per query tile: two 64-column score
+//    buffers and the D-column output) and issues, from one thread, S = Q K^T
 //    (M = 128, N = 64, K = D) into a score buffer and O += P V (M = 128,
-//    N = D, K = 64) into the output, each followed by a commit to an mbarrier;
-//    the next tile's S is issued before this tile's P V;
-//  * warps 4-7 run the softmax, one thread per query row (its TMEM lane): the
-//    row's 64 scores come out of TMEM, the causal mask and a base-2 online
-//    softmax with lazy rescale (the output row in TMEM is rescaled only when
-//    the running maximum grows by more than 2^8) give P, which is written to
-//    shared memory in the layout the P V product reads; the output row is
-//    divided by the row sum at the end.
+//    N = D, K = 64, P read from tensor memory) into the output, each
+//    followed by a commit to an mbarrier; the next tile's S is issued before
+//    this tile's P V;
+//  * a softmax warpgroup per query tile, one thread per query row (its TMEM
+//    lane): the row's 64 scores come out of tensor memory, the causal mask
+//    and a base-2 online softmax with lazy rescale (the output row is
+//    rescaled in place only when the running maximum grows by more than 2^8)
+//    give P, written back over the scores as 16-bit pairs, where the P V
+//    product reads it; the output row is divided by the row sum at the end.
 // Every wait is bounded; a chunk or context length out of range is skipped
 // and reported.
 
@@ -79,7 +81,7 @@ struct Params {
 //  Q, per query tile: D/64 column blocks of 128 rows (A of S, K-major);
 //  each stage: K then V, each D/64 line blocks of 64 key rows (B of S,
 //  K-major; B of P V, MN-major with the next 64 columns one line block on);
-//  P, per query tile: two buffers of 128 rows x 64 keys (A of P V, K-major).
+//  (P stays in tensor memory.)
 template <int D>
 struct Layout {
   static constexpr int NH = D / 64;
@@ -87,13 +89,11 @@ struct Layout {
   static constexpr int kLineBytes = kKeys * 128;          // one line block of a K or V tile
   static constexpr int kTileBytes = NH * kLineBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kPBytes = kRows * kKeys * 2;
   static constexpr int kOffStages = kQTiles * kQBytes;
-  static constexpr int kOffP = kOffStages + kStages * kStageBytes;
-  static constexpr int kOffBars = kOffP + kQTiles * 2 * kPBytes;
-  // stage_full[S], stage_empty[S], q_full, per query tile s_full[2], s_free[2],
-  // p_full[2], pv_done[2]; drain, tail (V rows past the last key zeroed)
-  static constexpr int kNumBars = 2 * kStages + 1 + 8 * kQTiles + 2;
+  static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
+  // stage_full[S], stage_empty[S], q_full, per query tile s_full[2], p_full[2],
+  // pv_done[2]; drain, tail (V rows past the last key zeroed)
+  static constexpr int kNumBars = 2 * kStages + 1 + 6 * kQTiles + 2;
   static constexpr int kOffTmem = kOffBars + kNumBars * 8;
   static constexpr int kSmem = 1024 + kOffTmem + 16;
 };
@@ -137,12 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* qtiles = smem;
   uint8_t* stages = smem + Lay::kOffStages;
-  uint8_t* pbufs = smem + Lay::kOffP;
   uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* stage_empty = stage_full + kStages;
   uint64_t* q_full = stage_empty + kStages;
-  uint64_t* tbars = q_full + 1;                 // per query tile: s_full[2], s_free[2], p_full[2], pv_done[2]
-  uint64_t* drain = tbars + 8 * kQTiles;
+  uint64_t* tbars = q_full + 1;                 // per query tile: s_full[2], p_full[2], pv_done[2]
+  uint64_t* drain = tbars + 6 * kQTiles;
   uint64_t* tail = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
 
@@ -186,10 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, kQTiles * kRows);
     for (int t = 0; t < kQTiles; ++t)
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&tbars[8 * t + i], 1);              // s_full
-        mbar_init(&tbars[8 * t + 2 + i], kRows);      // s_free
-        mbar_init(&tbars[8 * t + 4 + i], kRows);      // p_full
-        mbar_init(&tbars[8 * t + 6 + i], 1);          // pv_done
+        mbar_init(&tbars[6 * t + i], 1);              // s_full
+        mbar_init(&tbars[6 * t + 2 + i], kRows);      // p_full
+        mbar_init(&tbars[6 * t + 4 + i], 1);          // pv_done
       }
     mbar_init(drain, 1);
     mbar_init(tail, kRows);
@@ -262,12 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq0 = smem_desc_sw128(qtiles, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(stages, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(stages + Lay::kTileBytes, Lay::kLineBytes, 1024);
-      const uint64_t dp0 = smem_desc_sw128(pbufs, 16, 1024);
-      // S of query tile t for key tile j, into its score buffer j % 2
+      // S of query tile t for key tile j, into its score buffer j % 2, once
+      // the P V product two tiles back has read the P held there
       auto issue_s = [&](int t, int j) -> bool {
         const int b = j & 1;
-        uint64_t* s_free = &tbars[8 * t + 2];
-        if (j >= 2 && !mbar_wait(&s_free[b], ((j - 2) >> 1) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&tbars[6 * t + 4 + b], ((j - 2) >> 1) & 1)) return false;
         tc_fence_after();
         const uint64_t dq = dq0 + (t * Lay::kQBytes >> 4);
         const uint64_t dk = dk0 + ((j % kStages) * Lay::kStageBytes >> 4);
@@ -279,24 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ko = ((ks >> 2) * Lay::kLineBytes + (ks & 3) * 32) >> 4;
           tc_mma_f16(d, dq + qo, dk + ko, kIdescS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&tbars[8 * t + b]);                       // s_full
+        tc_commit(&tbars[6 * t + b]);                       // s_full
         return true;
       };
-      // O of query tile t += P V for key tile j
+      // O of query tile t += P V for key tile j; P (16-bit, two per column)
+      // is in the first 32 columns of score buffer j % 2, 8 columns per k-step
       auto issue_pv = [&](int t, int j) -> bool {
         const int b = j & 1;
-        if (!mbar_wait(&tbars[8 * t + 4 + b], (j >> 1) & 1)) return false;   // p_full
+        if (!mbar_wait(&tbars[6 * t + 2 + b], (j >> 1) & 1)) return false;   // p_full
         tc_fence_after();
         // V as B, MN-major: 16 keys are two 8-row groups; the next 64 columns
         // of D are one line block (kLineBytes) on
         const uint64_t dv = dv0 + ((j % kStages) * Lay::kStageBytes >> 4);
-        const uint64_t dp = dp0 + ((2 * t + b) * Lay::kPBytes >> 4);
+        const uint32_t a = tbase + 256 * t + b * kKeys;
         const uint32_t d = tbase + 256 * t + 128;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          tc_mma_f16(d, dp + ((kk * 32) >> 4), dv + ((kk * 16 * 128) >> 4), kIdescO,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&tbars[8 * t + 6 + b]);                   // pv_done
+          tc_mma_f16_ts(d, a + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&tbars[6 * t + 4 + b]);                   // pv_done
         return true;
       };
       auto issue_s_all = [&](int j) -> bool {
@@ -322,12 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - kSoftmaxWarp0) >> 2;             // query tile
     const int r = ((warp - kSoftmaxWarp0) & 3) * 32 + lane;   // row of the tile = TMEM lane
     const uint32_t tl = tbase + 256 * t + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
-    uint64_t* s_full = &tbars[8 * t];
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_full + 4;
-    uint64_t* pv_done = s_full + 6;
+    uint64_t* s_full = &tbars[6 * t];
+    uint64_t* p_full = s_full + 2;
+    uint64_t* pv_done = s_full + 4;
     uint8_t* qtile = qtiles + t * Lay::kQBytes;
-    uint8_t* pbuf = pbufs + 2 * t * Lay::kPBytes;
     const int n_my = nt[t];
     const int tok = tok0 + t * tok_per_qt + r / G;
     const int head = kvh * G + r % G;
@@ -363,8 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[h * 32 + i] = __uint_as_float(raw[i]);
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
       // causal mask (also hides keys past the context and rows past the chunk);
       // the row maximum is taken on unscaled scores (the scale is positive)
       const int key0 = j * kKeys;
@@ -401,32 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m = mt;
       }
-      // this P buffer was read by the P V product two tiles back
-      if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = pbuf + b * Lay::kPBytes + r * 128;
       // p = 2^(scale s - m): a masked score is -inf and gives 0 (m is finite
       // on a live row from its first tile on; a row past the chunk writes 0)
       const float nm = live ? -m : 0.f;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[kKeys / 2];                               // P as 16-bit pairs, key order
 #pragma unroll
-      for (int cc = 0; cc < kKeys / 8; ++cc) {
-        float e[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          e[i] = live ? ex2(fmaf(s[cc * 8 + i], p.q_scale, nm)) : 0.f;
-          ls[i & 3] += e[i];
-        }
-        uint4 w;
-        w.x = T::pack(e[0], e[1]);
-        w.y = T::pack(e[2], e[3]);
-        w.z = T::pack(e[4], e[5]);
-        w.w = T::pack(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w;
+      for (int i = 0; i < kKeys; i += 2) {
+        const float e0 = live ? ex2(fmaf(s[i], p.q_scale, nm)) : 0.f;
+        const float e1 = live ? ex2(fmaf(s[i + 1], p.q_scale, nm)) : 0.f;
+        ls[(i >> 1) & 3] += e0 + e1;
+        pk[i >> 1] = T::pack(e0, e1);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_st32(tl + b * kKeys, pk);                        // over the scores of this tile
       if (j == n_tiles - 1 && kv_end - key0 < kKeys) {
         if (t == zt) {
           // V rows past the last key may hold anything (0 x NaN is NaN): zero them
@@ -447,7 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
