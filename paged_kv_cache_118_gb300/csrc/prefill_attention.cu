@@ -49,7 +49,7 @@ namespace prefill {
 constexpr int kRows = 128;             // query rows of one query tile: the TMEM lanes
 constexpr int kQTiles = 2;             // query tiles per CTA, sharing every K/V tile
 constexpr int kKeys = 64;              // keys per tile
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: copies; warp 1: MMA; 4 warps per query tile
 constexpr int kSoftmaxWarp0 = 4;
 // per query tile t, from column 256 t: S0 [0, 64), S1 [64, 128), O [128, 128 + D)
