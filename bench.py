@@ -43,6 +43,7 @@ CONFIGS = {
     "llama13b": dict(layers=40),
     "gqa_prefix": dict(layers=16),
     "longctx": dict(layers=8),
+    "mqa": dict(layers=16),
 }
 
 
@@ -158,6 +159,8 @@ def workload_shape(name, seed):
         return wl.llama13b_lengths(128, seed), 40, 40, 128, 16, "f16"
     if name == "longctx":
         return np.array([n * 1024 for n in wl.LONGCTX_LENS_K], np.int32), 32, 8, 128, 16, "bf16"
+    if name == "mqa":
+        return wl.llama13b_lengths(128, seed), 64, 1, 128, 16, "bf16"
     if name == "gqa_prefix":
         pb = wl.gqa_prefix(seed)
         lens = np.array([int(pb.prefix_lens[s // 4]) + int(pb.tail_lens[s]) for s in range(256)],
@@ -174,6 +177,8 @@ def make_workload(name, seed):
         return wl.llama13b(seed)
     if name == "longctx":
         return wl.longctx(seed)
+    if name == "mqa":
+        return wl.mqa(seed)
     raise ValueError(name)
 
 

@@ -27,8 +27,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-SOURCES = ["decode_attention.cu", "prefill_attention.cu", "cache_ops.cu", "tma_map.cpp",
-           "block_manager.cpp", "api.cpp"]
+SOURCES = ["decode_attention.cu", "decode_tc.cu", "prefill_attention.cu", "cache_ops.cu",
+           "tma_map.cpp", "block_manager.cpp", "api.cpp"]
 
 
 def nvcc() -> str:

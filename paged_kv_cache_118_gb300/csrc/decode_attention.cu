@@ -1392,9 +1392,55 @@ extern "C" pkv_status pkv_paged_attention_decode(
                                                 max_blocks_per_seq, block_size, pt);
   if (workspace_bytes < need) return PKV_EWORKSPACE;
 
-  // Grouped query heads go to the tensor path when every TMA copy lands on a
-  // 1 KB boundary of a tile half (block_size >= 8), else to the packed-pair path.
   const int group = num_heads / num_kv_heads;
+  const int64_t rows_all = static_cast<int64_t>(num_seqs) * num_heads * parts;
+  float* part_acc = static_cast<float*>(workspace);
+  float2* part_ml = reinterpret_cast<float2*>(part_acc + rows_all * head_size);
+  int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + rows_all * head_size * 4 +
+                                        ((rows_all * 8 + 15) / 16) * 16);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ReduceParams rp{};
+  rp.part_acc = part_acc;
+  rp.part_ml = part_ml;
+  rp.context_lens = context_lens;
+  rp.num_seqs = num_seqs;
+  rp.num_heads = num_heads;
+  rp.max_parts = static_cast<int>(parts);
+  rp.partition_tokens = pt;
+  rp.max_context = static_cast<int>(max_ctx);
+  if (decode_tc_supported(group, head_size, block_size, pt)) {
+    // Large groups: all G heads of a KV head in one tensor-memory product.
+    if (parts * num_seqs * num_kv_heads > INT32_MAX / 2) return PKV_EINVAL;
+    DecodeTcArgs a{};
+    a.part_acc = part_acc;
+    a.part_ml = part_ml;
+    a.counter = counter;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.err = err_flag;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_size = head_size;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.partition_tokens = pt;
+    a.max_parts = static_cast<int>(parts);
+    a.bf16 = kv_dtype == PKV_BF16;
+    a.q_scale = scale * kLog2e;
+    if (launch_decode_tc(a, st) != cudaSuccess) return PKV_ECUDA;
+    const cudaError_t er = head_size == 128 ? launch_reduce<128>(out, out_dtype, rp, st)
+                                            : launch_reduce<64>(out, out_dtype, rp, st);
+    return er == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
+
+  // Grouped query heads go to the warp-level tensor path when every TMA copy
+  // lands on a 1 KB boundary of a tile half (block_size >= 8), else to the
+  // packed-pair path.
   const bool mma = group >= 2 && block_size >= 8;
   const int box_rows = std::min(block_size, kTile);
   CUtensorMap tk, tv;
@@ -1446,15 +1492,6 @@ extern "C" pkv_status pkv_paged_attention_decode(
   }
   if (e != cudaSuccess) return PKV_ECUDA;
 
-  ReduceParams rp{};
-  rp.part_acc = p.part_acc;
-  rp.part_ml = p.part_ml;
-  rp.context_lens = context_lens;
-  rp.num_seqs = num_seqs;
-  rp.num_heads = num_heads;
-  rp.max_parts = p.max_parts;
-  rp.partition_tokens = pt;
-  rp.max_context = static_cast<int>(max_ctx);
   e = head_size == 128 ? launch_reduce<128>(out, out_dtype, rp, s)
                        : launch_reduce<64>(out, out_dtype, rp, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;

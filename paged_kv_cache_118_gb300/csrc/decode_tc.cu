@@ -1,0 +1,552 @@
+// Paged decode attention for large query groups on the 5th-generation tensor
+// cores (tcgen05), accumulators in tensor memory.
+//
+// What is computed is the decode call's partition partial ("079｜vLLM 与
+// PagedAttention" §2 and the split-context form of [R] §3): for sequence s,
+// KV head h and a context partition [t0, t1) of its L tokens, every query head
+// g of h's group gets m = max_u scale q_g.k_u (base-2 units), l = sum_u
+// 2^(scale q_g.k_u - m) and acc = sum_u 2^(scale q_g.k_u - m) v_u, which the
+// decode reduce kernel merges with one global denominator.
+//
+// Why a second path: the warp-level tensor path serves at most 8 query heads
+// per KV head in a CTA, so a group of G > 8 heads reads each K/V byte G/8
+// times. Here the G heads (32, 64 or 128 of them) are the rows of one 128-row
+// product, and each K/V byte is read once.
+//
+// How (persistent CTAs, one per SM, 256 threads):
+//  * warp 0 claims units (partition, sequence, KV head) from a global counter,
+//    partition-major; per unit it loads the G query rows by TMA into one of two
+//    query buffers and streams the partition's 64-key K/V tiles (one TMA copy
+//    per physical block and 128-byte line) into a 4-stage ring;
+//  * one thread of warp 1 owns the 512 tensor-memory columns (two 64-column
+//    score buffers, two D-column output buffers, one per unit in flight) and
+//    issues S = Q K^T (M = 128, N = 64, K = D) and O += P V (P from tensor
+//    memory), committing each to an mbarrier; a tile's S is issued before the
+//    previous tile's P V, and the next unit's first S as soon as its queries
+//    are in;
+//  * warps 4-7 run the softmax, one thread per query row (its TMEM lane); rows
+//    past G are padding. At the end of a unit they write the partials from
+//    the unit's output buffer while the next unit runs in the other.
+// Every wait is bounded; bad block ids and lengths are reported and skipped.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+#include <type_traits>
+
+#include "pagedkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace tcdec {
+
+constexpr int kRows = 128;             // product rows: query heads of the KV head, padded
+constexpr int kKeys = 64;              // keys per tile
+constexpr int kStages = 4;
+constexpr int kThreads = 256;          // warp 0: claims and copies; warp 1: MMA; warps 4-7: softmax
+constexpr int kSoftmaxWarp0 = 4;
+// S0 [0, 64), S1 [64, 128), O0 [128, 128 + D), O1 [256, 256 + D)
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct Params {
+  float* part_acc;                     // [rows][D], rows = num_seqs * num_heads * max_parts
+  float2* part_ml;                     // [rows] = (m in base-2 units, l)
+  int* counter;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t* err;
+  int num_seqs, num_heads, num_kv_heads, group;
+  int num_blocks, block_size, max_blocks_per_seq;
+  int partition_tokens, max_parts, total_units, box_rows;
+  float q_scale;
+};
+
+struct UnitInfo {
+  int seq;                             // -1: no more units
+  int kvh;
+  int part;
+  int len;
+};
+
+// Shared memory from a 1024-byte aligned base; operands are 128-byte rows with
+// the 128-byte swizzle, 8-row groups 1024 bytes apart:
+//  Q, two buffers: D/64 column blocks of 128 rows (A of S, K-major; rows past
+//  G hold whatever an earlier unit left, and only their own rows of S, P and
+//  O see it);
+//  each stage: K then V, D/64 line blocks of 64 key rows (B of S, K-major; B
+//  of P V, MN-major with the next 64 columns one line block on).
+template <int D>
+struct Layout {
+  static constexpr int NH = D / 64;
+  static constexpr int kQBytes = kRows * D * 2;
+  static constexpr int kLineBytes = kKeys * 128;
+  static constexpr int kTileBytes = NH * kLineBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kOffStages = 2 * kQBytes;
+  static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
+  // stage_full[S], stage_empty[S], unit_full[2], unit_empty[2], q_full[2],
+  // q_free[2], s_full[2], p_full[2], pv_done[2], o_free[2], drain
+  static constexpr int kNumBars = 2 * kStages + 2 * 8 + 1;
+  static constexpr int kOffUnits = kOffBars + kNumBars * 8;
+  static constexpr int kOffTmem = kOffUnits + 2 * static_cast<int>(sizeof(UnitInfo));
+  static constexpr int kSmem = 1024 + kOffTmem + 16;
+};
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q, const Params p) {
+  using Lay = Layout<D>;
+  constexpr int NH = Lay::NH;
+  constexpr bool kBF16 = std::is_same<T, BF16>::value;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* qbufs = smem;
+  uint8_t* stages = smem + Lay::kOffStages;
+  uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
+  uint64_t* stage_empty = stage_full + kStages;
+  uint64_t* unit_full = stage_empty + kStages;
+  uint64_t* unit_empty = unit_full + 2;
+  uint64_t* q_full = unit_empty + 2;
+  uint64_t* q_free = q_full + 2;
+  uint64_t* s_full = q_free + 2;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* o_free = pv_done + 2;
+  uint64_t* drain = o_free + 2;
+  UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + Lay::kOffUnits);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int B = p.block_size;
+  const int PT = p.partition_tokens;
+  const int G = p.group;
+  const int max_ctx = p.max_blocks_per_seq * B;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&stage_full[i], 1);
+      mbar_init(&stage_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&unit_full[i], 1);
+      mbar_init(&unit_empty[i], kRows + 1);          // the softmax threads and the MMA thread
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_free[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kRows);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&o_free[i], kRows);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- claims, copies
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_q);
+      const uint64_t policy = l2_evict_first_policy();
+      const int R = p.box_rows;
+      const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
+      const int per_part = p.num_seqs * p.num_kv_heads;
+      int g = 0;                                           // tiles issued
+      int k = 0;                                           // units published
+      int last_issued[kStages];
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
+      bool ok = true;
+      while (ok) {
+        const int u = atomicAdd(p.counter, 1);
+        UnitInfo info{-1, 0, 0, 0};
+        int t_begin = 0, t_end = 0;
+        if (u < p.total_units) {
+          const int part = u / per_part;
+          const int rem = u - part * per_part;
+          const int seq = rem / p.num_kv_heads;
+          const int kvh = rem - seq * p.num_kv_heads;
+          const int L = __ldg(p.context_lens + seq);
+          if (L < 1 || L > max_ctx) {
+            if (part == 0 && kvh == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+            continue;
+          }
+          t_begin = part * PT;
+          if (t_begin >= L) continue;                      // this sequence has no such partition
+          t_end = min(L, t_begin + PT);
+          info = UnitInfo{seq, kvh, part, L};
+        }
+        const int slot = k & 1;
+        if (k >= 2 && (!mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1) ||
+                       !mbar_wait(&q_free[slot], ((k >> 1) & 1) ^ 1))) {
+          ok = false;
+          break;
+        }
+        units[slot] = info;
+        if (info.seq >= 0) {
+          // the group's query rows, one copy per 128-byte line
+          mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(NH) * G * 128);
+          const int row0 = info.seq * p.num_heads + info.kvh * G;
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            tma_load_3d(qbufs + slot * Lay::kQBytes + h * kRows * 128, &tm_q, &q_full[slot], 0, h,
+                        row0, policy);
+        }
+        mbar_arrive(&unit_full[slot]);
+        ++k;
+        if (info.seq < 0) break;
+        const int32_t* row = p.block_tables + static_cast<int64_t>(info.seq) * p.max_blocks_per_seq;
+        const int n_tiles = (t_end - t_begin + kKeys - 1) / kKeys;
+        for (int i = 0; i < n_tiles; ++i, ++g) {
+          const int st = g % kStages;
+          if (g >= kStages && !mbar_wait(&stage_empty[st], ((g / kStages) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          const int t0 = t_begin + i * kKeys;
+          const int valid = min(kKeys, t_end - t0);
+          const int copies = (valid + R - 1) / R;
+          uint8_t* kdst = stages + st * Lay::kStageBytes;
+          uint8_t* vdst = kdst + Lay::kTileBytes;
+          mbar_arrive_expect_tx(&stage_full[st], 2u * NH * copies * copy_bytes);
+          for (int c = 0; c < copies; ++c) {
+            const int tk = t0 + c * R;
+            int32_t id = __ldg(row + tk / B);
+            if (id < 0 || id >= p.num_blocks) {
+              flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+              id = 0;
+            }
+            const int z = id * B + tk % B;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              tma_load_4d(kdst + h * Lay::kLineBytes + c * copy_bytes, &tm_k, &stage_full[st], 0,
+                          z, info.kvh, h, policy);
+              tma_load_4d(vdst + h * Lay::kLineBytes + c * copy_bytes, &tm_v, &stage_full[st], 0,
+                          z, info.kvh, h, policy);
+            }
+          }
+          last_issued[st] = g;
+        }
+      }
+      if (!ok) {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        for (int st = 0; st < kStages; ++st)
+          if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = mma_idesc_f16(kBF16, kRows, kKeys, false);
+      constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
+      const uint64_t dq0 = smem_desc_sw128(qbufs, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(stages, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(stages + Lay::kTileBytes, Lay::kLineBytes, 1024);
+      int g = 0;                                           // tiles consumed
+      bool ok = true;
+      // S of global tile gi (its stage, score buffer gi % 2) from query buffer qb
+      auto issue_s = [&](int gi, int qb) -> bool {
+        const int st = gi % kStages, b = gi & 1;
+        if (!mbar_wait(&stage_full[st], (gi / kStages) & 1)) return false;
+        // the score buffer's P was read by the P V product two tiles back
+        if (gi >= 2 && !mbar_wait(&pv_done[b], ((gi - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t dq = dq0 + ((qb * Lay::kQBytes) >> 4);
+        const uint64_t dk = dk0 + ((st * Lay::kStageBytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t qo = ((ks >> 2) * kRows * 128 + (ks & 3) * 32) >> 4;
+          const uint32_t ko = ((ks >> 2) * Lay::kLineBytes + (ks & 3) * 32) >> 4;
+          tc_mma_f16(tbase + b * kKeys, dq + qo, dk + ko, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[b]);
+        return true;
+      };
+      // O of output buffer ob (+)= P V of global tile gi
+      auto issue_pv = [&](int gi, int ob, bool first) -> bool {
+        const int st = gi % kStages, b = gi & 1;
+        if (!mbar_wait(&p_full[b], (gi >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t dv = dv0 + ((st * Lay::kStageBytes) >> 4);
+        const uint32_t a = tbase + b * kKeys;
+        const uint32_t d = tbase + 128 + ob * 128;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc_mma_f16_ts(d, a + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO,
+                        (!first || kk > 0) ? 1u : 0u);
+        if constexpr (kBF16) {                              // + (p - hi) V
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            tc_mma_f16_ts(d, a + kKeys / 2 + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO, 1u);
+        }
+        tc_commit(&pv_done[b]);
+        tc_commit(&stage_empty[st]);
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait(&unit_full[slot], (k >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const UnitInfo info = units[slot];
+        mbar_arrive(&unit_empty[slot]);
+        if (info.seq < 0) break;
+        const int t_begin = info.part * PT;
+        const int n_tiles = (min(info.len, t_begin + PT) - t_begin + kKeys - 1) / kKeys;
+        if (!mbar_wait(&q_full[slot], (k >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        // the output buffer was read out at the end of the unit two back
+        if (k >= 2 && !mbar_wait(&o_free[slot], ((k >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        // the unit's last S is issued in iteration max(n_tiles - 2, 0); then
+        // the query buffer may be refilled once those products are done
+        const int last_s = n_tiles >= 2 ? n_tiles - 2 : 0;
+        ok = issue_s(g, slot);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          if (i + 1 < n_tiles) ok = issue_s(g + i + 1, slot);
+          if (ok && i == last_s) tc_commit(&q_free[slot]);
+          if (ok) ok = issue_pv(g + i, slot, i == 0);
+        }
+        g += n_tiles;
+      }
+      if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      tc_commit(drain);
+      mbar_wait(drain, 0);
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ---------------------------------------------------------- softmax
+    const int r = (warp - kSoftmaxWarp0) * 32 + lane;     // row = TMEM lane
+    const uint32_t tl = tbase + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    const bool live = r < G;
+    int g = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&unit_full[slot], (k >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const UnitInfo info = units[slot];
+      mbar_arrive(&unit_empty[slot]);
+      if (info.seq < 0) break;
+      const int t_begin = info.part * PT;
+      const int t_end = min(info.len, t_begin + PT);
+      const int n_tiles = (t_end - t_begin + kKeys - 1) / kKeys;
+      const uint32_t to = tl + 128 + slot * 128;          // this unit's output columns
+      float m = -INFINITY, l = 0.f;
+      for (int i = 0; i < n_tiles; ++i, ++g) {
+        const int b = g & 1;
+        // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (g >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[kKeys];
+#pragma unroll
+        for (int h = 0; h < kKeys / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(tl + b * kKeys + h * 32, raw);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[h * 32 + c] = __uint_as_float(raw[c]);
+        }
+        const int valid = t_end - (t_begin + i * kKeys);  // keys of the tile that exist
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (valid >= kKeys) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) {
+            s[c] = c < valid ? s[c] : -INFINITY;
+            mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+          }
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.q_scale;
+        const bool need = mt > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {               // the whole warp takes this branch
+          const float mn = need ? mt : m;
+          if (i > 0) {
+            // the output rows hold earlier tiles of the unit: rescale them
+            // once their P V is done (factor 1 on rows that keep their max)
+            if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float c = (need && m != -INFINITY) ? ex2(m - mn) : 1.f;
+#pragma unroll
+            for (int h = 0; h < D / 32; ++h) {
+              uint32_t raw[32];
+              tmem_ld32(to + h * 32, raw);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * c);
+              tmem_st32(to + h * 32, raw);
+            }
+            l *= c;
+          }
+          m = mn;
+        }
+        const float nm = live ? -m : 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // P as 16-bit pairs over the first 32 columns of the scores; bf16 P also
+        // keeps its rounding error (p - hi) in the next 32, read by a second P V
+        uint32_t pk[kKeys / 2], pl[kKeys / 2];
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 2) {
+          const float e0 = live ? ex2(fmaf(s[c], p.q_scale, nm)) : 0.f;
+          const float e1 = live ? ex2(fmaf(s[c + 1], p.q_scale, nm)) : 0.f;
+          ls[(c >> 1) & 3] += e0 + e1;
+          pk[c >> 1] = T::pack(e0, e1);
+          if constexpr (kBF16) {
+            const float2 h = T::to_float2(pk[c >> 1]);
+            pl[c >> 1] = T::pack(e0 - h.x, e1 - h.y);
+          }
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tmem_st32(tl + b * kKeys, pk);                      // over the scores of this tile
+        if constexpr (kBF16) tmem_st32(tl + b * kKeys + kKeys / 2, pl);
+        if (valid < kKeys) {
+          // V rows past the last key may hold anything (0 x NaN is NaN): zero them
+          uint8_t* vt = stages + (g % kStages) * Lay::kStageBytes + Lay::kTileBytes;
+          for (int idx = r; idx < NH * kKeys; idx += kRows) {
+            const int kr = idx % kKeys, h = idx / kKeys;
+            if (kr >= valid) {
+              uint4* d = reinterpret_cast<uint4*>(vt + h * Lay::kLineBytes + kr * 128);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) d[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&p_full[b]);
+      }
+      if (!ok) break;
+      // the unit's partials, once its last P V is done
+      if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int64_t prow = (static_cast<int64_t>(info.seq) * p.num_heads + info.kvh * G + r) *
+                               p.max_parts + info.part;
+#pragma unroll
+      for (int h = 0; h < D / 32; ++h) {
+        uint32_t raw[32];
+        tmem_ld32(to + h * 32, raw);
+        if (live) {
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(raw[4 * e]), __uint_as_float(raw[4 * e + 1]),
+                                 __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
+        }
+      }
+      if (live) p.part_ml[prow] = make_float2(m, l);
+      tc_fence_before();
+      mbar_arrive(&o_free[slot]);
+    }
+    if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int D, typename T>
+static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                          const Params& p, cudaStream_t s) {
+  auto kern = decode_tc_kernel<D, T>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  static int sms = 0;
+  // one CTA per SM: it holds all 512 tensor-memory columns, so shared memory is
+  // requested past half an SM even where the layout needs less (d = 64)
+  constexpr int kSmemLaunch = Layout<D>::kSmem > 120 * 1024 ? Layout<D>::kSmem : 120 * 1024;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
+    int dev = 0;
+    if (attr == cudaSuccess) attr = cudaGetDevice(&dev);
+    if (attr == cudaSuccess)
+      attr = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (attr != cudaSuccess) return attr;
+  const int grid = std::max(1, std::min(p.total_units, sms));
+  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kSmemLaunch, s>>>(tk, tv, tq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tcdec
+
+// From 32 heads per KV head on, reading each K/V byte once beats the
+// warp-level path's re-reads (measured: 1.6x at 32, 2.6x at 64, 4.3x at 128
+// heads; at 16 the warp-level path's two reads still win).
+bool decode_tc_supported(int group, int head_size, int block_size, int partition_tokens) {
+  return group >= 32 && tcdec::kRows % group == 0 && (head_size == 64 || head_size == 128) &&
+         block_size >= 8 && partition_tokens % tcdec::kKeys == 0;
+}
+
+cudaError_t launch_decode_tc(const DecodeTcArgs& a, cudaStream_t s) {
+  const int group = a.num_heads / a.num_kv_heads;
+  const int box_rows = std::min(a.block_size, tcdec::kKeys);
+  const int64_t slots = static_cast<int64_t>(a.num_blocks) * a.block_size;
+  CUtensorMap tk, tv, tq;
+  if (!encode_cache_map(&tk, a.k_cache, a.head_size, a.num_kv_heads, slots, box_rows,
+                        kLineSwizzled) ||
+      !encode_cache_map(&tv, a.v_cache, a.head_size, a.num_kv_heads, slots, box_rows,
+                        kLineSwizzled) ||
+      !encode_query_map(&tq, a.q, a.head_size, static_cast<int64_t>(a.num_seqs) * a.num_heads,
+                        group))
+    return cudaErrorInvalidValue;
+  tcdec::Params p{};
+  p.part_acc = a.part_acc;
+  p.part_ml = a.part_ml;
+  p.counter = a.counter;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.err = a.err;
+  p.num_seqs = a.num_seqs;
+  p.num_heads = a.num_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = group;
+  p.num_blocks = a.num_blocks;
+  p.block_size = a.block_size;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.partition_tokens = a.partition_tokens;
+  p.max_parts = a.max_parts;
+  p.total_units = a.max_parts * a.num_seqs * a.num_kv_heads;
+  p.box_rows = box_rows;
+  p.q_scale = a.q_scale;
+  if (a.head_size == 128)
+    return a.bf16 ? tcdec::launch<128, BF16>(tk, tv, tq, p, s)
+                  : tcdec::launch<128, F16>(tk, tv, tq, p, s);
+  return a.bf16 ? tcdec::launch<64, BF16>(tk, tv, tq, p, s)
+                : tcdec::launch<64, F16>(tk, tv, tq, p, s);
+}
+
+}  // namespace pkv

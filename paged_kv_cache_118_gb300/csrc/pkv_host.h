@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 #include <cstdint>
 
@@ -21,5 +22,30 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 enum CacheView { kRowsPlain = 0, kRowsSwizzled = 1, kLineSwizzled = 2 };
 bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads, int64_t slots,
                       int box_rows, CacheView view);
+
+// TMA map of the queries [rows][D] (16-bit elements) as (64 elements, D/64
+// lines, row) with the box 64 x 1 x box_rows and the 128-byte swizzle: one
+// line of box_rows consecutive rows per copy.
+bool encode_query_map(CUtensorMap* tm, const void* base, int D, int64_t rows, int box_rows);
+
+struct DecodeTcArgs {
+  float* part_acc;
+  float2* part_ml;
+  int* counter;                        // zero at launch
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t* err;
+  int num_seqs, num_heads, num_kv_heads, head_size, num_blocks, block_size, max_blocks_per_seq;
+  int partition_tokens, max_parts;
+  bool bf16;
+  float q_scale;                       // scale * log2(e)
+};
+// The tensor-memory decode path for large query groups (decode_tc.cu): writes
+// the same partition partials as the other decode paths.
+bool decode_tc_supported(int group, int head_size, int block_size, int partition_tokens);
+cudaError_t launch_decode_tc(const DecodeTcArgs& a, cudaStream_t stream);
 
 }  // namespace pkv

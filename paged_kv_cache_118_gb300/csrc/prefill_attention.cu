@@ -294,6 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kKeys / 16; ++kk)
           tc_mma_f16_ts(d, a + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO,
                         (j > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (kBF16) {                              // + (p - hi) V
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            tc_mma_f16_ts(d, a + kKeys / 2 + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO, 1u);
+        }
         tc_commit(&tbars[6 * t + 4 + b]);                   // pv_done
         return true;
       };
@@ -346,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_my; ++j) {
       const int b = j & 1;
-      if (!mbar_wait(&s_full[b], (j >> 1) & 1)) {
+      // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (j >> 1) & 1))) {
         ok = false;
         break;
       }
@@ -374,15 +380,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.q_scale;
-      if (mt > m + kRescaleThreshold) {
-        if (m != -INFINITY) {
-          // the output row holds earlier tiles: rescale it once their P V is done
-          if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+      const bool need = mt > m + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {                 // the whole warp takes this branch
+        const float mn = need ? mt : m;
+        if (j > 0) {
+          // the output rows hold earlier tiles: rescale them once their P V is
+          // done (factor 1 on rows that keep their max or hold nothing yet)
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float c = ex2(m - mt);
+          const float c = (need && m != -INFINITY) ? ex2(m - mn) : 1.f;
 #pragma unroll
           for (int h = 0; h < D / 32; ++h) {
             uint32_t raw[32];
@@ -393,22 +402,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           l *= c;
         }
-        m = mt;
+        m = mn;
       }
       // p = 2^(scale s - m): a masked score is -inf and gives 0 (m is finite
       // on a live row from its first tile on; a row past the chunk writes 0)
       const float nm = live ? -m : 0.f;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[kKeys / 2];                               // P as 16-bit pairs, key order
+      // P as 16-bit pairs over the first 32 columns of the scores; bf16 P also
+      // keeps its rounding error (p - hi) in the next 32, read by a second P V
+      uint32_t pk[kKeys / 2], pl[kKeys / 2];
 #pragma unroll
       for (int i = 0; i < kKeys; i += 2) {
         const float e0 = live ? ex2(fmaf(s[i], p.q_scale, nm)) : 0.f;
         const float e1 = live ? ex2(fmaf(s[i + 1], p.q_scale, nm)) : 0.f;
         ls[(i >> 1) & 3] += e0 + e1;
         pk[i >> 1] = T::pack(e0, e1);
+        if constexpr (kBF16) {
+          const float2 h = T::to_float2(pk[i >> 1]);
+          pl[i >> 1] = T::pack(e0 - h.x, e1 - h.y);
+        }
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_st32(tl + b * kKeys, pk);                        // over the scores of this tile
+      if constexpr (kBF16) tmem_st32(tl + b * kKeys + kKeys / 2, pl);
       if (j == n_tiles - 1 && kv_end - key0 < kKeys) {
         if (t == zt) {
           // V rows past the last key may hold anything (0 x NaN is NaN): zero them
@@ -433,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[b]);
     }
     if (n_my > 0) {
-      if (ok && mbar_wait(&pv_done[(n_my - 1) & 1], ((n_my - 1) >> 1) & 1)) {
+      if (__all_sync(0xffffffffu,
+                     ok && mbar_wait(&pv_done[(n_my - 1) & 1], ((n_my - 1) >> 1) & 1))) {
         tc_fence_after();
         float o[D];
 #pragma unroll
@@ -469,14 +486,16 @@ static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Pa
   auto kern = prefill_kernel<D, T>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
+  // one CTA per SM: it holds all 512 tensor-memory columns, so shared memory is
+  // requested past half an SM even where the layout needs less (d = 64)
+  constexpr int kSmemLaunch = Layout<D>::kSmem > 120 * 1024 ? Layout<D>::kSmem : 120 * 1024;
   std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Layout<D>::kSmem);
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
   });
   if (attr != cudaSuccess) return attr;
   const int tiles = (p.max_query_len * p.group + kQTiles * kRows - 1) / (kQTiles * kRows);
   dim3 grid(tiles, num_kv_heads, num_seqs);
-  kern<<<grid, kThreads, Layout<D>::kSmem, s>>>(tk, tv, p);
+  kern<<<grid, kThreads, kSmemLaunch, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 

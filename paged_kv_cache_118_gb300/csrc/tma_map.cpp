@@ -61,4 +61,18 @@ bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads
   return r == CUDA_SUCCESS;
 }
 
+bool encode_query_map(CUtensorMap* tm, const void* base, int D, int64_t rows, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace pkv

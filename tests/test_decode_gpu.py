@@ -299,3 +299,30 @@ def test_shared_prefix_runs(case):
         assert_close(out, want, dt)
         outs.append(out)
     assert torch.equal(outs[0], outs[1])
+
+
+TC_CASES = [
+    # lens, H, H_kv, D, B, dtype, partition_tokens: groups of 32..128 query heads
+    # per KV head run on the tensor-memory path
+    ((1, 63, 64, 65, 700, 1500), 64, 2, 128, 16, "bf16", 512),
+    ((5, 300, 2049), 64, 2, 128, 32, "f16", 256),
+    ((77, 1000, 2), 64, 1, 64, 8, "bf16", 64),
+    ((3, 129, 4100), 128, 1, 128, 128, "f16", 0),
+    ((33, 70, 130), 32, 1, 64, 64, "f16", 128),
+    ((20, 1024, 517), 96, 3, 128, 16, "bf16", 512),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=[f"tc{i}" for i in range(len(TC_CASES))])
+def test_large_groups_against_oracle(case):
+    lens, H, Hkv, D, B, dt, pt = case
+    batch = decode_batch("t", lens, H, Hkv, D, B, dt, seed=len(lens) + H + D)
+    run_case(batch, pt=pt)
+
+
+def test_large_groups_outlier_keys():
+    """Nearly one-hot softmax rows on the tensor-memory path (rescales of the
+    output rows in tensor memory)."""
+    batch = decode_batch("t", (3000, 700, 129), 64, 2, 128, 16, "bf16", seed=21,
+                         outlier_frac=0.02)
+    run_case(batch)

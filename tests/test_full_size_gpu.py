@@ -14,8 +14,8 @@ from oracle.attention import paged_attention_decode as oracle_decode
 from oracle.block_manager import BlockManager as RefBM
 from oracle.pipeline import build_decode_state, build_shared_prefix_state, pool_demand
 from parity import (assert_close, dev, gpu_decode_state, oracle_sampled, sample_seqs)
-from workloads import (LLAMA_BLOCK_SIZES, free_order, gqa_prefix, llama13b, longctx, opt13b,
-                       poison_bits)
+from workloads import (LLAMA_BLOCK_SIZES, free_order, gqa_prefix, llama13b, longctx, mqa,
+                       opt13b, poison_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -131,6 +131,26 @@ def test_longctx_full():
     cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale), out=out32)
     torch.cuda.synchronize()
     seqs = [0, 4, 7]                       # 32k, 128k, 40k tokens
+    want = oracle_sampled(batch, seqs)
+    for s in seqs:
+        assert_close(out[s], want[s], "bf16")
+        assert_close(out32[s], want[s], "bf16")
+    assert cache.err.item() == 0
+
+
+def test_mqa_full():
+    """64 query heads on one KV head (the tensor-memory path): sampled
+    sequences against the oracle, both output types."""
+    batch = mqa(0)
+    n = _pool(batch.context_lens, 16)
+    order = free_order(n, 0)
+    cache, tables, ctx = gpu_decode_state(batch, n, order, poison=True)
+    _tables_match_oracle(batch, n, order, tables)
+    out = cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale))
+    out32 = torch.empty(out.shape, dtype=torch.float32, device="cuda")
+    cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale), out=out32)
+    torch.cuda.synchronize()
+    seqs = sample_seqs(batch.context_lens, 6, 1)
     want = oracle_sampled(batch, seqs)
     for s in seqs:
         assert_close(out[s], want[s], "bf16")

@@ -201,6 +201,12 @@ def longctx(seed: int = 0, scale_k: int = 1024) -> DecodeBatch:
     return decode_batch("longctx", lens, 32, 8, 128, 16, "bf16", seed, outlier_frac=0.01)
 
 
+def mqa(seed: int = 0, num_seqs: int = 128) -> DecodeBatch:
+    """Multi-query decode: 64 query heads sharing one KV head, head_dim 128,
+    bf16, block_size 16, a batch of 128 with lengths uniform in [1, 4096]."""
+    return decode_batch("mqa", llama13b_lengths(num_seqs, seed), 64, 1, 128, 16, "bf16", seed)
+
+
 @dataclass
 class SharedPrefixBatch:
     """Beam groups that share a prefix of physical blocks.
