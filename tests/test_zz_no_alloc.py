@@ -43,7 +43,8 @@ def _case(lens, H, Hkv, B, dt, seed):
 
 def test_matches_workspace_entry_point_twice_in_a_row():
     cases = [((3000, 17, 900, 1, 2048, 513), 32, 8, 16, "bf16", 1),
-             ((40, 700, 1500), 40, 40, 32, "f16", 2)]
+             ((40, 700, 1500), 40, 40, 32, "f16", 2),
+             ((1200, 5, 333), 64, 1, 16, "bf16", 3)]          # 64 heads per KV head: tcgen05
     runs = []
     for lens, H, Hkv, B, dt, seed in cases:
         batch, cache, tables, ctx = _case(lens, H, Hkv, B, dt, seed)
