@@ -79,22 +79,25 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(config: str, kernel_src: str, bytes_per_launch: float):
+def profile_traffic(config: str, bytes_per_launch: float):
     """DRAM bytes per decode launch, from the committed ncu summary of this
-    workload, if it was taken on the kernel source as it is now (its sha256 is
-    recorded there). The captured launch's traffic is scaled to this run's
-    launch by the ratio of algorithmic bytes (same batch, a few tokens longer
-    or shorter)."""
+    workload, if it was taken on the kernel source as it is now (the summary
+    names the source file and records its sha256). The captured launch's
+    traffic is scaled to this run's launch by the ratio of algorithmic bytes
+    (same batch, a few tokens longer or shorter)."""
     path = os.path.join(ROOT, "profiles", f"decode_partition_{config}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})\s*\((\S+)", text)
     t = re.search(r"captured_traffic_bytes:\s*([0-9]+)", text)
     a = re.search(r"captured_algorithmic_bytes:\s*([0-9]+)", text)
     if not (m and t and a):
         return None
-    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    src = os.path.join(ROOT, m.group(2))
+    if not os.path.exists(src):
+        return None
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
     if m.group(1) != cur:
         return None
     return round(float(t.group(1)) * bytes_per_launch / float(a.group(1)))
@@ -399,8 +402,7 @@ def run_ours(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2)}
 
     peak, peak_kind = load_peaks()
-    src = os.path.join(ROOT, "paged_kv_cache_118_gb300", "csrc", "decode_attention.cu")
-    traffic = profile_traffic(args.config, src, float(np.mean(per_call)))
+    traffic = profile_traffic(args.config, float(np.mean(per_call)))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),

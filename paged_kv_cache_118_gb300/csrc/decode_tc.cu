@@ -14,19 +14,28 @@
 // product, and each K/V byte is read once.
 //
 // How (persistent CTAs, one per SM, 256 threads):
-//  * warp 0 claims units (partition, sequence, KV head) from a global counter,
-//    partition-major; per unit it loads the G query rows by TMA into one of two
-//    query buffers and streams the partition's 64-key K/V tiles (one TMA copy
-//    per physical block and 128-byte line) into a 4-stage ring;
+//  * warp 0 claims units (sequence, partition, KV head) from a global counter.
+//    Up to 1024 sequences, only units that exist are numbered: every whole
+//    partition first, then the partial last ones, which fill the end of the
+//    run (prefix sums per sequence); larger batches number them all and skip
+//    the empty ones. Per unit it reads the partition's block ids (one per lane),
+//    loads the G query rows by TMA into one of two query buffers and streams
+//    the partition's 64-key K/V tiles into a ring of 3 to 6 stages (as many
+//    as shared memory holds beside the rest), one TMA copy per
+//    physical block and 128-byte line, issued by several lanes at once;
 //  * one thread of warp 1 owns the 512 tensor-memory columns (two 64-column
 //    score buffers, two D-column output buffers, one per unit in flight) and
 //    issues S = Q K^T (M = 128, N = 64, K = D) and O += P V (P from tensor
 //    memory), committing each to an mbarrier; a tile's S is issued before the
 //    previous tile's P V, and the next unit's first S as soon as its queries
 //    are in;
-//  * warps 4-7 run the softmax, one thread per query row (its TMEM lane); rows
-//    past G are padding. At the end of a unit they write the partials from
-//    the unit's output buffer while the next unit runs in the other.
+//  * warps 4-7 run the softmax, one thread per query row (its TMEM lane). The
+//    query rows hold 128 / G copies of the group's G heads, and copy c of a
+//    head takes keys [c 64 G / 128, (c + 1) 64 G / 128) of every tile (its P
+//    is 0 elsewhere), so every thread works on 64 G / 128 keys per tile. At
+//    the end of a unit the copies of a head are merged through shared memory
+//    and the partials written, while the next unit runs in the other output
+//    buffer.
 // Every wait is bounded; bad block ids and lengths are reported and skipped.
 
 #include <cuda.h>
@@ -46,9 +55,12 @@ namespace tcdec {
 
 constexpr int kRows = 128;             // product rows: query heads of the KV head, padded
 constexpr int kKeys = 64;              // keys per tile
-constexpr int kStages = 4;
+constexpr int kMaxStages = 6;
+constexpr int kSmemLimit = 232448;     // shared memory one CTA may ask for
 constexpr int kThreads = 256;          // warp 0: claims and copies; warp 1: MMA; warps 4-7: softmax
 constexpr int kSoftmaxWarp0 = 4;
+constexpr int kMaxIds = 256;           // block ids of one unit, read ahead of its copies
+constexpr int kCompactMaxSeqs = 1024;  // batches up to this size get a compact work list
 // S0 [0, 64), S1 [64, 128), O0 [128, 128 + D), O1 [256, 256 + D)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
@@ -75,12 +87,15 @@ struct UnitInfo {
 
 // Shared memory from a 1024-byte aligned base; operands are 128-byte rows with
 // the 128-byte swizzle, 8-row groups 1024 bytes apart:
-//  Q, two buffers: D/64 column blocks of 128 rows (A of S, K-major; rows past
-//  G hold whatever an earlier unit left, and only their own rows of S, P and
-//  O see it);
+//  Q, two buffers: D/64 column blocks of 128 rows, 128 / G copies of the G
+//  query rows (A of S, K-major);
 //  each stage: K then V, D/64 line blocks of 64 key rows (B of S, K-major; B
-//  of P V, MN-major with the next 64 columns one line block on).
-template <int D>
+//  of P V, MN-major with the next 64 columns one line block on);
+//  merge area: (m, l, O) of the C - 1 copies past the first, one row of D + 3
+//  floats (an odd stride, so a warp writing its rows meets no bank conflict);
+//  then the barriers, the unit slots and the work list.
+// The ring takes as many stages (up to kMaxStages) as the rest leaves room for.
+template <int D, int C>
 struct Layout {
   static constexpr int NH = D / 64;
   static constexpr int kQBytes = kRows * D * 2;
@@ -88,21 +103,38 @@ struct Layout {
   static constexpr int kTileBytes = NH * kLineBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kOffStages = 2 * kQBytes;
-  static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
-  // stage_full[S], stage_empty[S], unit_full[2], unit_empty[2], q_full[2],
-  // q_free[2], s_full[2], p_full[2], pv_done[2], o_free[2], drain
-  static constexpr int kNumBars = 2 * kStages + 2 * 8 + 1;
+  static constexpr int kMergeStride = D + 3;
+  static constexpr int kMergeBytes = (kRows - kRows / C) * kMergeStride * 4;
+  // barriers: stage_full[S], stage_empty[S], unit_full[2], unit_empty[2],
+  // q_full[2], q_free[2], s_full[2], p_full[2], pv_done[2], o_free[2], drain,
+  // mrg_full, mrg_free
+  static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 3) * 8 +
+                                    2 * static_cast<int>(sizeof(UnitInfo)) + kMaxIds * 4 +
+                                    2 * (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 4 + 16;
+  static constexpr int kFit =
+      (kSmemLimit - 1024 - kOffStages - kMergeBytes - kTailBytes - 16) / kStageBytes;
+  static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
+  static constexpr int kOffMerge = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffBars = (kOffMerge + kMergeBytes + 15) / 16 * 16;
+  static constexpr int kNumBars = 2 * kStages + 2 * 8 + 3;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;
-  static constexpr int kOffTmem = kOffUnits + 2 * static_cast<int>(sizeof(UnitInfo));
+  static constexpr int kOffIds = kOffUnits + 2 * static_cast<int>(sizeof(UnitInfo));
+  static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions
+  static constexpr int kOffTail = kOffPref + (kCompactMaxSeqs + 4) * 4;   // last, partial ones
+  static constexpr int kOffLens = kOffTail + (kCompactMaxSeqs + 4) * 4;
+  static constexpr int kOffTmem = kOffLens + kCompactMaxSeqs * 4;
   static constexpr int kSmem = 1024 + kOffTmem + 16;
+  static_assert(kStages >= 3 && kSmem <= kSmemLimit, "shared memory of one CTA");
 };
 
-template <int D, typename T>
+// C: copies of the G = 128 / C query rows in the product's rows.
+template <int D, typename T, int C>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const Params p) {
-  using Lay = Layout<D>;
+  using Lay = Layout<D, C>;
+  constexpr int kStages = Lay::kStages;
   constexpr int NH = Lay::NH;
   constexpr bool kBF16 = std::is_same<T, BF16>::value;
   extern __shared__ uint8_t smem_raw[];
@@ -121,7 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_free = pv_done + 2;
   uint64_t* drain = o_free + 2;
+  uint64_t* mrg_full = drain + 1;
+  uint64_t* mrg_free = mrg_full + 1;
+  float* merge = reinterpret_cast<float*>(smem + Lay::kOffMerge);
   UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + Lay::kOffUnits);
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + Lay::kOffIds);
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + Lay::kOffPref);
+  int32_t* tpref = reinterpret_cast<int32_t*>(smem + Lay::kOffTail);
+  int32_t* lens = reinterpret_cast<int32_t*>(smem + Lay::kOffLens);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
 
   const int warp = threadIdx.x >> 5;
@@ -147,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_free[i], kRows);
     }
     mbar_init(drain, 1);
+    mbar_init(mrg_full, C > 1 ? kRows - kRows / C : 1);  // the copies past the first
+    mbar_init(mrg_free, kRows / C);                      // the first copies
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -161,92 +202,186 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_q);
-      const uint64_t policy = l2_evict_first_policy();
-      const int R = p.box_rows;
-      const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
-      const int per_part = p.num_seqs * p.num_kv_heads;
-      int g = 0;                                           // tiles issued
-      int k = 0;                                           // units published
-      int last_issued[kStages];
+    }
+    const uint64_t policy = l2_evict_first_policy();
+    const int R = p.box_rows;
+    const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
+    const int Hkv = p.num_kv_heads;
+    // The work list. Batches of up to kCompactMaxSeqs sequences number only
+    // the units that exist: first every whole partition, sequence-major, then
+    // the partial last partitions, shorter on average, so that they fill the
+    // end of the run (prefix sums per sequence, then a binary search per
+    // claim). Larger batches number every (partition, sequence, KV head),
+    // partition-major, and skip the empty ones.
+    const bool compact = p.num_seqs <= kCompactMaxSeqs;
+    int total = p.total_units;
+    int whole_units = 0;
+    if (compact) {
+      int lv[kCompactMaxSeqs / 32];                        // all lengths in one round of loads
 #pragma unroll
-      for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
-      bool ok = true;
-      while (ok) {
-        const int u = atomicAdd(p.counter, 1);
-        UnitInfo info{-1, 0, 0, 0};
-        int t_begin = 0, t_end = 0;
-        if (u < p.total_units) {
-          const int part = u / per_part;
+      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
+        const int sq = it * 32 + lane;
+        lv[it] = sq < p.num_seqs ? __ldg(p.context_lens + sq) : 0;
+      }
+      int carry = 0, tcarry = 0;
+#pragma unroll
+      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
+        if (it * 32 >= p.num_seqs) break;
+        const int sq = it * 32 + lane;
+        const int L = lv[it];
+        const bool valid = sq < p.num_seqs && L >= 1 && L <= max_ctx;
+        if (sq < p.num_seqs && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+        int x = valid ? L / PT : 0;                        // whole partitions
+        int y = valid && L % PT != 0 ? 1 : 0;              // a partial last one
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int xo = __shfl_up_sync(0xffffffffu, x, o);
+          const int yo = __shfl_up_sync(0xffffffffu, y, o);
+          if (lane >= o) {
+            x += xo;
+            y += yo;
+          }
+        }
+        if (sq < p.num_seqs) {
+          pref[sq + 1] = carry + x;
+          tpref[sq + 1] = tcarry + y;
+          lens[sq] = L;
+        }
+        carry += __shfl_sync(0xffffffffu, x, 31);
+        tcarry += __shfl_sync(0xffffffffu, y, 31);
+      }
+      if (lane == 0) {
+        pref[0] = 0;
+        tpref[0] = 0;
+      }
+      whole_units = carry;
+      total = (carry + tcarry) * Hkv;
+      __syncwarp();
+    }
+    int g = 0;                                             // tiles issued
+    int k = 0;                                             // units published
+    int last_issued[kStages];
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
+    bool ok = true;
+    while (ok) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(p.counter, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      UnitInfo info{-1, 0, 0, 0};
+      int t_begin = 0, t_end = 0;
+      if (u < total) {
+        int seq, kvh, part, L;
+        if (compact) {
+          int w = u / Hkv;
+          kvh = u - w * Hkv;
+          const bool tail = w >= whole_units;
+          const int32_t* pf = tail ? tpref : pref;
+          if (tail) w -= whole_units;
+          int lo = 0, hi = p.num_seqs;                     // largest lo with pf[lo] <= w
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pf[mid] <= w) lo = mid; else hi = mid;
+          }
+          seq = lo;
+          L = lens[lo];
+          part = tail ? L / PT : w - pref[lo];
+        } else {
+          const int per_part = p.num_seqs * Hkv;
+          part = u / per_part;
           const int rem = u - part * per_part;
-          const int seq = rem / p.num_kv_heads;
-          const int kvh = rem - seq * p.num_kv_heads;
-          const int L = __ldg(p.context_lens + seq);
+          seq = rem / Hkv;
+          kvh = rem - seq * Hkv;
+          L = __ldg(p.context_lens + seq);
           if (L < 1 || L > max_ctx) {
-            if (part == 0 && kvh == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+            if (lane == 0 && part == 0 && kvh == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
             continue;
           }
-          t_begin = part * PT;
-          if (t_begin >= L) continue;                      // this sequence has no such partition
-          t_end = min(L, t_begin + PT);
-          info = UnitInfo{seq, kvh, part, L};
+          if (part * PT >= L) continue;                    // this sequence has no such partition
         }
-        const int slot = k & 1;
-        if (k >= 2 && (!mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1) ||
-                       !mbar_wait(&q_free[slot], ((k >> 1) & 1) ^ 1))) {
+        t_begin = part * PT;
+        t_end = min(L, t_begin + PT);
+        info = UnitInfo{seq, kvh, part, L};
+      }
+      const int b0 = t_begin / B;
+      if (info.seq >= 0) {
+        // lane 0 read the previous unit's ids before the __syncwarp that ends
+        // the loop
+        const int32_t* row =
+            p.block_tables + static_cast<int64_t>(info.seq) * p.max_blocks_per_seq;
+        const int nb = (t_end - 1) / B - b0 + 1;
+        for (int i = lane; i < nb; i += 32) {
+          int32_t id = __ldg(row + b0 + i);
+          if (id < 0 || id >= p.num_blocks) {
+            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+            id = 0;
+          }
+          ids[i] = id;
+        }
+      }
+      __syncwarp();
+      const int slot = k & 1;
+      bool w_ok = true;
+      if (lane == 0 && k >= 2)
+        w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1) &&
+               mbar_wait(&q_free[slot], ((k >> 1) & 1) ^ 1);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        units[slot] = info;
+        if (info.seq >= 0) {
+          // the group's query rows, once per copy
+          mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(NH) * kRows * 128);
+          const int row0 = info.seq * p.num_heads + info.kvh * G;
+#pragma unroll
+          for (int c = 0; c < C; ++c)
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              tma_load_3d(qbufs + slot * Lay::kQBytes + h * kRows * 128 + c * G * 128, &tm_q,
+                          &q_full[slot], 0, h, row0, policy);
+        }
+        mbar_arrive(&unit_full[slot]);
+      }
+      ++k;
+      if (info.seq < 0) break;
+      // lane l copies line (l / 2) % NH of K (l even) or V (l odd) for the
+      // tile's copy l / (2 NH)
+      const int my_c = lane / (2 * NH);
+      const int my_h = (lane >> 1) % NH;
+      const CUtensorMap* my_map = (lane & 1) ? &tm_v : &tm_k;
+      const uint32_t my_off =
+          (lane & 1) * Lay::kTileBytes + my_h * Lay::kLineBytes + my_c * copy_bytes;
+      const int n_tiles = (t_end - t_begin + kKeys - 1) / kKeys;
+      for (int i = 0; i < n_tiles; ++i, ++g) {
+        const int st = g % kStages;
+        bool e_ok = true;
+        if (lane == 0 && g >= kStages) e_ok = mbar_wait(&stage_empty[st], ((g / kStages) & 1) ^ 1);
+        if (!__shfl_sync(0xffffffffu, e_ok, 0)) {
           ok = false;
           break;
         }
-        units[slot] = info;
-        if (info.seq >= 0) {
-          // the group's query rows, one copy per 128-byte line
-          mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(NH) * G * 128);
-          const int row0 = info.seq * p.num_heads + info.kvh * G;
-#pragma unroll
-          for (int h = 0; h < NH; ++h)
-            tma_load_3d(qbufs + slot * Lay::kQBytes + h * kRows * 128, &tm_q, &q_full[slot], 0, h,
-                        row0, policy);
-        }
-        mbar_arrive(&unit_full[slot]);
-        ++k;
-        if (info.seq < 0) break;
-        const int32_t* row = p.block_tables + static_cast<int64_t>(info.seq) * p.max_blocks_per_seq;
-        const int n_tiles = (t_end - t_begin + kKeys - 1) / kKeys;
-        for (int i = 0; i < n_tiles; ++i, ++g) {
-          const int st = g % kStages;
-          if (g >= kStages && !mbar_wait(&stage_empty[st], ((g / kStages) & 1) ^ 1)) {
-            ok = false;
-            break;
-          }
-          const int t0 = t_begin + i * kKeys;
-          const int valid = min(kKeys, t_end - t0);
-          const int copies = (valid + R - 1) / R;
-          uint8_t* kdst = stages + st * Lay::kStageBytes;
-          uint8_t* vdst = kdst + Lay::kTileBytes;
+        const int t0 = t_begin + i * kKeys;
+        const int copies = (min(kKeys, t_end - t0) + R - 1) / R;
+        if (lane == 0) {
           mbar_arrive_expect_tx(&stage_full[st], 2u * NH * copies * copy_bytes);
-          for (int c = 0; c < copies; ++c) {
-            const int tk = t0 + c * R;
-            int32_t id = __ldg(row + tk / B);
-            if (id < 0 || id >= p.num_blocks) {
-              flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-              id = 0;
-            }
-            const int z = id * B + tk % B;
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              tma_load_4d(kdst + h * Lay::kLineBytes + c * copy_bytes, &tm_k, &stage_full[st], 0,
-                          z, info.kvh, h, policy);
-              tma_load_4d(vdst + h * Lay::kLineBytes + c * copy_bytes, &tm_v, &stage_full[st], 0,
-                          z, info.kvh, h, policy);
-            }
-          }
           last_issued[st] = g;
         }
+        __syncwarp();
+        if (my_c < copies) {
+          const int tk = t0 + my_c * R;
+          const int z = ids[tk / B - b0] * B + tk % B;
+          tma_load_4d(stages + st * Lay::kStageBytes + my_off, my_map, &stage_full[st], 0, z,
+                      info.kvh, my_h, policy);
+        }
       }
-      if (!ok) {
-        flag_error(p.err, PKV_DEVERR_TIMEOUT);
-        for (int st = 0; st < kStages; ++st)
-          if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
-      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      for (int st = 0; st < kStages; ++st)
+        if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
@@ -334,9 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- softmax
+    constexpr int KC = kKeys / C;                          // keys of a tile per copy
     const int r = (warp - kSoftmaxWarp0) * 32 + lane;     // row = TMEM lane
     const uint32_t tl = tbase + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
-    const bool live = r < G;
+    const int cp = r / G;                                  // copy (the same across a warp)
+    const int hr = r - cp * G;                             // head of the group
     int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -361,24 +498,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float s[kKeys];
+        // this copy's KC scores of the tile
+        float s[KC];
+        {
+          float all[kKeys];
 #pragma unroll
-        for (int h = 0; h < kKeys / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(tl + b * kKeys + h * 32, raw);
+          for (int h = 0; h < kKeys / 32; ++h) {
+            uint32_t raw[32];
+            tmem_ld32(tl + b * kKeys + h * 32, raw);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[h * 32 + c] = __uint_as_float(raw[c]);
+            for (int e = 0; e < 32; ++e) all[h * 32 + e] = __uint_as_float(raw[e]);
+          }
+#pragma unroll
+          for (int e = 0; e < KC; ++e) {
+            float v = all[e];
+#pragma unroll
+            for (int cc = 1; cc < C; ++cc) v = cp == cc ? all[cc * KC + e] : v;
+            s[e] = v;
+          }
         }
-        const int valid = t_end - (t_begin + i * kKeys);  // keys of the tile that exist
+        const int tile_valid = t_end - (t_begin + i * kKeys);   // keys of the tile that exist
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (valid >= kKeys) {
+        if (tile_valid >= kKeys) {
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+          for (int e = 0; e < KC; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
         } else {
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) {
-            s[c] = c < valid ? s[c] : -INFINITY;
-            mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+          for (int e = 0; e < KC; ++e) {
+            s[e] = cp * KC + e < tile_valid ? s[e] : -INFINITY;
+            mx[e & 3] = fmaxf(mx[e & 3], s[e]);
           }
         }
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.q_scale;
@@ -406,31 +554,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m = mn;
         }
-        const float nm = live ? -m : 0.f;
+        // p = 2^(scale s - m) on this copy's keys, 0 on the others' (a slice
+        // with no key yet keeps m = -inf and gives 0)
+        const float nm = m == -INFINITY ? 0.f : -m;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t vh[KC / 2], vl[KC / 2];
+#pragma unroll
+        for (int e = 0; e < KC; e += 2) {
+          const float e0 = ex2(fmaf(s[e], p.q_scale, nm));
+          const float e1 = ex2(fmaf(s[e + 1], p.q_scale, nm));
+          ls[(e >> 1) & 3] += e0 + e1;
+          vh[e >> 1] = T::pack(e0, e1);
+          if constexpr (kBF16) {
+            const float2 h = T::to_float2(vh[e >> 1]);
+            vl[e >> 1] = T::pack(e0 - h.x, e1 - h.y);
+          }
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // P as 16-bit pairs over the first 32 columns of the scores; bf16 P also
         // keeps its rounding error (p - hi) in the next 32, read by a second P V
         uint32_t pk[kKeys / 2], pl[kKeys / 2];
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 2) {
-          const float e0 = live ? ex2(fmaf(s[c], p.q_scale, nm)) : 0.f;
-          const float e1 = live ? ex2(fmaf(s[c + 1], p.q_scale, nm)) : 0.f;
-          ls[(c >> 1) & 3] += e0 + e1;
-          pk[c >> 1] = T::pack(e0, e1);
-          if constexpr (kBF16) {
-            const float2 h = T::to_float2(pk[c >> 1]);
-            pl[c >> 1] = T::pack(e0 - h.x, e1 - h.y);
+        for (int cc = 0; cc < C; ++cc)
+#pragma unroll
+          for (int e = 0; e < KC / 2; ++e) {
+            pk[cc * KC / 2 + e] = cp == cc ? vh[e] : 0u;
+            if constexpr (kBF16) pl[cc * KC / 2 + e] = cp == cc ? vl[e] : 0u;
           }
-        }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st32(tl + b * kKeys, pk);                      // over the scores of this tile
         if constexpr (kBF16) tmem_st32(tl + b * kKeys + kKeys / 2, pl);
-        if (valid < kKeys) {
+        if (tile_valid < kKeys) {
           // V rows past the last key may hold anything (0 x NaN is NaN): zero them
           uint8_t* vt = stages + (g % kStages) * Lay::kStageBytes + Lay::kTileBytes;
           for (int idx = r; idx < NH * kKeys; idx += kRows) {
             const int kr = idx % kKeys, h = idx / kKeys;
-            if (kr >= valid) {
+            if (kr >= tile_valid) {
               uint4* d = reinterpret_cast<uint4*>(vt + h * Lay::kLineBytes + kr * 128);
 #pragma unroll
               for (int e = 0; e < 8; ++e) d[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -448,21 +606,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int64_t prow = (static_cast<int64_t>(info.seq) * p.num_heads + info.kvh * G + r) *
+      const int64_t prow = (static_cast<int64_t>(info.seq) * p.num_heads + info.kvh * G + hr) *
                                p.max_parts + info.part;
+      if constexpr (C == 1) {
 #pragma unroll
-      for (int h = 0; h < D / 32; ++h) {
-        uint32_t raw[32];
-        tmem_ld32(to + h * 32, raw);
-        if (live) {
+        for (int h = 0; h < D / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(to + h * 32, raw);
           float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(__uint_as_float(raw[4 * e]), __uint_as_float(raw[4 * e + 1]),
                                  __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
         }
+        p.part_ml[prow] = make_float2(m, l);
+      } else if (cp > 0) {
+        // hand (m, l, O) to the first copy of the head
+        if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (k - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        float* row = merge + ((cp - 1) * G + hr) * Lay::kMergeStride;
+#pragma unroll
+        for (int h = 0; h < D / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(to + h * 32, raw);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) row[h * 32 + e] = __uint_as_float(raw[e]);
+        }
+        row[D] = m;
+        row[D + 1] = l;
+        mbar_arrive(mrg_full);
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1))) {
+          ok = false;
+          break;
+        }
+        float f[C], M = m;
+#pragma unroll
+        for (int cc = 1; cc < C; ++cc) M = fmaxf(M, merge[((cc - 1) * G + hr) * Lay::kMergeStride + D]);
+        f[0] = m == -INFINITY ? 0.f : ex2(m - M);
+        float lt = l * f[0];
+#pragma unroll
+        for (int cc = 1; cc < C; ++cc) {
+          const float* row = merge + ((cc - 1) * G + hr) * Lay::kMergeStride;
+          f[cc] = row[D] == -INFINITY ? 0.f : ex2(row[D] - M);
+          lt = fmaf(row[D + 1], f[cc], lt);
+        }
+#pragma unroll
+        for (int h = 0; h < D / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(to + h * 32, raw);
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(raw[e]) * f[0];
+#pragma unroll
+          for (int cc = 1; cc < C; ++cc) {
+            const float* row = merge + ((cc - 1) * G + hr) * Lay::kMergeStride + h * 32;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = fmaf(row[e], f[cc], o[e]);
+          }
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        }
+        p.part_ml[prow] = make_float2(M, lt);
+        mbar_arrive(mrg_free);
       }
-      if (live) p.part_ml[prow] = make_float2(m, l);
       tc_fence_before();
       mbar_arrive(&o_free[slot]);
     }
@@ -476,16 +687,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, typename T>
+template <int D, typename T, int C>
 static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                           const Params& p, cudaStream_t s) {
-  auto kern = decode_tc_kernel<D, T>;
+  auto kern = decode_tc_kernel<D, T, C>;
+  using Lay = Layout<D, C>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   static int sms = 0;
   // one CTA per SM: it holds all 512 tensor-memory columns, so shared memory is
   // requested past half an SM even where the layout needs less (d = 64)
-  constexpr int kSmemLaunch = Layout<D>::kSmem > 120 * 1024 ? Layout<D>::kSmem : 120 * 1024;
+  constexpr int kSmemLaunch = Lay::kSmem > 120 * 1024 ? Lay::kSmem : 120 * 1024;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
     int dev = 0;
@@ -501,14 +713,33 @@ static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const CU
   return cudaGetLastError();
 }
 
+template <int C>
+static cudaError_t launch_c(int D, bool bf16, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tq, const Params& p, cudaStream_t s) {
+  if (D == 128) return bf16 ? launch<128, BF16, C>(tk, tv, tq, p, s)
+                            : launch<128, F16, C>(tk, tv, tq, p, s);
+  return bf16 ? launch<64, BF16, C>(tk, tv, tq, p, s) : launch<64, F16, C>(tk, tv, tq, p, s);
+}
+
 }  // namespace tcdec
+
+static cudaError_t dispatch_copies(int D, bool bf16, int copies, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tq,
+                                   const tcdec::Params& p, cudaStream_t s) {
+  switch (copies) {
+    case 1: return tcdec::launch_c<1>(D, bf16, tk, tv, tq, p, s);
+    case 2: return tcdec::launch_c<2>(D, bf16, tk, tv, tq, p, s);
+    default: return tcdec::launch_c<4>(D, bf16, tk, tv, tq, p, s);
+  }
+}
 
 // From 32 heads per KV head on, reading each K/V byte once beats the
 // warp-level path's re-reads (measured: 1.6x at 32, 2.6x at 64, 4.3x at 128
 // heads; at 16 the warp-level path's two reads still win).
 bool decode_tc_supported(int group, int head_size, int block_size, int partition_tokens) {
   return group >= 32 && tcdec::kRows % group == 0 && (head_size == 64 || head_size == 128) &&
-         block_size >= 8 && partition_tokens % tcdec::kKeys == 0;
+         block_size >= 8 && partition_tokens % tcdec::kKeys == 0 &&
+         partition_tokens / block_size + 2 <= tcdec::kMaxIds;
 }
 
 cudaError_t launch_decode_tc(const DecodeTcArgs& a, cudaStream_t s) {
@@ -542,11 +773,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs& a, cudaStream_t s) {
   p.total_units = a.max_parts * a.num_seqs * a.num_kv_heads;
   p.box_rows = box_rows;
   p.q_scale = a.q_scale;
-  if (a.head_size == 128)
-    return a.bf16 ? tcdec::launch<128, BF16>(tk, tv, tq, p, s)
-                  : tcdec::launch<128, F16>(tk, tv, tq, p, s);
-  return a.bf16 ? tcdec::launch<64, BF16>(tk, tv, tq, p, s)
-                : tcdec::launch<64, F16>(tk, tv, tq, p, s);
+  return dispatch_copies(a.head_size, a.bf16, tcdec::kRows / group, tk, tv, tq, p, s);
 }
 
 }  // namespace pkv

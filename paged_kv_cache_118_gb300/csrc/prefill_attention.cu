@@ -13,8 +13,9 @@
 // 128 rows; a row is one (query token, query head of the KV head's group), so
 // 128/G tokens per query tile):
 //  * warp 0 streams 64-key tiles of K and V over the causal range only, one
-//    TMA copy per physical block and 128-byte line (128-byte swizzle), into a
-//    3-stage ring completing on mbarriers; both query tiles use each K/V tile;
+//    TMA copy per physical block and 128-byte line (128-byte swizzle), each
+//    lane issuing one, into a 5-stage ring completing on mbarriers; both
+//    query tiles use each K/V tile;
 //  * warp 1 owns the tensor memory (per query tile: two 64-column score
 //    buffers and the D-column output) and issues, from one thread, S = Q K^T
 //    (M = 128, N = 64, K = D) into a score buffer and O += P V (M = 128,
@@ -201,52 +202,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- copies
+    // Lane l copies line (l / 2) % NH of K (l even) or V (l odd) for the
+    // tile's copy l / (2 NH); it reads that copy's block id before the wait
+    // for the stage, so the read overlaps the wait.
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const uint64_t policy = l2_evict_first_policy();
-      const int R = p.box_rows;
-      const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
-      const int32_t* row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
-      int last_issued[kStages];
+    }
+    const uint64_t policy = l2_evict_first_policy();
+    const int R = p.box_rows;
+    const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
+    const int32_t* row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
+    const int my_c = lane / (2 * NH);
+    const int my_h = (lane >> 1) % NH;
+    const CUtensorMap* my_map = (lane & 1) ? &tm_v : &tm_k;
+    const uint32_t my_off =
+        (lane & 1) * Lay::kTileBytes + my_h * Lay::kLineBytes + my_c * copy_bytes;
+    int last_issued[kStages];
 #pragma unroll
-      for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
-      bool ok = true;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(&stage_empty[st], ((j / kStages) & 1) ^ 1)) {
-          ok = false;
-          break;
-        }
-        const int t0 = j * kKeys;
-        const int valid = min(kKeys, kv_end - t0);
-        const int copies = (valid + R - 1) / R;            // copies of R rows cover the keys
-        uint8_t* kdst = stages + st * Lay::kStageBytes;
-        uint8_t* vdst = kdst + Lay::kTileBytes;
+    for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % kStages;
+      const int t0 = j * kKeys;
+      const int copies = (min(kKeys, kv_end - t0) + R - 1) / R;   // copies of R rows cover the keys
+      const bool mine = my_c < copies;
+      const int tk = t0 + my_c * R;                        // first key of the lane's copy
+      int32_t id = mine ? __ldg(row + tk / B) : 0;
+      bool e_ok = true;
+      if (lane == 0 && j >= kStages) e_ok = mbar_wait(&stage_empty[st], ((j / kStages) & 1) ^ 1);
+      if (!__shfl_sync(0xffffffffu, e_ok, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(&stage_full[st], 2u * NH * copies * copy_bytes);
-        for (int c = 0; c < copies; ++c) {
-          const int tk = t0 + c * R;                        // first key of the copy
-          int32_t id = __ldg(row + tk / B);
-          if (id < 0 || id >= p.num_blocks) {
-            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;
-          }
-          const int z = id * B + tk % B;
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            tma_load_4d(kdst + h * Lay::kLineBytes + c * copy_bytes, &tm_k, &stage_full[st], 0, z,
-                        kvh, h, policy);
-            tma_load_4d(vdst + h * Lay::kLineBytes + c * copy_bytes, &tm_v, &stage_full[st], 0, z,
-                        kvh, h, policy);
-          }
-        }
         last_issued[st] = j;
       }
-      if (!ok) {
-        flag_error(p.err, PKV_DEVERR_TIMEOUT);
-        for (int st = 0; st < kStages; ++st)
-          if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
+      __syncwarp();
+      if (mine) {
+        if (id < 0 || id >= p.num_blocks) {
+          flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+          id = 0;
+        }
+        tma_load_4d(stages + st * Lay::kStageBytes + my_off, my_map, &stage_full[st], 0,
+                    id * B + tk % B, kvh, my_h, policy);
       }
+    }
+    if (!ok && lane == 0) {
+      flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      for (int st = 0; st < kStages; ++st)
+        if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue

@@ -310,6 +310,11 @@ TC_CASES = [
     ((3, 129, 4100), 128, 1, 128, 128, "f16", 0),
     ((33, 70, 130), 32, 1, 64, 64, "f16", 128),
     ((20, 1024, 517), 96, 3, 128, 16, "bf16", 512),
+    # 64-key tiles gathered from blocks of 8, 16 and 64 rows, two 128-byte
+    # lines per row; one group of 128 heads (a single copy of the query rows)
+    ((9, 200, 1031), 64, 1, 128, 8, "f16", 128),
+    ((17, 1500, 64), 128, 1, 128, 16, "bf16", 512),
+    ((50, 640, 3), 32, 1, 128, 64, "bf16", 256),
 ]
 
 
@@ -318,6 +323,15 @@ def test_large_groups_against_oracle(case):
     lens, H, Hkv, D, B, dt, pt = case
     batch = decode_batch("t", lens, H, Hkv, D, B, dt, seed=len(lens) + H + D)
     run_case(batch, pt=pt)
+
+
+def test_large_groups_many_sequences():
+    """More sequences than the compact work list takes: every (partition,
+    sequence, KV head) is numbered and the empty ones are skipped."""
+    rng = np.random.default_rng(5)
+    lens = tuple(int(x) for x in rng.integers(1, 200, 1100))
+    batch = decode_batch("t", lens, 32, 1, 64, 16, "f16", seed=6)
+    run_case(batch, pt=64)
 
 
 def test_large_groups_outlier_keys():
