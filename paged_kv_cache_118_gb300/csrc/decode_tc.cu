@@ -91,8 +91,12 @@ struct UnitInfo {
 //  query rows (A of S, K-major);
 //  each stage: K then V, D/64 line blocks of 64 key rows (B of S, K-major; B
 //  of P V, MN-major with the next 64 columns one line block on);
-//  merge area: (m, l, O) of the C - 1 copies past the first, one row of D + 3
-//  floats (an odd stride, so a warp writing its rows meets no bank conflict);
+//  merge area (four copies): (m, l, O) of the copies past the first, one row
+//  of D + 3 floats (an odd stride, so a warp writing its rows meets no bank
+//  conflict); two copies merge O through the unit's own query buffer instead,
+//  free once its last S is done (G rows of D floats; the 16-byte chunks of
+//  row h XOR-swizzled by h mod 8), and (m, l) through a small array per query
+//  buffer;
 //  then the barriers, the unit slots and the work list.
 // The ring takes as many stages (up to kMaxStages) as the rest leaves room for.
 template <int D, int C>
@@ -103,14 +107,16 @@ struct Layout {
   static constexpr int kTileBytes = NH * kLineBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kOffStages = 2 * kQBytes;
+  static constexpr bool kMergeInQ = C == 2;
   static constexpr int kMergeStride = D + 3;
-  static constexpr int kMergeBytes = (kRows - kRows / C) * kMergeStride * 4;
+  static constexpr int kMergeBytes = kMergeInQ ? 0 : (kRows - kRows / C) * kMergeStride * 4;
   // barriers: stage_full[S], stage_empty[S], unit_full[2], unit_empty[2],
   // q_full[2], q_free[2], s_full[2], p_full[2], pv_done[2], o_free[2], drain,
   // mrg_full, mrg_free
   static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 3) * 8 +
                                     2 * static_cast<int>(sizeof(UnitInfo)) + kMaxIds * 4 +
-                                    2 * (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 4 + 16;
+                                    2 * (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 4 +
+                                    2 * (kRows / 2) * 8 + 16;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kOffStages - kMergeBytes - kTailBytes - 16) / kStageBytes;
   static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
@@ -122,7 +128,8 @@ struct Layout {
   static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions
   static constexpr int kOffTail = kOffPref + (kCompactMaxSeqs + 4) * 4;   // last, partial ones
   static constexpr int kOffLens = kOffTail + (kCompactMaxSeqs + 4) * 4;
-  static constexpr int kOffTmem = kOffLens + kCompactMaxSeqs * 4;
+  static constexpr int kOffMl = kOffLens + kCompactMaxSeqs * 4;   // (m, l) of copy 1, per buffer
+  static constexpr int kOffTmem = kOffMl + 2 * (kRows / 2) * 8;
   static constexpr int kSmem = 1024 + kOffTmem + 16;
   static_assert(kStages >= 3 && kSmem <= kSmemLimit, "shared memory of one CTA");
 };
@@ -156,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mrg_full = drain + 1;
   uint64_t* mrg_free = mrg_full + 1;
   float* merge = reinterpret_cast<float*>(smem + Lay::kOffMerge);
+  float2* mrg_ml = reinterpret_cast<float2*>(smem + Lay::kOffMl);
   UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + Lay::kOffUnits);
   int32_t* ids = reinterpret_cast<int32_t*>(smem + Lay::kOffIds);
   int32_t* pref = reinterpret_cast<int32_t*>(smem + Lay::kOffPref);
@@ -179,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&unit_full[i], 1);
       mbar_init(&unit_empty[i], kRows + 1);          // the softmax threads and the MMA thread
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_free[i], 1);
+      // two copies: the first copy's rows free the buffer after the merge
+      mbar_init(&q_free[i], Lay::kMergeInQ ? kRows / C : 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kRows);
       mbar_init(&pv_done[i], 1);
@@ -458,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = issue_s(g, slot);
         for (int i = 0; ok && i < n_tiles; ++i) {
           if (i + 1 < n_tiles) ok = issue_s(g + i + 1, slot);
-          if (ok && i == last_s) tc_commit(&q_free[slot]);
+          if (!Lay::kMergeInQ && ok && i == last_s) tc_commit(&q_free[slot]);
           if (ok) ok = issue_pv(g + i, slot, i == 0);
         }
         g += n_tiles;
@@ -498,23 +507,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // this copy's KC scores of the tile
+        // this copy's KC scores of the tile (its columns only)
         float s[KC];
-        {
-          float all[kKeys];
+        if constexpr (KC == 16) {
+          uint32_t raw[16];
+          tmem_ld16(tl + b * kKeys + cp * KC, raw);
 #pragma unroll
-          for (int h = 0; h < kKeys / 32; ++h) {
+          for (int e = 0; e < 16; ++e) s[e] = __uint_as_float(raw[e]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < KC / 32; ++h) {
             uint32_t raw[32];
-            tmem_ld32(tl + b * kKeys + h * 32, raw);
+            tmem_ld32(tl + b * kKeys + cp * KC + h * 32, raw);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) all[h * 32 + e] = __uint_as_float(raw[e]);
-          }
-#pragma unroll
-          for (int e = 0; e < KC; ++e) {
-            float v = all[e];
-#pragma unroll
-            for (int cc = 1; cc < C; ++cc) v = cp == cc ? all[cc * KC + e] : v;
-            s[e] = v;
+            for (int e = 0; e < 32; ++e) s[h * 32 + e] = __uint_as_float(raw[e]);
           }
         }
         const int tile_valid = t_end - (t_begin + i * kKeys);   // keys of the tile that exist
@@ -620,6 +626,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
         }
         p.part_ml[prow] = make_float2(m, l);
+      } else if (Lay::kMergeInQ) {
+        // O of copy 1 through this unit's query buffer (its products are done)
+        // chunk j of each 8-chunk group sits at j ^ (hr mod 8): the 8 rows of a
+        // wavefront meet 8 different bank groups
+        float4* qm = reinterpret_cast<float4*>(qbufs + slot * Lay::kQBytes) + hr * (D / 4);
+        const int xr = hr & 7;
+        if (cp > 0) {
+#pragma unroll
+          for (int h = 0; h < D / 32; ++h) {
+            uint32_t raw[32];
+            tmem_ld32(to + h * 32, raw);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              qm[h * 8 + (j ^ xr)] =
+                  make_float4(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1]),
+                              __uint_as_float(raw[4 * j + 2]), __uint_as_float(raw[4 * j + 3]));
+          }
+          mrg_ml[slot * (kRows / 2) + hr] = make_float2(m, l);
+          fence_proxy_async_smem();                        // the buffer's next user is TMA
+          mbar_arrive(mrg_full);
+        } else {
+          if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1))) {
+            ok = false;
+            break;
+          }
+          const float2 o1 = mrg_ml[slot * (kRows / 2) + hr];
+          const float M = fmaxf(m, o1.x);
+          const float f0 = m == -INFINITY ? 0.f : ex2(m - M);
+          const float f1 = o1.x == -INFINITY ? 0.f : ex2(o1.x - M);
+#pragma unroll
+          for (int h = 0; h < D / 32; ++h) {
+            uint32_t raw[32];
+            tmem_ld32(to + h * 32, raw);
+            float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 v = qm[h * 8 + (j ^ xr)];
+              dst[j] = make_float4(fmaf(v.x, f1, __uint_as_float(raw[4 * j]) * f0),
+                                   fmaf(v.y, f1, __uint_as_float(raw[4 * j + 1]) * f0),
+                                   fmaf(v.z, f1, __uint_as_float(raw[4 * j + 2]) * f0),
+                                   fmaf(v.w, f1, __uint_as_float(raw[4 * j + 3]) * f0));
+            }
+          }
+          p.part_ml[prow] = make_float2(M, fmaf(o1.y, f1, l * f0));
+          fence_proxy_async_smem();
+          mbar_arrive(&q_free[slot]);                      // the producer may refill it
+        }
       } else if (cp > 0) {
         // hand (m, l, O) to the first copy of the head
         if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (k - 1) & 1))) {
