@@ -19,23 +19,25 @@
 //    partition first, then the partial last ones, which fill the end of the
 //    run (prefix sums per sequence); larger batches number them all and skip
 //    the empty ones. Per unit it reads the partition's block ids (one per lane),
-//    loads the G query rows by TMA into one of two query buffers and streams
+//    loads the G query rows by TMA into a staging buffer and streams
 //    the partition's 64-key K/V tiles into a ring of 3 to 6 stages (as many
 //    as shared memory holds beside the rest), one TMA copy per
 //    physical block and 128-byte line, issued by several lanes at once;
 //  * one thread of warp 1 owns the 512 tensor-memory columns (two 64-column
-//    score buffers, two D-column output buffers, one per unit in flight) and
-//    issues S = Q K^T (M = 128, N = 64, K = D) and O += P V (P from tensor
-//    memory), committing each to an mbarrier; a tile's S is issued before the
+//    score buffers, two D-column output buffers and two query buffers, one of
+//    each per unit in flight), copies each unit's query rows from the staging
+//    buffer into tensor memory (tcgen05.cp) and issues S = Q K^T (M = 128,
+//    N = 64, K = D; Q from tensor memory) and O += P V (P from tensor memory),
+//    committing each to an mbarrier; a tile's S is issued before the
 //    previous tile's P V, and the next unit's first S as soon as its queries
 //    are in;
 //  * warps 4-7 run the softmax, one thread per query row (its TMEM lane). The
 //    query rows hold 128 / G copies of the group's G heads, and copy c of a
 //    head takes keys [c 64 G / 128, (c + 1) 64 G / 128) of every tile (its P
 //    is 0 elsewhere), so every thread works on 64 G / 128 keys per tile. At
-//    the end of a unit the copies of a head are merged through shared memory
-//    and the partials written, while the next unit runs in the other output
-//    buffer.
+//    the end of a unit the copies of a head are merged through shared memory,
+//    half of D at a time, and the partials written, while the next unit runs
+//    in the other output buffer.
 // Every wait is bounded; bad block ids and lengths are reported and skipped.
 
 #include <cuda.h>
@@ -61,8 +63,10 @@ constexpr int kThreads = 256;          // warp 0: claims and copies; warp 1: MMA
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kMaxIds = 256;           // block ids of one unit, read ahead of its copies
 constexpr int kCompactMaxSeqs = 1024;  // batches up to this size get a compact work list
-// S0 [0, 64), S1 [64, 128), O0 [128, 128 + D), O1 [256, 256 + D)
+// S0 [0, 64), S1 [64, 128), O0 [128, 128 + D), O1 [256, 256 + D),
+// Q0 [384, 384 + D/2), Q1 [448, 448 + D/2) (16-bit pairs)
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kQCol = 384;
 constexpr float kRescaleThreshold = 8.0f;
 
 struct Params {
@@ -87,16 +91,13 @@ struct UnitInfo {
 
 // Shared memory from a 1024-byte aligned base; operands are 128-byte rows with
 // the 128-byte swizzle, 8-row groups 1024 bytes apart:
-//  Q, two buffers: D/64 column blocks of 128 rows, 128 / G copies of the G
-//  query rows (A of S, K-major);
+//  Q staging: D/64 column blocks of 128 rows, 128 / G copies of the G query
+//  rows (K-major; copied to tensor memory at the start of the unit);
 //  each stage: K then V, D/64 line blocks of 64 key rows (B of S, K-major; B
 //  of P V, MN-major with the next 64 columns one line block on);
-//  merge area (four copies): (m, l, O) of the copies past the first, one row
-//  of D + 3 floats (an odd stride, so a warp writing its rows meets no bank
-//  conflict); two copies merge O through the unit's own query buffer instead,
-//  free once its last S is done (G rows of D floats; the 16-byte chunks of
-//  row h XOR-swizzled by h mod 8), and (m, l) through a small array per query
-//  buffer;
+//  merge area (two or four copies): half of D of the copies past the first,
+//  one row of D/2 + 1 floats (an odd stride, so a warp writing its rows meets
+//  no bank conflict), then their (m, l);
 //  then the barriers, the unit slots and the work list.
 // The ring takes as many stages (up to kMaxStages) as the rest leaves room for.
 template <int D, int C>
@@ -106,17 +107,17 @@ struct Layout {
   static constexpr int kLineBytes = kKeys * 128;
   static constexpr int kTileBytes = NH * kLineBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kOffStages = 2 * kQBytes;
-  static constexpr bool kMergeInQ = C == 2;
-  static constexpr int kMergeStride = D + 3;
-  static constexpr int kMergeBytes = kMergeInQ ? 0 : (kRows - kRows / C) * kMergeStride * 4;
+  static constexpr int kOffStages = kQBytes;
+  static constexpr int kHalf = D / 2;
+  static constexpr int kMergeRows = kRows - kRows / C;
+  static constexpr int kMergeStride = kHalf + 1;
+  static constexpr int kMergeBytes = kMergeRows * (kMergeStride + 2) * 4;
   // barriers: stage_full[S], stage_empty[S], unit_full[2], unit_empty[2],
-  // q_full[2], q_free[2], s_full[2], p_full[2], pv_done[2], o_free[2], drain,
+  // q_full, q_free, s_full[2], p_full[2], pv_done[2], o_free[2], drain,
   // mrg_full, mrg_free
   static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 3) * 8 +
                                     2 * static_cast<int>(sizeof(UnitInfo)) + kMaxIds * 4 +
-                                    2 * (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 4 +
-                                    2 * (kRows / 2) * 8 + 16;
+                                    2 * (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 4 + 16;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kOffStages - kMergeBytes - kTailBytes - 16) / kStageBytes;
   static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
@@ -128,8 +129,7 @@ struct Layout {
   static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions
   static constexpr int kOffTail = kOffPref + (kCompactMaxSeqs + 4) * 4;   // last, partial ones
   static constexpr int kOffLens = kOffTail + (kCompactMaxSeqs + 4) * 4;
-  static constexpr int kOffMl = kOffLens + kCompactMaxSeqs * 4;   // (m, l) of copy 1, per buffer
-  static constexpr int kOffTmem = kOffMl + 2 * (kRows / 2) * 8;
+  static constexpr int kOffTmem = kOffLens + kCompactMaxSeqs * 4;
   static constexpr int kSmem = 1024 + kOffTmem + 16;
   static_assert(kStages >= 3 && kSmem <= kSmemLimit, "shared memory of one CTA");
 };
@@ -153,9 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* stage_empty = stage_full + kStages;
   uint64_t* unit_full = stage_empty + kStages;
   uint64_t* unit_empty = unit_full + 2;
-  uint64_t* q_full = unit_empty + 2;
-  uint64_t* q_free = q_full + 2;
-  uint64_t* s_full = q_free + 2;
+  uint64_t* q_full = unit_empty + 2;                     // the staging buffer
+  uint64_t* q_free = q_full + 1;
+  uint64_t* s_full = q_free + 1;
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_free = pv_done + 2;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mrg_full = drain + 1;
   uint64_t* mrg_free = mrg_full + 1;
   float* merge = reinterpret_cast<float*>(smem + Lay::kOffMerge);
-  float2* mrg_ml = reinterpret_cast<float2*>(smem + Lay::kOffMl);
+  float2* mrg_ml = reinterpret_cast<float2*>(merge + Lay::kMergeRows * Lay::kMergeStride);
   UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + Lay::kOffUnits);
   int32_t* ids = reinterpret_cast<int32_t*>(smem + Lay::kOffIds);
   int32_t* pref = reinterpret_cast<int32_t*>(smem + Lay::kOffPref);
@@ -186,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&unit_full[i], 1);
       mbar_init(&unit_empty[i], kRows + 1);          // the softmax threads and the MMA thread
-      mbar_init(&q_full[i], 1);
-      // two copies: the first copy's rows free the buffer after the merge
-      mbar_init(&q_free[i], Lay::kMergeInQ ? kRows / C : 1);
+
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kRows);
       mbar_init(&pv_done[i], 1);
       mbar_init(&o_free[i], kRows);
     }
+    mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     mbar_init(drain, 1);
     mbar_init(mrg_full, C > 1 ? kRows - kRows / C : 1);  // the copies past the first
     mbar_init(mrg_free, kRows / C);                      // the first copies
@@ -331,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       const int slot = k & 1;
       bool w_ok = true;
-      if (lane == 0 && k >= 2)
-        w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1) &&
-               mbar_wait(&q_free[slot], ((k >> 1) & 1) ^ 1);
+      if (lane == 0 && k >= 2) w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1);
+      // the staging buffer, once the previous unit's rows are in tensor memory
+      if (lane == 0 && k >= 1 && info.seq >= 0) w_ok = w_ok && mbar_wait(q_free, (k - 1) & 1);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
         ok = false;
         break;
@@ -342,14 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         units[slot] = info;
         if (info.seq >= 0) {
           // the group's query rows, once per copy
-          mbar_arrive_expect_tx(&q_full[slot], static_cast<uint32_t>(NH) * kRows * 128);
+          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(NH) * kRows * 128);
           const int row0 = info.seq * p.num_heads + info.kvh * G;
 #pragma unroll
           for (int c = 0; c < C; ++c)
 #pragma unroll
             for (int h = 0; h < NH; ++h)
-              tma_load_3d(qbufs + slot * Lay::kQBytes + h * kRows * 128 + c * G * 128, &tm_q,
-                          &q_full[slot], 0, h, row0, policy);
+              tma_load_3d(qbufs + h * kRows * 128 + c * G * 128, &tm_q, q_full, 0, h, row0,
+                          policy);
         }
         mbar_arrive(&unit_full[slot]);
       }
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = mma_idesc_f16(kBF16, kRows, kKeys, false);
       constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
-      const uint64_t dq0 = smem_desc_sw128(qbufs, 16, 1024);
+      const uint64_t dq0 = smem_desc_sw128(qbufs, 16, 1024);   // the staging buffer
       const uint64_t dk0 = smem_desc_sw128(stages, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(stages + Lay::kTileBytes, Lay::kLineBytes, 1024);
       int g = 0;                                           // tiles consumed
@@ -409,13 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the score buffer's P was read by the P V product two tiles back
         if (gi >= 2 && !mbar_wait(&pv_done[b], ((gi - 2) >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t dq = dq0 + ((qb * Lay::kQBytes) >> 4);
+        const uint32_t qt = tbase + kQCol + qb * (D / 2);
         const uint64_t dk = dk0 + ((st * Lay::kStageBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t qo = ((ks >> 2) * kRows * 128 + (ks & 3) * 32) >> 4;
           const uint32_t ko = ((ks >> 2) * Lay::kLineBytes + (ks & 3) * 32) >> 4;
-          tc_mma_f16(tbase + b * kKeys, dq + qo, dk + ko, kIdescS, ks > 0 ? 1u : 0u);
+          tc_mma_f16_ts(tbase + b * kKeys, qt + ks * 8, dk + ko, kIdescS, ks > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[b]);
         return true;
@@ -452,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (info.seq < 0) break;
         const int t_begin = info.part * PT;
         const int n_tiles = (min(info.len, t_begin + PT) - t_begin + kKeys - 1) / kKeys;
-        if (!mbar_wait(&q_full[slot], (k >> 1) & 1)) {
+        if (!mbar_wait(q_full, k & 1)) {
           ok = false;
           break;
         }
@@ -461,13 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // the unit's last S is issued in iteration max(n_tiles - 2, 0); then
-        // the query buffer may be refilled once those products are done
-        const int last_s = n_tiles >= 2 ? n_tiles - 2 : 0;
+        tc_fence_after();
+        // the query rows into this unit's query columns, one 16-element k-step
+        // (128 rows x 32 bytes) per copy, in order with the products around
+        // them (the unit two back read these columns before); the staging
+        // buffer is free once the copies are done
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_cp_128x256b(tbase + kQCol + slot * (D / 2) + ks * 8,
+                         dq0 + (((ks >> 2) * kRows * 128 + (ks & 3) * 32) >> 4));
+        tc_commit(q_free);
         ok = issue_s(g, slot);
         for (int i = 0; ok && i < n_tiles; ++i) {
           if (i + 1 < n_tiles) ok = issue_s(g + i + 1, slot);
-          if (!Lay::kMergeInQ && ok && i == last_s) tc_commit(&q_free[slot]);
           if (ok) ok = issue_pv(g + i, slot, i == 0);
         }
         g += n_tiles;
@@ -626,106 +631,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
         }
         p.part_ml[prow] = make_float2(m, l);
-      } else if (Lay::kMergeInQ) {
-        // O of copy 1 through this unit's query buffer (its products are done)
-        // chunk j of each 8-chunk group sits at j ^ (hr mod 8): the 8 rows of a
-        // wavefront meet 8 different bank groups
-        float4* qm = reinterpret_cast<float4*>(qbufs + slot * Lay::kQBytes) + hr * (D / 4);
-        const int xr = hr & 7;
-        if (cp > 0) {
-#pragma unroll
-          for (int h = 0; h < D / 32; ++h) {
-            uint32_t raw[32];
-            tmem_ld32(to + h * 32, raw);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              qm[h * 8 + (j ^ xr)] =
-                  make_float4(__uint_as_float(raw[4 * j]), __uint_as_float(raw[4 * j + 1]),
-                              __uint_as_float(raw[4 * j + 2]), __uint_as_float(raw[4 * j + 3]));
-          }
-          mrg_ml[slot * (kRows / 2) + hr] = make_float2(m, l);
-          fence_proxy_async_smem();                        // the buffer's next user is TMA
-          mbar_arrive(mrg_full);
-        } else {
-          if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1))) {
-            ok = false;
-            break;
-          }
-          const float2 o1 = mrg_ml[slot * (kRows / 2) + hr];
-          const float M = fmaxf(m, o1.x);
-          const float f0 = m == -INFINITY ? 0.f : ex2(m - M);
-          const float f1 = o1.x == -INFINITY ? 0.f : ex2(o1.x - M);
-#pragma unroll
-          for (int h = 0; h < D / 32; ++h) {
-            uint32_t raw[32];
-            tmem_ld32(to + h * 32, raw);
-            float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 v = qm[h * 8 + (j ^ xr)];
-              dst[j] = make_float4(fmaf(v.x, f1, __uint_as_float(raw[4 * j]) * f0),
-                                   fmaf(v.y, f1, __uint_as_float(raw[4 * j + 1]) * f0),
-                                   fmaf(v.z, f1, __uint_as_float(raw[4 * j + 2]) * f0),
-                                   fmaf(v.w, f1, __uint_as_float(raw[4 * j + 3]) * f0));
-            }
-          }
-          p.part_ml[prow] = make_float2(M, fmaf(o1.y, f1, l * f0));
-          fence_proxy_async_smem();
-          mbar_arrive(&q_free[slot]);                      // the producer may refill it
-        }
-      } else if (cp > 0) {
-        // hand (m, l, O) to the first copy of the head
-        if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (k - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        float* row = merge + ((cp - 1) * G + hr) * Lay::kMergeStride;
-#pragma unroll
-        for (int h = 0; h < D / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(to + h * 32, raw);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) row[h * 32 + e] = __uint_as_float(raw[e]);
-        }
-        row[D] = m;
-        row[D + 1] = l;
-        mbar_arrive(mrg_full);
       } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1))) {
-          ok = false;
-          break;
-        }
-        float f[C], M = m;
+        // the copies' output rows meet in shared memory, half of D per round
+        // (rounds 2k and 2k + 1 of this CTA's k-th unit)
+        float f[C], M = m, lt = 0.f;
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          const int round = 2 * k + hf;
+          if (cp > 0) {
+            if (round >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (round - 1) & 1))) {
+              ok = false;
+              break;
+            }
+            float* row = merge + ((cp - 1) * G + hr) * Lay::kMergeStride;
 #pragma unroll
-        for (int cc = 1; cc < C; ++cc) M = fmaxf(M, merge[((cc - 1) * G + hr) * Lay::kMergeStride + D]);
-        f[0] = m == -INFINITY ? 0.f : ex2(m - M);
-        float lt = l * f[0];
+            for (int h = 0; h < Lay::kHalf / 32; ++h) {
+              uint32_t raw[32];
+              tmem_ld32(to + hf * Lay::kHalf + h * 32, raw);
 #pragma unroll
-        for (int cc = 1; cc < C; ++cc) {
-          const float* row = merge + ((cc - 1) * G + hr) * Lay::kMergeStride;
-          f[cc] = row[D] == -INFINITY ? 0.f : ex2(row[D] - M);
-          lt = fmaf(row[D + 1], f[cc], lt);
-        }
+              for (int e = 0; e < 32; ++e) row[h * 32 + e] = __uint_as_float(raw[e]);
+            }
+            if (hf == 0) mrg_ml[(cp - 1) * G + hr] = make_float2(m, l);
+            mbar_arrive(mrg_full);
+          } else {
+            if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, round & 1))) {
+              ok = false;
+              break;
+            }
+            if (hf == 0) {
 #pragma unroll
-        for (int h = 0; h < D / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(to + h * 32, raw);
-          float o[32];
+              for (int cc = 1; cc < C; ++cc) M = fmaxf(M, mrg_ml[(cc - 1) * G + hr].x);
+              f[0] = m == -INFINITY ? 0.f : ex2(m - M);
+              lt = l * f[0];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(raw[e]) * f[0];
+              for (int cc = 1; cc < C; ++cc) {
+                const float2 ml = mrg_ml[(cc - 1) * G + hr];
+                f[cc] = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+                lt = fmaf(ml.y, f[cc], lt);
+              }
+              p.part_ml[prow] = make_float2(M, lt);
+            }
 #pragma unroll
-          for (int cc = 1; cc < C; ++cc) {
-            const float* row = merge + ((cc - 1) * G + hr) * Lay::kMergeStride + h * 32;
+            for (int h = 0; h < Lay::kHalf / 32; ++h) {
+              uint32_t raw[32];
+              tmem_ld32(to + hf * Lay::kHalf + h * 32, raw);
+              float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + hf * Lay::kHalf + h * 32);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = fmaf(row[e], f[cc], o[e]);
+              for (int j = 0; j < 8; ++j) {
+                float o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  o[i] = __uint_as_float(raw[4 * j + i]) * f[0];
+#pragma unroll
+                  for (int cc = 1; cc < C; ++cc)
+                    o[i] = fmaf(merge[((cc - 1) * G + hr) * Lay::kMergeStride + h * 32 + 4 * j + i],
+                                f[cc], o[i]);
+                }
+                dst[j] = make_float4(o[0], o[1], o[2], o[3]);
+              }
+            }
+            mbar_arrive(mrg_free);
           }
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
-        p.part_ml[prow] = make_float2(M, lt);
-        mbar_arrive(mrg_free);
+        if (!ok) break;
       }
       tc_fence_before();
       mbar_arrive(&o_free[slot]);
