@@ -109,7 +109,9 @@ struct Layout {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kOffStages = kQBytes;
   static constexpr int kHalf = D / 2;
-  static constexpr int kMergeRows = kRows - kRows / C;
+  // two copies exchange halves (all 128 rows write one); four pass the
+  // later copies' rows to the first
+  static constexpr int kMergeRows = C == 2 ? kRows : kRows - kRows / C;
   static constexpr int kMergeStride = kHalf + 1;
   static constexpr int kMergeBytes = kMergeRows * (kMergeStride + 2) * 4;
   // barriers: stage_full[S], stage_empty[S], unit_full[2], unit_empty[2],
@@ -195,8 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
     mbar_init(drain, 1);
-    mbar_init(mrg_full, C > 1 ? kRows - kRows / C : 1);  // the copies past the first
-    mbar_init(mrg_free, kRows / C);                      // the first copies
+    // two copies: every row; four: the copies past the first, then the first
+    mbar_init(mrg_full, C == 2 ? kRows : (C > 1 ? kRows - kRows / C : 1));
+    mbar_init(mrg_free, C == 2 ? kRows : kRows / C);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -631,6 +634,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
         }
         p.part_ml[prow] = make_float2(m, l);
+      } else if constexpr (C == 2) {
+        // Copy c merges and writes the half [c D/2, (c + 1) D/2) of the head's
+        // row; it hands its other half, with its (m, l), to the other copy.
+        if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (k - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        float* out_row = merge + (cp * G + hr) * Lay::kMergeStride;
+#pragma unroll
+        for (int h = 0; h < Lay::kHalf / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(to + (1 - cp) * Lay::kHalf + h * 32, raw);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) out_row[h * 32 + e] = __uint_as_float(raw[e]);
+        }
+        mrg_ml[cp * G + hr] = make_float2(m, l);
+        mbar_arrive(mrg_full);
+        if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1))) {
+          ok = false;
+          break;
+        }
+        const float* in_row = merge + ((1 - cp) * G + hr) * Lay::kMergeStride;
+        const float2 mo = mrg_ml[(1 - cp) * G + hr];
+        const float M = fmaxf(m, mo.x);
+        const float fm = m == -INFINITY ? 0.f : ex2(m - M);
+        const float fo = mo.x == -INFINITY ? 0.f : ex2(mo.x - M);
+        if (cp == 0) p.part_ml[prow] = make_float2(M, fmaf(mo.y, fo, l * fm));
+#pragma unroll
+        for (int h = 0; h < Lay::kHalf / 32; ++h) {
+          uint32_t raw[32];
+          tmem_ld32(to + cp * Lay::kHalf + h * 32, raw);
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + cp * Lay::kHalf + h * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o[i] = fmaf(in_row[h * 32 + 4 * j + i], fo, __uint_as_float(raw[4 * j + i]) * fm);
+            dst[j] = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        mbar_arrive(mrg_free);
       } else {
         // the copies' output rows meet in shared memory, half of D per round
         // (rounds 2k and 2k + 1 of this CTA's k-th unit)
