@@ -20,7 +20,7 @@
 //    run (prefix sums per sequence); larger batches number them all and skip
 //    the empty ones. Per unit it reads the partition's block ids (one per lane),
 //    loads the G query rows by TMA into a staging buffer and streams
-//    the partition's 64-key K/V tiles into a ring of 3 to 6 stages (as many
+//    the partition's 64-key K/V tiles into a ring of 4 to 6 stages (as many
 //    as shared memory holds beside the rest), one TMA copy per
 //    physical block and 128-byte line, issued by several lanes at once;
 //  * one thread of warp 1 owns the 512 tensor-memory columns (two 64-column
@@ -35,9 +35,10 @@
 //    query rows hold 128 / G copies of the group's G heads, and copy c of a
 //    head takes keys [c 64 G / 128, (c + 1) 64 G / 128) of every tile (its P
 //    is 0 elsewhere), so every thread works on 64 G / 128 keys per tile. At
-//    the end of a unit the copies of a head are merged through shared memory,
-//    half of D at a time, and the partials written, while the next unit runs
-//    in the other output buffer.
+//    the end of a unit the copies of a head are merged through shared memory
+//    (two copies exchange halves of D and each writes one; with four, copy 0
+//    takes the others' rows half of D at a time) and the partials written,
+//    while the next unit runs in the other output buffer.
 // Every wait is bounded; bad block ids and lengths are reported and skipped.
 
 #include <cuda.h>
@@ -55,7 +56,7 @@
 namespace pkv {
 namespace tcdec {
 
-constexpr int kRows = 128;             // product rows: query heads of the KV head, padded
+constexpr int kRows = 128;             // product rows: 128 / G copies of the group's query heads
 constexpr int kKeys = 64;              // keys per tile
 constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;     // shared memory one CTA may ask for
@@ -95,9 +96,10 @@ struct UnitInfo {
 //  rows (K-major; copied to tensor memory at the start of the unit);
 //  each stage: K then V, D/64 line blocks of 64 key rows (B of S, K-major; B
 //  of P V, MN-major with the next 64 columns one line block on);
-//  merge area (two or four copies): half of D of the copies past the first,
-//  one row of D/2 + 1 floats (an odd stride, so a warp writing its rows meets
-//  no bank conflict), then their (m, l);
+//  merge area (two or four copies): rows of D/2 + 1 floats (an odd stride, so
+//  a warp writing its rows meets no bank conflict), then the rows' (m, l):
+//  with two copies every row passes the half of D its partner writes; with
+//  four the rows of copies 1-3 pass half of D per round to copy 0;
 //  then the barriers, the unit slots and the work list.
 // The ring takes as many stages (up to kMaxStages) as the rest leaves room for.
 template <int D, int C>
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* qbufs = smem;
+  uint8_t* qstage = smem;
   uint8_t* stages = smem + Lay::kOffStages;
   uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
   uint64_t* stage_empty = stage_full + kStages;
@@ -188,7 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&unit_full[i], 1);
       mbar_init(&unit_empty[i], kRows + 1);          // the softmax threads and the MMA thread
-
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kRows);
       mbar_init(&pv_done[i], 1);
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < C; ++c)
 #pragma unroll
             for (int h = 0; h < NH; ++h)
-              tma_load_3d(qbufs + h * kRows * 128 + c * G * 128, &tm_q, q_full, 0, h, row0,
+              tma_load_3d(qstage + h * kRows * 128 + c * G * 128, &tm_q, q_full, 0, h, row0,
                           policy);
         }
         mbar_arrive(&unit_full[slot]);
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = mma_idesc_f16(kBF16, kRows, kKeys, false);
       constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
-      const uint64_t dq0 = smem_desc_sw128(qbufs, 16, 1024);   // the staging buffer
+      const uint64_t dq0 = smem_desc_sw128(qstage, 16, 1024);   // the staging buffer
       const uint64_t dk0 = smem_desc_sw128(stages, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(stages + Lay::kTileBytes, Lay::kLineBytes, 1024);
       int g = 0;                                           // tiles consumed
