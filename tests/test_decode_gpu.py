@@ -315,6 +315,12 @@ TC_CASES = [
     ((9, 200, 1031), 64, 1, 128, 8, "f16", 128),
     ((17, 1500, 64), 128, 1, 128, 16, "bf16", 512),
     ((50, 640, 3), 32, 1, 128, 64, "bf16", 256),
+    # a long context: the default 1024-token partitions, 40 partials per row
+    # (the four-warp reduce); one copy of 128 heads at d = 64; blocks of 256
+    # rows (tiles inside one block)
+    ((40000, 5, 33000), 64, 1, 128, 16, "bf16", 0),
+    ((7, 777), 128, 1, 64, 32, "bf16", 256),
+    ((1, 2, 3, 4, 100, 513), 64, 1, 128, 256, "f16", 512),
 ]
 
 
