@@ -23,6 +23,11 @@ CASES = [
     ((1500, 33), (129, 5), 16, 2, 128, 32, "bf16"),
     ((640,), (640,), 64, 1, 64, 128, "bf16"),
     ((77, 400, 9), (3, 65, 9), 40, 40, 128, 64, "f16"),
+    # 128 query heads per KV head (one token per query tile), 256-row blocks,
+    # and a whole 1000-token prompt over 8-row blocks at d = 128
+    ((300, 50), (300, 7), 128, 1, 64, 16, "bf16"),
+    ((600, 70), (600, 70), 8, 2, 128, 256, "f16"),
+    ((1000,), (1000,), 8, 8, 128, 8, "bf16"),
 ]
 
 
