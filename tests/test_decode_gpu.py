@@ -199,8 +199,12 @@ def test_copy_blocks_bitwise(n_pairs):
     assert np.array_equal(vc.view(torch.int16).cpu().numpy().view(np.uint16), vc_h)
 
 
-def test_decode_flags_bad_block_ids_and_lengths():
-    batch = decode_batch("t", (40, 70, 20), 4, 4, 64, 16, "f16", seed=21)
+@pytest.mark.parametrize("heads", [(4, 4), (64, 1)], ids=["mha", "tcgen05"])
+def test_decode_flags_bad_block_ids_and_lengths(heads):
+    """Both the warp-level path and the tensor-memory path (64 query heads on
+    one KV head) report a bad block id and an out-of-range length, and give
+    the bad sequence a zero row."""
+    batch = decode_batch("t", (40, 70, 20), heads[0], heads[1], 64, 16, "f16", seed=21)
     n = 20
     cache, tables, ctx = gpu_decode_state(batch, n, free_order(n, 0))
     q = dev(batch.q, "f16")
