@@ -1,5 +1,6 @@
-"""bench.py's multi-rank host logic on two gloo ranks (CPU): the job time is
-the slowest rank's, and the whole-job GB/s counts every rank's bytes."""
+"""bench.py host logic on the CPU: on two gloo ranks the job time is the
+slowest rank's and the whole-job GB/s counts every rank's bytes; the traffic
+figure comes from an ncu summary only while its kernel source is unchanged."""
 
 import os
 import socket
@@ -44,3 +45,24 @@ def test_single_process_needs_no_group():
     import bench
     assert bench.max_over_ranks(2.5) == 2.5
     assert bench.whole_job_gbps(6_700_500_000, 1, 1000.0) == pytest.approx(6.7005)
+
+
+def test_profile_traffic_follows_the_source_the_summary_names(tmp_path, monkeypatch):
+    """A committed ncu summary feeds the bench line's traffic only while the
+    kernel source it names still has the recorded sha256; the captured bytes
+    are scaled by the ratio of algorithmic bytes."""
+    import hashlib
+
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "decode_partition_x.md").write_text(
+        f"source_sha256: {sha}   (k.cu at capture time)\n"
+        "captured_traffic_bytes: 1010\ncaptured_algorithmic_bytes: 1000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("x", 2000.0) == 2020
+    assert bench.profile_traffic("missing", 2000.0) is None
+    src.write_text("kernel v2\n")                        # the kernel changed since the capture
+    assert bench.profile_traffic("x", 2000.0) is None
