@@ -312,7 +312,7 @@ def run_ours(args, rank, world, local_rank):
     ctx_log = []
     ev_pairs = []
 
-    def step(timed_kernels: bool):
+    def step(timed_kernels: bool, before=None, after=None):
         new_slots, cow = bm.append_slots(seq_ids)                       # host block manager
         tab, lens = bm.fill_tables(seq_ids, width)
         d_new.copy_(torch.from_numpy(new_slots).pin_memory(), non_blocking=True)
@@ -320,6 +320,8 @@ def run_ours(args, rank, world, local_rank):
         d_lens.copy_(torch.from_numpy(lens).pin_memory(), non_blocking=True)
         ctx_log.append(lens.astype(np.int64))
         for l in range(layers):
+            if before is not None:
+                before(l)
             if len(cow):
                 pk.pkv_copy_blocks(kc[l], vc[l], cow)
                 launches[0] += -(-len(cow) // 1024)
@@ -333,6 +335,8 @@ def run_ours(args, rank, world, local_rank):
             if timed_kernels:
                 b.record(stream)
                 ev_pairs.append((a, b))
+            if after is not None:
+                after(l)
             launches[0] += 3
 
     dist = world > 1
@@ -377,21 +381,61 @@ def run_ours(args, rank, world, local_rank):
     tokens_s = S * args.steps * world / (ms * 1e-3)
     assert err.item() == 0, f"device error flag {err.item()}"
 
-    # ---- end-to-end: host inputs in, host outputs back, inside the timed region
+    # ---- end-to-end: host inputs in, host outputs back, inside the timed region.
+    # As a serving pipeline would: the layers' q and new K/V go up on a copy
+    # stream and their outputs come down on another, a group of layers at a
+    # time (four groups per step), so a group waits only for its own inputs;
+    # events keep a buffer from being refilled (or an output overwritten)
+    # before the previous step has used (or read back) it.
     e2e = None
     if not args.no_e2e:
         for _ in range(args.warmup):
             step(False)
         ctx_log.clear()
+        up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ng = min(4, layers)
+        bounds = [layers * g // ng for g in range(ng + 1)]          # group g: layers [b_g, b_g+1)
+        group_of = [g for g in range(ng) for _ in range(bounds[g], bounds[g + 1])]
+        ev_in = [torch.cuda.Event() for _ in range(ng)]
+        ev_used = [torch.cuda.Event() for _ in range(ng)]
+        ev_read = [torch.cuda.Event() for _ in range(ng)]
+        later = [False]
+
+        def before(l):
+            g = group_of[l]
+            if l == bounds[g]:
+                stream.wait_event(ev_in[g])
+                if later[0]:
+                    stream.wait_event(ev_read[g])
+
+        def after(l):
+            g = group_of[l]
+            if l == bounds[g + 1] - 1:
+                a, b = bounds[g], bounds[g + 1]
+                ev_used[g].record(stream)
+                down.wait_event(ev_used[g])
+                with torch.cuda.stream(down):
+                    out_host[a:b].copy_(out[a:b], non_blocking=True)
+                ev_read[g].record(down)
+
         barrier()
         w0 = time.perf_counter()
         t0.record(stream)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
         for _ in range(args.steps):
-            q.copy_(host["q"], non_blocking=True)
-            knew.copy_(host["k"], non_blocking=True)
-            vnew.copy_(host["v"], non_blocking=True)
-            step(False)
-            out_host.copy_(out, non_blocking=True)
+            with torch.cuda.stream(up):
+                for g in range(ng):
+                    a, b = bounds[g], bounds[g + 1]
+                    if later[0]:
+                        up.wait_event(ev_used[g])
+                    q[a:b].copy_(host["q"][a:b], non_blocking=True)
+                    knew[a:b].copy_(host["k"][a:b], non_blocking=True)
+                    vnew[a:b].copy_(host["v"][a:b], non_blocking=True)
+                    ev_in[g].record(up)
+            step(False, before, after)
+            later[0] = True
+        stream.wait_stream(down)
         t1.record(stream)
         barrier()
         ms_e2e = max_over_ranks(max(t0.elapsed_time(t1), (time.perf_counter() - w0) * 1e3), dev)
