@@ -12,9 +12,20 @@ that layer's own pool. Every layer's pool is a separate 1.3 GB region, so each
 step reads ~42 GB of cache — far more than L2 (no flush needed).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--block-size B] [--partition-tokens P]
 
 Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
 on the host cores on a bounded sample of the same workload.
+
+The default run (1 GPU) adds a ``per_config`` object: every workload of the
+set measured the same way, each with fewer layers where its pools are large
+(every step still reads far more than L2): the tiny batch (latency only), the
+LLaMA-13B-shaped batch at each block size 8..128, the GQA shared-prefix batch,
+the long-context batch at 512- and 1024-token partitions, and the 64-heads-per-
+KV-head batch. Their key and value data are drawn on the device (torch's
+generator, N(0, 1) rounded to the storage type, 1% of key vectors x8 for the
+long-context batch) with the workloads' own lengths, shapes and block
+placement: drawing several GB on the host would take minutes.
 """
 
 from __future__ import annotations
@@ -45,6 +56,15 @@ CONFIGS = {
     "longctx": dict(layers=8),
     "mqa": dict(layers=16),
 }
+# The default run's per-config measurements: (key, config, block size,
+# partition tokens, layers). Layers are chosen so that a step reads several
+# GB (far more than L2) while the pools stay well inside HBM.
+PER_CONFIG = [("llama13b_b%d" % b, "llama13b", b, 0, 4) for b in (8, 16, 32, 64, 128)] + [
+    ("gqa_prefix", "gqa_prefix", 16, 0, 16),
+    ("longctx_p512", "longctx", 16, 512, 8),
+    ("longctx_p1024", "longctx", 16, 1024, 8),
+    ("mqa", "mqa", 16, 0, 16),
+]
 
 
 # ---------------------------------------------------------------- helpers
@@ -153,31 +173,48 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
-def workload_shape(name, seed):
-    """Lengths and dimensions of a workload, without drawing its token data."""
+def workload_shape(name, seed, block_size=0):
+    """Lengths and dimensions of a workload, without drawing its token data
+    (block_size 0: the workload's own, 16)."""
     import workloads as wl
+    B = block_size or 16
     if name == "opt13b":
-        return wl.opt13b_lengths(64, seed), 40, 40, 128, 16, "f16"
+        return wl.opt13b_lengths(64, seed), 40, 40, 128, B, "f16"
     if name == "llama13b":
-        return wl.llama13b_lengths(128, seed), 40, 40, 128, 16, "f16"
+        return wl.llama13b_lengths(128, seed), 40, 40, 128, B, "f16"
     if name == "longctx":
-        return np.array([n * 1024 for n in wl.LONGCTX_LENS_K], np.int32), 32, 8, 128, 16, "bf16"
+        return np.array([n * 1024 for n in wl.LONGCTX_LENS_K], np.int32), 32, 8, 128, B, "bf16"
     if name == "mqa":
-        return wl.llama13b_lengths(128, seed), 64, 1, 128, 16, "bf16"
+        return wl.llama13b_lengths(128, seed), 64, 1, 128, B, "bf16"
     if name == "gqa_prefix":
-        pb = wl.gqa_prefix(seed)
-        lens = np.array([int(pb.prefix_lens[s // 4]) + int(pb.tail_lens[s]) for s in range(256)],
-                        np.int32)
-        return lens, 32, 8, 128, 16, "bf16"
+        pl, tl = wl.gqa_prefix_lengths(seed)
+        lens = np.array([int(pl[s // 4]) + int(tl[s]) for s in range(256)], np.int32)
+        return lens, 32, 8, 128, B, "bf16"
     raise ValueError(name)
 
 
-def make_workload(name, seed):
+def device_tokens(n, Hkv, D, tdt, gen, dev, outlier_frac=0.0, chunk=1 << 16):
+    """n token rows [n, Hkv, D] of N(0, 1) values rounded to tdt, drawn on the
+    device; with outlier_frac > 0 a (token, head) vector is x8 with that
+    probability (the long-context workload's keys)."""
+    import torch
+    out = torch.empty((n, Hkv, D), dtype=tdt, device=dev)
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        x = torch.randn((b - a, Hkv, D), generator=gen, device=dev, dtype=torch.float32)
+        if outlier_frac > 0.0:
+            hit = torch.rand((b - a, Hkv, 1), generator=gen, device=dev) < outlier_frac
+            x = torch.where(hit, x * 8.0, x)
+        out[a:b] = x.to(tdt)
+    return out
+
+
+def make_workload(name, seed, block_size=16):
     import workloads as wl
     if name == "opt13b":
         return wl.opt13b(seed)
     if name == "llama13b":
-        return wl.llama13b(seed)
+        return wl.llama13b(seed, block_size=block_size)
     if name == "longctx":
         return wl.longctx(seed)
     if name == "mqa":
@@ -201,36 +238,50 @@ def setup_pools(args, rank, dev, layers, total_steps):
     import workloads as wl
 
     seed = args.seed + rank
+    devv = getattr(args, "device_values", False)
+    gen = None
+    if devv:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
     if args.config == "gqa_prefix":
-        pb = wl.gqa_prefix(seed)
-        S, H, Hkv, D, B = pb.num_seqs, pb.num_heads, pb.num_kv_heads, pb.head_size, pb.block_size
+        pl, tl = wl.gqa_prefix_lengths(seed)
+        beams, groups = 4, len(pl)
+        S, H, Hkv, D, B = groups * beams, 32, 8, 128, 16
         tdt = torch.bfloat16
-        L0 = np.array([int(pb.prefix_lens[s // pb.beams]) + int(pb.tail_lens[s]) + 1
-                       for s in range(S)], np.int64)
-        unique = int(np.sum(-(-pb.prefix_lens // B))) + int(np.sum(-(-(pb.tail_lens + B + total_steps) // B)))
+        p_off = np.concatenate([[0], np.cumsum(pl)]).astype(np.int64)
+        t_off = np.concatenate([[0], np.cumsum(tl)]).astype(np.int64)
+        L0 = np.array([int(pl[s // beams]) + int(tl[s]) + 1 for s in range(S)], np.int64)
+        unique = int(np.sum(-(-pl // B))) + int(np.sum(-(-(tl + B + total_steps) // B)))
         num_blocks = int(math.ceil(1.2 * unique))
         bm = pk.BlockManager(num_blocks, B, wl.free_order(num_blocks, seed))
         pre = []
-        for g in range(pb.num_groups):
-            bm.allocate(g * pb.beams, int(pb.prefix_lens[g]))
-            pre.append(bm.slots(g * pb.beams))
-            for j in range(1, pb.beams):
-                bm.fork(g * pb.beams, g * pb.beams + j)
-        tail_slots = np.full(int(pb.tail_offsets[-1]), -1, np.int64)
+        for g in range(groups):
+            bm.allocate(g * beams, int(pl[g]))
+            pre.append(bm.slots(g * beams))
+            for j in range(1, beams):
+                bm.fork(g * beams, g * beams + j)
+        tail_slots = np.full(int(t_off[-1]), -1, np.int64)
         cows = []
-        for i in range(int(pb.tail_lens.max())):
-            seqs = np.nonzero(pb.tail_lens > i)[0]
+        for i in range(int(tl.max())):
+            seqs = np.nonzero(tl > i)[0]
             sl, cow = bm.append_slots(seqs)
-            tail_slots[pb.tail_offsets[seqs] + i] = sl
+            tail_slots[t_off[seqs] + i] = sl
             cows.append(cow)
         cows = np.concatenate(cows)
         kc = torch.empty((layers, num_blocks, B, Hkv, D), dtype=tdt, device=dev)
         vc = torch.empty_like(kc)
-        parts = [(np.concatenate(pre), pb.prefix_k, pb.prefix_v), (tail_slots, pb.tail_k, pb.tail_v)]
-        for i, (sl, kk, vv) in enumerate(parts):
-            d_sl = torch.from_numpy(sl).to(dev)
-            kt = torch.from_numpy(kk.view(np.int16)).view(tdt).to(dev)
-            vt = torch.from_numpy(vv.view(np.int16)).view(tdt).to(dev)
+        if devv:
+            src = [(np.concatenate(pre), lambda: device_tokens(int(p_off[-1]), Hkv, D, tdt, gen, dev)),
+                   (tail_slots, lambda: device_tokens(int(t_off[-1]), Hkv, D, tdt, gen, dev))]
+        else:
+            pb = wl.gqa_prefix(seed)
+            up = lambda a: torch.from_numpy(a.view(np.int16)).view(tdt).to(dev)
+            src = [(np.concatenate(pre), lambda: up(pb.prefix_k), lambda: up(pb.prefix_v)),
+                   (tail_slots, lambda: up(pb.tail_k), lambda: up(pb.tail_v))]
+        for i, part in enumerate(src):
+            d_sl = torch.from_numpy(part[0]).to(dev)
+            kt = part[1]()
+            vt = part[1]() if devv else part[2]()
             for l in range(layers):
                 if i == 1:
                     pk.pkv_copy_blocks(kc[l], vc[l], cows)
@@ -239,35 +290,42 @@ def setup_pools(args, rank, dev, layers, total_steps):
         # tokens of shared (full) blocks are read by several beams but stored once
         refs = np.array([bm.refcount(b) for b in range(num_blocks)])
         shared_extra = int(np.sum(np.maximum(refs - 1, 0))) * B
-        info = dict(dtype="bf16", scale=float(pb.scale), cow_pairs=int(len(cows)),
-                    groups=pb.num_groups, beams=pb.beams)
+        scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+        info = dict(dtype="bf16", scale=scale, cow_pairs=int(len(cows)), groups=groups,
+                    beams=beams)
     else:
-        batch = make_workload(args.config, seed)
-        S, H, Hkv, D, B = (batch.num_seqs, batch.num_heads, batch.num_kv_heads,
-                           batch.head_size, batch.block_size)
-        tdt = torch.float16 if batch.dtype == "f16" else torch.bfloat16
-        L0 = batch.context_lens.astype(np.int64)            # context at the first step
+        lens, H, Hkv, D, B, dname = workload_shape(args.config, seed, args.block_size)
+        S = len(lens)
+        tdt = torch.float16 if dname == "f16" else torch.bfloat16
+        L0 = lens.astype(np.int64)                          # context at the first step
         final = L0 + total_steps
         num_blocks = int(math.ceil(1.2 * int(np.sum(-(-final // B)))))
         bm = pk.BlockManager(num_blocks, B, wl.free_order(num_blocks, seed))
         kc = torch.empty((layers, num_blocks, B, Hkv, D), dtype=tdt, device=dev)
         vc = torch.empty_like(kc)
         # prefill L-1 tokens of every sequence into every layer's pool
-        keep = np.ones(batch.total_tokens, bool)
-        keep[batch.offsets[1:] - 1] = False
         slots = []
         for s in range(S):
             bm.allocate(s, int(L0[s]) - 1)
             if L0[s] > 1:
                 slots.append(bm.slots(s))
         d_slots = torch.from_numpy(np.concatenate(slots)).to(dev)
-        kp = torch.from_numpy(batch.k_tokens[keep].view(np.int16)).view(tdt).to(dev)
-        vp = torch.from_numpy(batch.v_tokens[keep].view(np.int16)).view(tdt).to(dev)
+        if devv:
+            n = int(np.sum(L0 - 1))
+            of = 0.01 if args.config == "longctx" else 0.0
+            kp = device_tokens(n, Hkv, D, tdt, gen, dev, outlier_frac=of)
+            vp = device_tokens(n, Hkv, D, tdt, gen, dev)
+        else:
+            batch = make_workload(args.config, seed, B)
+            keep = np.ones(batch.total_tokens, bool)
+            keep[batch.offsets[1:] - 1] = False
+            kp = torch.from_numpy(batch.k_tokens[keep].view(np.int16)).view(tdt).to(dev)
+            vp = torch.from_numpy(batch.v_tokens[keep].view(np.int16)).view(tdt).to(dev)
         for l in range(layers):
             pk.pkv_reshape_and_cache(kp, vp, kc[l], vc[l], d_slots)
         del kp, vp, d_slots
         shared_extra = 0
-        info = dict(dtype=batch.dtype, scale=float(batch.scale))
+        info = dict(dtype=dname, scale=float(np.float32(1.0) / np.sqrt(np.float32(D))))
     torch.cuda.synchronize()
     width = int(np.max(-(-(L0 + total_steps) // B)))
     return dict(bm=bm, kc=kc, vc=vc, S=S, H=H, Hkv=Hkv, D=D, B=B, tdt=tdt, L0=L0,
@@ -446,7 +504,8 @@ def run_ours(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2)}
 
     peak, peak_kind = load_peaks()
-    traffic = profile_traffic(args.config, float(np.mean(per_call)))
+    traffic = profile_traffic(getattr(args, "profile_key", None) or args.config,
+                              float(np.mean(per_call)))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
@@ -457,6 +516,9 @@ def run_ours(args, rank, world, local_rank):
                    "context_tokens_first_step": int(L0.sum()), "partition_tokens": pk.pkv_decode_partition_tokens(width, B, pt),
                    "num_blocks": num_blocks, "seed": args.seed,
                    "l2": "inputs larger than L2 (each step reads every layer's pool)",
+                   "values": ("drawn on the device (torch generator)"
+                              if getattr(args, "device_values", False) else
+                              "workloads.py generators (host)"),
                    **({"groups": st["groups"], "beams": st["beams"],
                        "cow_pairs": st["cow_pairs"]} if "groups" in st else {})},
         "decode_tokens_per_s": round(tokens_s, 1),
@@ -642,7 +704,7 @@ def _oracle_worker(args):
     """Spawned process: build the oracle's state for a share of the sequences
     (untimed), then time oracle decode steps (append + scatter + attention)
     until the time budget is used."""
-    cfg, seed, seqs, budget_s, min_reps = args
+    cfg, seed, seqs, budget_s, min_reps, block_size, max_tokens = args
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[var] = "1"
     sys.path.insert(0, ROOT)
@@ -650,8 +712,8 @@ def _oracle_worker(args):
     from oracle.attention import paged_attention_decode
     from oracle.cache_ops import reshape_and_cache
     from oracle.pipeline import build_decode_state, pool_demand
-    all_lens, H, Hkv, D, B, dtype = workload_shape(cfg, seed)
-    lens = all_lens[seqs]
+    all_lens, H, Hkv, D, B, dtype = workload_shape(cfg, seed, block_size)
+    lens = np.minimum(all_lens[seqs], max_tokens) if max_tokens else all_lens[seqs]
     sub = wl.decode_batch("sample", lens, H, Hkv, D, B, dtype, seed + 1000 * seqs[0],
                           outlier_frac=0.01 if cfg == "longctx" else 0.0)
     n = pool_demand(lens + 64, sub.block_size) + 8
@@ -670,28 +732,45 @@ def _oracle_worker(args):
     return done_bytes, time.perf_counter() - t0, reps
 
 
-def oracle_throughput(cfg, seed, budget_s, min_reps=1):
+def oracle_throughput(cfg, seed, budget_s, min_reps=1, block_size=0):
     """Oracle GB/s on all host cores: the batch's sequences dealt round-robin
     to one spawned worker per core; each times whole oracle decode steps of
     its share for about ``budget_s`` seconds."""
-    n_seqs = len(workload_shape(cfg, seed)[0])
+    return oracle_throughputs([(cfg, block_size)], seed, budget_s, min_reps, 0)[0]
+
+
+def oracle_throughputs(cases, seed, budget_s, min_reps=1, one_seq_tokens=0):
+    """oracle_throughput of several (config, block size) cases through one
+    pool of spawned workers (one per core); returns one
+    (GB/s, workers, reps, wall seconds) per case. With one_seq_tokens > 0 each
+    worker takes a single sequence of the batch (spread over it), its context
+    capped at that many tokens: a bounded sample of a large batch."""
     cores = os.cpu_count() or 1
-    workers = min(cores, n_seqs)
-    shares = [list(range(w, n_seqs, workers)) for w in range(workers)]
+    jobs, spans = [], []
+    for cfg, bs in cases:
+        n_seqs = len(workload_shape(cfg, seed, bs)[0])
+        workers = min(cores, n_seqs)
+        spans.append((len(jobs), workers))
+        shares = ([[w * n_seqs // workers] for w in range(workers)] if one_seq_tokens else
+                  [list(range(w, n_seqs, workers)) for w in range(workers)])
+        jobs += [(cfg, seed, sh, budget_s, min_reps, bs, one_seq_tokens) for sh in shares]
     ctx = mp.get_context("spawn")
-    with ctx.Pool(workers) as pool:
-        res = pool.map(_oracle_worker, [(cfg, seed, s, budget_s, min_reps) for s in shares])
-    total = sum(r[0] for r in res)
-    wall = max(r[1] for r in res)
-    reps = min(r[2] for r in res)
-    return total / wall / 1e9, workers, reps, wall
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_worker, jobs, chunksize=1)
+    out = []
+    for first, workers in spans:
+        r = res[first:first + workers]
+        wall = max(x[1] for x in r)
+        out.append((sum(x[0] for x in r) / wall / 1e9, workers, min(x[2] for x in r), wall))
+    return out
 
 
 def run_reference(args, rank):
     """The oracle as it stands, timed on the host cores: each step is one
     bounded sample — a single layer's decode step of the whole batch."""
     gbs, cores, reps, wall = oracle_throughput(args.config, args.seed, budget_s=0.0,
-                                               min_reps=args.warmup + args.steps)
+                                               min_reps=args.warmup + args.steps,
+                                               block_size=args.block_size)
     sample = (f"{args.config} batch, one layer per step, {reps} oracle decode steps "
               f"(append + reshape_and_cache + fp64 attention) over {cores} spawn workers")
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
@@ -703,6 +782,119 @@ def run_reference(args, rank):
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- tiny batch latency
+
+def run_tiny(args):
+    """The tiny batch (4 sequences of 5..31 tokens, 4 heads, d = 64, B = 4,
+    fp16; ~64 KB of cache, resident in L2): decode-call latency only. One call
+    between two synchronisations (CUDA events around it), and the mean per
+    call when calls are queued back to back."""
+    import torch
+    import paged_kv_cache_118_gb300 as pk
+    import workloads as wl
+    from paged_kv_cache_118_gb300.cache import PagedKVCache
+    b = wl.tiny(args.seed)
+    order = wl.free_order(wl.TINY_POOL_BLOCKS, args.seed)
+    cache = PagedKVCache(wl.TINY_POOL_BLOCKS, b.block_size, b.num_kv_heads, b.head_size,
+                         torch.float16, free_order=order)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.float16).cuda()
+    cache.prefill(range(b.num_seqs), b.context_lens, up(b.k_tokens), up(b.v_tokens))
+    tables, ctx = cache.tables(range(b.num_seqs))
+    q = up(b.q)
+    out = torch.empty_like(q)
+    ws = cache.workspace(b.num_seqs, b.num_heads, tables.shape[1])
+    call = lambda: pk.pkv_paged_attention_decode(out, q, cache.k_cache, cache.v_cache, tables,
+                                                 ctx, b.block_size, float(b.scale), ws, 0,
+                                                 cache.err)
+    for _ in range(20):
+        call()
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    single = []
+    for _ in range(200):
+        a.record()
+        call()
+        e.record()
+        torch.cuda.synchronize()
+        single.append(a.elapsed_time(e) * 1e3)
+    n = 1000
+    a.record()
+    for _ in range(n):
+        call()
+    e.record()
+    torch.cuda.synchronize()
+    assert cache.err.item() == 0
+    return {"metric": "decode call latency (L2-resident; no roofline claim)", "unit": "us",
+            "latency_us": round(float(np.median(single)), 2),
+            "latency_us_p90": round(float(np.percentile(single, 90)), 2),
+            "back_to_back_us_per_call": round(a.elapsed_time(e) * 1e3 / n, 2),
+            "gpu_launches_per_call": 2,
+            "config": {"workload": "tiny_decode", "num_seqs": b.num_seqs,
+                       "context_lens": [int(x) for x in b.context_lens],
+                       "num_heads": b.num_heads, "num_kv_heads": b.num_kv_heads,
+                       "head_size": b.head_size, "block_size": b.block_size,
+                       "pool_blocks": wl.TINY_POOL_BLOCKS, "dtype": "f16"}}
+
+
+# ---------------------------------------------------------------- every workload
+
+def _summary(line):
+    """The per-config fields of a bench line."""
+    keep = ("value", "unit", "ms_per_step", "decode_tokens_per_s", "logical_GBps",
+            "frac_of_hbm_peak", "roofline", "e2e", "gpu_launches", "clocks", "config", "dtype",
+            "steps", "warmup")
+    return {k: line[k] for k in keep if k in line}
+
+
+def run_per_config(args, cpu):
+    """Every workload measured like the headline one (see PER_CONFIG); cpu maps
+    a key to its oracle baseline. A failure in one entry is recorded there and
+    does not stop the others."""
+    import torch
+    out = {}
+    try:
+        out["tiny"] = run_tiny(args)
+    except Exception as e:          # pragma: no cover - reported in the line
+        out["tiny"] = {"error": f"{type(e).__name__}: {e}"}
+    for key, cfg, bs, pt, layers in PER_CONFIG:
+        sub = argparse.Namespace(**vars(args))
+        sub.config, sub.block_size, sub.partition_tokens, sub.layers = cfg, bs, pt, layers
+        sub.steps, sub.warmup = args.per_config_steps, 3
+        sub.device_values, sub.profile_key = True, key
+        try:
+            line = _summary(run_ours(sub, 0, 1, 0))
+            line["cpu_baseline"] = cpu.get(key)
+            out[key] = line
+        except Exception as e:      # pragma: no cover - reported in the line
+            out[key] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return out
+
+
+def per_config_cpu(args):
+    """Oracle baselines of the per-config entries (one spawn pool; a share of
+    each batch per worker for about args.per_config_cpu_budget seconds).
+    Longctx at 512 and 1024 partitions share one: the oracle has no partitions."""
+    cases, keys = [], []
+    for key, cfg, bs, pt, layers in PER_CONFIG:
+        if (cfg, bs) not in cases:
+            cases.append((cfg, bs))
+        keys.append((key, cases.index((cfg, bs))))
+    cap = 8192
+    res = oracle_throughputs(cases, args.seed, args.per_config_cpu_budget, one_seq_tokens=cap)
+    out = {}
+    for key, i in keys:
+        gbs, cores, reps, wall = res[i]
+        cfg, bs = cases[i]
+        out[key] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                    "sample": f"{cfg} batch (block size {bs}): one sequence per worker, spread "
+                              f"over the batch, context capped at {cap} tokens; {reps}+ oracle "
+                              f"decode steps (append + reshape_and_cache + fp64 attention) per "
+                              f"worker, {wall:.1f} s on {cores} spawn workers"}
+    return out
 
 
 # ---------------------------------------------------------------- main
@@ -717,6 +909,12 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="block size of the workload (0: its own, 16); llama13b sweeps 8..128")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config measurements of the default run")
+    ap.add_argument("--per-config-steps", type=int, default=10)
+    ap.add_argument("--per-config-cpu-budget", type=float, default=2.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -746,10 +944,17 @@ def main():
             print(json.dumps(run_reference(args, rank)), flush=True)
         return
 
+    per_config = (world == 1 and not args.no_per_config and args.config == "opt13b"
+                  and args.block_size in (0, 16) and args.partition_tokens == 0
+                  and args.layers == 0)
     cpu = None
+    cpu_per = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # before the first GPU call: the oracle pool is spawned, not forked
-        gbs, cores, reps, wall = oracle_throughput(args.config, args.seed, args.cpu_budget)
+        # before the first GPU call: the oracle pools are spawned, not forked
+        if per_config:
+            cpu_per = per_config_cpu(args)
+        gbs, cores, reps, wall = oracle_throughput(args.config, args.seed, args.cpu_budget,
+                                                   block_size=args.block_size)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{args.config} batch, one layer, {reps}+ oracle decode steps per "
                          f"worker (append + reshape_and_cache + fp64 attention), "
@@ -761,6 +966,11 @@ def main():
         td.init_process_group("nccl")
     line = run_ours(args, rank, world, local_rank)
     line["cpu_baseline"] = cpu
+    if per_config and rank == 0:
+        import torch
+        torch.cuda.empty_cache()
+        line["per_config"] = {"opt13b": dict(_summary(line), cpu_baseline=cpu),
+                              **run_per_config(args, cpu_per)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

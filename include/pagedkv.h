@@ -129,7 +129,9 @@ pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
  *    pkv_decode_workspace_size(num_seqs, num_heads, head_size,
  *    max_blocks_per_seq, block_size, partition_tokens) > PKV_NOALLOC_SCRATCH_BYTES.
  *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream
+ *    device, with that device current; host code cannot name device memory
+ *    directly), and so does the first call after a cudaDeviceReset of that
+ *    device, which unloads the array. Make that first call before any stream
  *    capture. A failed lookup returns PKV_ECUDA.
  *  - All calls share the one array and it keeps the last call's contents.
  *    Nothing in it needs to start at zero (each call writes every partial it

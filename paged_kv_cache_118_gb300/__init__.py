@@ -105,9 +105,73 @@ def _ptr(t) -> int | None:
 
 
 def _need_cuda(*ts):
-    for t in ts:
-        if t is not None and not t.is_cuda:
-            raise ValueError("pagedkv kernels take CUDA tensors")
+    devs = {t.device for t in ts if t is not None}
+    if any(d.type != "cuda" for d in devs):
+        raise ValueError("pagedkv kernels take CUDA tensors")
+    if len(devs) > 1:
+        raise ValueError(f"pagedkv tensors must share one device, got {sorted(map(str, devs))}")
+
+
+# ---------------------------------------------------------------- argument checks
+# The C ABI sees only pointers and sizes, so every shape, dtype and layout fact
+# the kernels rely on is checked here first: a tensor of the wrong type or shape
+# would otherwise be read or written past its end.
+
+_KV_DTYPES = (torch.float16, torch.bfloat16)
+
+
+def _require(cond: bool, where: str, what: str) -> None:
+    if not cond:
+        raise ValueError(f"{where}: {what}")
+
+
+def _contiguous(where: str, **ts) -> None:
+    for name, t in ts.items():
+        if t is not None:
+            _require(t.is_contiguous(), where, f"{name} must be contiguous")
+
+
+def _check_caches(where: str, k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    _require(k_cache.dim() == 4, where,
+             "k_cache must be [num_blocks, block_size, num_kv_heads, head_size]")
+    _require(tuple(v_cache.shape) == tuple(k_cache.shape), where,
+             f"v_cache shape {tuple(v_cache.shape)} != k_cache shape {tuple(k_cache.shape)}")
+    _require(k_cache.dtype in _KV_DTYPES and v_cache.dtype == k_cache.dtype, where,
+             "caches must both be float16 or both bfloat16")
+    _contiguous(where, k_cache=k_cache, v_cache=v_cache)
+
+
+def _check_int(where: str, name: str, t: torch.Tensor, dtype, shape) -> None:
+    _require(t.dtype == dtype, where, f"{name} must be {dtype}, got {t.dtype}")
+    _require(tuple(t.shape) == tuple(shape), where,
+             f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    _require(t.is_contiguous(), where, f"{name} must be contiguous")
+
+
+def _check_err(where: str, err_flag) -> None:
+    if err_flag is not None:
+        _require(err_flag.dtype == torch.int32 and err_flag.numel() >= 1, where,
+                 "err_flag must be an int32 tensor of at least one element")
+
+
+def _check_decode(where: str, out, q, k_cache, v_cache, block_tables, context_lens,
+                  block_size, err_flag) -> None:
+    _check_caches(where, k_cache, v_cache)
+    nb, B, Hkv, D = k_cache.shape
+    _require(q.dim() == 3, where, "q must be [num_seqs, num_heads, head_size]")
+    S, H, Dq = q.shape
+    _require(q.dtype == k_cache.dtype, where, f"q dtype {q.dtype} != cache dtype {k_cache.dtype}")
+    _require(Dq == D, where, f"q head_size {Dq} != cache head_size {D}")
+    _require(H % Hkv == 0, where, f"num_heads {H} is not a multiple of num_kv_heads {Hkv}")
+    _require(int(block_size) == B, where, f"block_size {block_size} != cache block size {B}")
+    _require(tuple(out.shape) == tuple(q.shape), where,
+             f"out shape {tuple(out.shape)} != q shape {tuple(q.shape)}")
+    _require(out.dtype in _DTYPE, where, f"out dtype {out.dtype} is not float16/bfloat16/float32")
+    _require(block_tables.dim() == 2, where, "block_tables must be [num_seqs, max_blocks_per_seq]")
+    _check_int(where, "block_tables", block_tables, torch.int32, (S, block_tables.shape[1]))
+    _check_int(where, "context_lens", context_lens, torch.int32, (S,))
+    _contiguous(where, q=q, out=out)
+    _check_err(where, err_flag)
 
 
 # ---------------------------------------------------------------- kernels
@@ -144,9 +208,13 @@ def pkv_paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torc
     num_kv_heads, head_size]; block_tables: int32 [num_seqs, max_blocks_per_seq];
     context_lens: int32 [num_seqs]; workspace: bytes from decode_workspace().
     """
+    where = "pkv_paged_attention_decode"
+    _check_decode(where, out, q, k_cache, v_cache, block_tables, context_lens, block_size,
+                  err_flag)
+    _contiguous(where, workspace=workspace)
     _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, err_flag)
     S, H, D = q.shape
-    nb, B, Hkv, D2 = k_cache.shape
+    nb, B, Hkv, _ = k_cache.shape
     st = lib.pkv_paged_attention_decode(
         _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
         _ptr(block_tables), _ptr(context_lens), S, H, Hkv, D, nb, block_size,
@@ -166,6 +234,8 @@ def pkv_paged_attention_decode_noalloc(out: torch.Tensor, q: torch.Tensor,
     """pkv_paged_attention_decode without a workspace argument, for callers that
     cannot allocate device memory: the partials go to the library's built-in
     NOALLOC_SCRATCH_BYTES array (shared by all calls; keep calls on one stream)."""
+    _check_decode("pkv_paged_attention_decode_noalloc", out, q, k_cache, v_cache, block_tables,
+                  context_lens, block_size, err_flag)
     _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, err_flag)
     S, H, D = q.shape
     nb, B, Hkv, _ = k_cache.shape
@@ -184,9 +254,24 @@ def pkv_paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: tor
     """Causal attention of each sequence's query chunk (its last C tokens) over
     its paged history. q, out: [total_queries, num_heads, head_size];
     query_start: int32 [num_seqs + 1]."""
+    where = "pkv_paged_attention_prefill"
+    _check_caches(where, k_cache, v_cache)
+    nb, B, Hkv, D = k_cache.shape
+    _require(q.dim() == 3 and q.shape[2] == D, where, "q must be [total_queries, num_heads, head_size]")
+    _require(q.dtype == k_cache.dtype, where, f"q dtype {q.dtype} != cache dtype {k_cache.dtype}")
+    _require(q.shape[1] % Hkv == 0, where, "num_heads is not a multiple of num_kv_heads")
+    _require(int(block_size) == B, where, f"block_size {block_size} != cache block size {B}")
+    _require(tuple(out.shape) == tuple(q.shape), where, "out must have q's shape")
+    _require(out.dtype in _DTYPE, where, f"out dtype {out.dtype} is not float16/bfloat16/float32")
+    S = context_lens.shape[0] if context_lens.dim() == 1 else -1
+    _check_int(where, "context_lens", context_lens, torch.int32, (S,))
+    _require(block_tables.dim() == 2, where, "block_tables must be [num_seqs, max_blocks_per_seq]")
+    _check_int(where, "block_tables", block_tables, torch.int32, (S, block_tables.shape[1]))
+    _check_int(where, "query_start", query_start, torch.int32, (S + 1,))
+    _contiguous(where, q=q, out=out)
+    _check_err(where, err_flag)
     _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start, err_flag)
     _, H, D = q.shape
-    nb, B, Hkv, _ = k_cache.shape
     st = lib.pkv_paged_attention_prefill(
         _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
         _ptr(block_tables), _ptr(context_lens), _ptr(query_start), context_lens.shape[0], H,
@@ -199,6 +284,17 @@ def pkv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tenso
                           v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                           err_flag: torch.Tensor | None = None, stream=None) -> None:
     """k_cache[slot // B, slot % B] = k[t] (and v) for every token t with slot >= 0."""
+    where = "pkv_reshape_and_cache"
+    _check_caches(where, k_cache, v_cache)
+    _require(k.dim() == 3 and tuple(v.shape) == tuple(k.shape), where,
+             "k and v must both be [num_tokens, num_kv_heads, head_size]")
+    _require(tuple(k.shape[1:]) == tuple(k_cache.shape[2:]), where,
+             f"k rows {tuple(k.shape[1:])} != cache rows {tuple(k_cache.shape[2:])}")
+    _require(k.dtype == k_cache.dtype and v.dtype == k_cache.dtype, where,
+             f"k/v dtype must be the cache dtype {k_cache.dtype}")
+    _check_int(where, "slot_mapping", slot_mapping, torch.int64, (k.shape[0],))
+    _contiguous(where, k=k, v=v)
+    _check_err(where, err_flag)
     _need_cuda(k, v, k_cache, v_cache, slot_mapping, err_flag)
     T, Hkv, D = k.shape
     nb, B = k_cache.shape[:2]
@@ -214,6 +310,7 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
 
     src_dst_pairs: host int32 array-like [n, 2]."""
     import numpy as np
+    _check_caches("pkv_copy_blocks", k_cache, v_cache)
     _need_cuda(k_cache, v_cache)
     pairs = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int32).reshape(-1, 2))
     block_bytes = k_cache[0].numel() * k_cache.element_size()
@@ -227,6 +324,11 @@ def pkv_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tenso
     """dst pool block d = src pool block s for each (s, d); either pool may be a
     pinned host tensor (swap space)."""
     import numpy as np
+    where = "pkv_swap_blocks"
+    _check_caches(where, src_k, src_v)
+    _check_caches(where, dst_k, dst_v)
+    _require(tuple(dst_k.shape[1:]) == tuple(src_k.shape[1:]) and dst_k.dtype == src_k.dtype,
+             where, "source and destination pools must have the same block shape and dtype")
     for t in (dst_k, dst_v, src_k, src_v):
         if not (t.is_cuda or t.is_pinned()):
             raise ValueError("swap pools must be CUDA tensors or pinned host tensors")

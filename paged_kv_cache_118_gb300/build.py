@@ -28,7 +28,7 @@ LIB = os.path.join(PKG, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 SOURCES = ["decode_attention.cu", "decode_tc.cu", "prefill_attention.cu", "cache_ops.cu",
-           "tma_map.cpp", "block_manager.cpp", "api.cpp"]
+           "tma_map.cpp", "device_state.cpp", "block_manager.cpp", "api.cpp"]
 
 
 def nvcc() -> str:

@@ -95,15 +95,11 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// SM count of the current device (152 on GB300 if the lookup fails: it only
+// sizes the grid of a grid-stride loop).
 static int sm_count() {
-  static int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      v = 152;
-    return v;
-  }();
-  return n;
+  int n = 0;
+  return device_sm_count(&n) == cudaSuccess ? n : 152;
 }
 
 }  // namespace pkv

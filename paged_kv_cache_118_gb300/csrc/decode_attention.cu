@@ -1029,7 +1029,17 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     } else {
       // Merge this warp's partial into shared memory (one row of D + 2 floats
       // per head: m, l, acc), then the four warps' rows into the unit's partial.
-      if (k >= 1) mbar_wait(&merge_bar[1], (k - 1) & 1);   // previous unit's partials read
+      // A wait that gives up flags the timeout and aborts the kernel; the merge
+      // is then skipped (its shared rows may still be in use).
+      auto merge_wait = [&](uint64_t* bar, int parity) {
+        const bool w = __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        if (!w && lane == 0) {
+          flag_error(p.err, PKV_DEVERR_TIMEOUT);
+          st_volatile(abort_flag, 1);
+        }
+        return w;
+      };
+      const bool free_ok = k < 1 || merge_wait(&merge_bar[1], (k - 1) & 1);  // previous partials read
       // Lanes j, j+8, j+16, j+24 hold the same elements: merge the groups first.
 #pragma unroll
       for (int g = 0; g < GS; ++g) {
@@ -1052,22 +1062,23 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
           b += __shfl_xor_sync(0xffffffffu, b, 8);
           a += __shfl_xor_sync(0xffffffffu, a, 16);
           b += __shfl_xor_sync(0xffffffffu, b, 16);
-          if (grp == 0) {
+          if (grp == 0 && free_ok) {
             const int el = (e / 4) * 64 + 8 * j + 2 * (e % 4);
             cw[2 + el] = a;
             cw[2 + el + 1] = b;
           }
         }
-        if (grp == 0 && j == 0) {
+        if (grp == 0 && j == 0 && free_ok) {
           cw[0] = mx;
           cw[1] = ls;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&merge_bar[0]);
-      mbar_wait(&merge_bar[0], k & 1);
+      const bool full_ok = merge_wait(&merge_bar[0], k & 1);
 
-      for (int idx = threadIdx.x; idx < heads * D; idx += kConsumerWarps * 32) {
+      for (int idx = threadIdx.x; free_ok && full_ok && idx < heads * D;
+           idx += kConsumerWarps * 32) {
         const int g = idx / D;
         const int e = idx % D;
         float mw[kConsumerWarps];
@@ -1235,45 +1246,22 @@ static int pick_group_slice(int group) {
   return 1;
 }
 
-static int device_sm_count() {
-  static int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      v = 0;
-    return v;
-  }();
-  return n;
-}
-
 template <int D, int GS, typename T, bool kMma>
 static cudaError_t launch_partition(const CUtensorMap& tk, const CUtensorMap& tv,
                                     const DecodeParams& p, cudaStream_t stream) {
   auto kern = decode_partition_kernel<D, GS, T, kMma>;
   const int slice = p.partition_tokens / p.block_size + 2;
   const int smem = DecodeLayout<D, GS, kMma>::smem_bytes(slice);
-  // Attribute and occupancy are looked up once per shared-memory size.
-  static int cached_smem = -1, cached_blocks = 0;
-  static std::mutex mu;
-  int per_sm;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (cached_smem != smem) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      int blocks = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, smem);
-      if (e != cudaSuccess) return e;
-      cached_smem = smem;
-      cached_blocks = blocks;
-    }
-    per_sm = cached_blocks;
-  }
-  const int sms = device_sm_count();
-  if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+  // attribute and occupancy: once per device and shared-memory size
+  int per_sm = 0, sms = 0;
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), kThreads, smem, &per_sm);
+  if (e != cudaSuccess) return e;
+  e = device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int grid = static_cast<int>(std::min<int64_t>(p.total_units,
                                                       static_cast<int64_t>(sms) * per_sm));
-  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int), stream);
+  e = cudaMemsetAsync(p.counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(tk, tv, p);
   return cudaGetLastError();
@@ -1517,20 +1505,29 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};   // context the address belongs to
 }  // namespace
 
 // Device address of g_noalloc_scratch on the current device. Host code only
 // sees a host-side stand-in under the array's name, so the address is looked
-// up once per device (with that device current) and remembered.
+// up with the device current, once per device, and remembered together with
+// the unique id of the context it was found in: after a cudaDeviceReset the
+// device runs a new context (with the library's image loaded anew), whose
+// first call looks the address up again instead of using a stale one.
 static pkv_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ECUDA;
+  unsigned long long ctx_id = 0;
+  if (!current_context_id(&ctx_id)) return PKV_ECUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc_ptr[dev] == nullptr || ctx_id == 0 || g_noalloc_ctx[dev] != ctx_id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return PKV_ECUDA;
+    // the lookup makes the device's context current if none was
+    if (ctx_id == 0 && !current_context_id(&ctx_id)) return PKV_ECUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx_id;
   }
   *out = g_noalloc_ptr[dev];
   return PKV_OK;

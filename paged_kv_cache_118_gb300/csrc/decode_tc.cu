@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
       tc_commit(drain);
-      mbar_wait(drain, 0);
+      if (!mbar_wait(drain, 0)) flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- softmax
@@ -758,22 +758,16 @@ static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const CU
                           const Params& p, cudaStream_t s) {
   auto kern = decode_tc_kernel<D, T, C>;
   using Lay = Layout<D, C>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  static int sms = 0;
   // one CTA per SM: it holds all 512 tensor-memory columns, so shared memory is
   // requested past half an SM even where the layout needs less (d = 64)
   constexpr int kSmemLaunch = Lay::kSmem > 120 * 1024 ? Lay::kSmem : 120 * 1024;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
-    int dev = 0;
-    if (attr == cudaSuccess) attr = cudaGetDevice(&dev);
-    if (attr == cudaSuccess)
-      attr = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  });
-  if (attr != cudaSuccess) return attr;
+  int sms = 0;
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), kThreads, kSmemLaunch,
+                                 nullptr);
+  if (e == cudaSuccess) e = device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(p.total_units, sms));
-  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int), s);
+  e = cudaMemsetAsync(p.counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, kSmemLaunch, s>>>(tk, tv, tq, p);
   return cudaGetLastError();

@@ -10,6 +10,16 @@ namespace pkv {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Unique id of the CUDA context current on this thread (0 if none is); false
+// if the driver cannot tell.
+bool current_context_id(unsigned long long* id);
+// SM count of the current device, looked up once per device.
+cudaError_t device_sm_count(int* sms);
+// Sets a kernel's dynamic shared-memory limit to smem_bytes on the current
+// device and returns how many CTAs of `threads` threads fit on one SM (both
+// once per device, kernel and size; ctas_per_sm may be NULL).
+cudaError_t prepare_kernel(const void* kernel, int threads, int smem_bytes, int* ctas_per_sm);
+
 // TMA map of one cache.
 //  kRowsPlain: 3-D view (D, KV head, slot), box D x 1 x box_rows.
 //  kRowsSwizzled: 4-D view (64 elements, slot, KV head, D/64 lines), box

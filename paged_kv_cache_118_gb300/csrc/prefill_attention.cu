@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
       // everything issued has completed before the columns are freed
       tc_commit(drain);
-      mbar_wait(drain, 0);
+      if (!mbar_wait(drain, 0)) flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- softmax
@@ -490,14 +490,11 @@ template <int D, typename T>
 static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Params& p,
                           int num_kv_heads, int num_seqs, cudaStream_t s) {
   auto kern = prefill_kernel<D, T>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
   // one CTA per SM: it holds all 512 tensor-memory columns, so shared memory is
   // requested past half an SM even where the layout needs less (d = 64)
   constexpr int kSmemLaunch = Layout<D>::kSmem > 120 * 1024 ? Layout<D>::kSmem : 120 * 1024;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch);
-  });
+  const cudaError_t attr =
+      prepare_kernel(reinterpret_cast<const void*>(kern), kThreads, kSmemLaunch, nullptr);
   if (attr != cudaSuccess) return attr;
   const int tiles = (p.max_query_len * p.group + kQTiles * kRows - 1) / (kQTiles * kRows);
   dim3 grid(tiles, num_kv_heads, num_seqs);

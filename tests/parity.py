@@ -88,6 +88,53 @@ def oracle_sampled(batch, seqs):
     return out
 
 
+def _available_bytes() -> int:
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 16 << 30
+
+
+def oracle_all(batch, seqs=None, max_workers=8):
+    """Oracle outputs [H, D] of every sequence (or of ``seqs``), each computed
+    from a pool of its own, by a pool of threads (numpy's array operations
+    release the interpreter lock). The number of threads is bounded by host
+    memory: the oracle widens a sequence's keys and values to float64, with
+    temporaries of about eight times their element count each."""
+    import concurrent.futures as cf
+    seqs = list(range(batch.num_seqs)) if seqs is None else list(seqs)
+    longest = int(max(batch.context_lens[s] for s in seqs))
+    per_seq = longest * batch.num_kv_heads * batch.head_size * 8 * 8 * 2
+    workers = max(1, min(max_workers, len(seqs), _available_bytes() // 2 // max(per_seq, 1)))
+    out = {}
+    with cf.ThreadPoolExecutor(workers) as ex:
+        for part in ex.map(lambda s: oracle_sampled(batch, [s]), seqs):
+            out.update(part)
+    return out
+
+
+def stack_oracle(want: dict, seqs) -> np.ndarray:
+    return np.stack([want[s] for s in seqs])
+
+
+def record_max_err(name: str, err: float) -> None:
+    """Keep the largest error seen per check; written as JSON to the path in
+    PKV_PARITY_REPORT (if set) so that a run can report it."""
+    import json
+    import os
+    RECORDED[name] = max(err, RECORDED.get(name, 0.0))
+    path = os.environ.get("PKV_PARITY_REPORT")
+    if path:
+        with open(path, "w") as f:
+            json.dump(RECORDED, f, indent=1, sort_keys=True)
+
+
+RECORDED: dict = {}
+
+
 def sample_seqs(lens, k, seed):
     """Shortest, longest, median and k-3 seeded others."""
     order = np.argsort(lens, kind="stable")

@@ -1,9 +1,18 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py
-times (block size 16 or the sweep's, 512-token partitions, output in the
-input dtype): sampled sequences against the oracle (all heads of each), plus
-what holds at any size — bit-exact tables, pools and copy pairs against the
-oracle's host pipeline, bit-identical outputs across block sizes."""
+times (block size 16 or the sweep's, the default partitions, output in the
+input dtype), and with fp32 outputs held to the plain bound: EVERY sequence
+and head of each batch against the oracle, element by element. Also what
+holds at any size: bit-exact tables, pools and copy pairs against the
+oracle's host pipeline, and bit-identical outputs across block sizes.
 
+The long-context batch also runs at its stated 512-token partitions (1232
+partitions, up to 256 partials per row for the merge).
+
+The oracle is one fp64 mat-vec per (sequence, head); it runs on a pool of
+host threads (tests/parity.py, ``oracle_all``).
+"""
+
+import functools
 import math
 
 import numpy as np
@@ -13,7 +22,8 @@ import torch
 from oracle.attention import paged_attention_decode as oracle_decode
 from oracle.block_manager import BlockManager as RefBM
 from oracle.pipeline import build_decode_state, build_shared_prefix_state, pool_demand
-from parity import (assert_close, dev, gpu_decode_state, oracle_sampled, sample_seqs)
+from parity import (assert_close, dev, gpu_decode_state, oracle_all, record_max_err,
+                    stack_oracle)
 from workloads import (LLAMA_BLOCK_SIZES, free_order, gqa_prefix, llama13b, longctx, mqa,
                        opt13b, poison_bits)
 
@@ -36,6 +46,18 @@ def _tables_match_oracle(batch, n, order, tables):
                                                                    tables.shape[1]))
 
 
+def _check_all(name, cache, q, tables, ctx, scale, want, dtype, partition_tokens=0):
+    """Both output types of one decode call against the oracle, every element."""
+    out = cache.attend(q, tables, ctx, scale, partition_tokens=partition_tokens)
+    out32 = torch.empty(out.shape, dtype=torch.float32, device="cuda")
+    cache.attend(q, tables, ctx, scale, out=out32, partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    record_max_err(f"{name} ({dtype} out)", assert_close(out, want, dtype))
+    record_max_err(f"{name} (fp32 out)", assert_close(out32, want, dtype))
+    assert cache.err.item() == 0
+    return out
+
+
 def test_opt13b_full():
     batch = opt13b(0)
     n = _pool(batch.context_lens, 16)
@@ -47,20 +69,14 @@ def test_opt13b_full():
                           ref["k_cache"])
     assert np.array_equal(cache.v_cache.view(torch.int16).cpu().numpy().view(np.uint16),
                           ref["v_cache"])
-    out = cache.attend(dev(batch.q, "f16"), tables, ctx, float(batch.scale))
-    torch.cuda.synchronize()
-    seqs = sample_seqs(batch.context_lens, 8, 0)
-    want = oracle_decode(batch.q, ref["k_cache"], ref["v_cache"], ref["block_tables"],
-                         batch.context_lens, 16, batch.scale, "f16", seqs=seqs)
-    assert_close(out[seqs], want[seqs], "f16")
-    assert cache.err.item() == 0
+    want = stack_oracle(oracle_all(batch), range(batch.num_seqs))
+    _check_all("opt13b", cache, dev(batch.q, "f16"), tables, ctx, float(batch.scale), want, "f16")
 
 
 def test_llama13b_block_size_sweep_full():
     outs = []
     base = llama13b(0, block_size=16)
-    seqs = sample_seqs(base.context_lens, 4, 1)
-    want = oracle_sampled(base, seqs)
+    want = stack_oracle(oracle_all(base), range(base.num_seqs))   # the same for every B
     for B in LLAMA_BLOCK_SIZES:
         batch = base
         batch.block_size = B
@@ -68,11 +84,8 @@ def test_llama13b_block_size_sweep_full():
         order = free_order(n, B)
         cache, tables, ctx = gpu_decode_state(batch, n, order, poison=False)
         _tables_match_oracle(batch, n, order, tables)
-        out = cache.attend(dev(batch.q, "f16"), tables, ctx, float(batch.scale))
-        torch.cuda.synchronize()
-        for s in seqs:
-            assert_close(out[s], want[s], "f16")
-        assert cache.err.item() == 0
+        out = _check_all(f"llama13b B={B}", cache, dev(batch.q, "f16"), tables, ctx,
+                         float(batch.scale), want, "f16")
         outs.append(out.cpu())
         del cache, tables, ctx, out
         torch.cuda.empty_cache()
@@ -111,48 +124,52 @@ def test_gqa_shared_prefix_full():
                           ref["k_cache"])
     assert np.array_equal(cache.v_cache.view(torch.int16).cpu().numpy().view(np.uint16),
                           ref["v_cache"])
-    out = cache.attend(dev(pb.q, "bf16"), tables, ctx, float(pb.scale))
-    torch.cuda.synchronize()
-    seqs = sample_seqs(np.array(lens_logical), 8, 2)
-    want = oracle_decode(pb.q, ref["k_cache"], ref["v_cache"], ref["block_tables"],
-                         ref["context_lens"], 16, pb.scale, "bf16", seqs=seqs)
-    assert_close(out[seqs], want[seqs], "bf16")
-    assert cache.err.item() == 0
+    # every beam against the oracle on the oracle's own shared-prefix pool
+    want = _oracle_threads(lambda s: oracle_decode(
+        pb.q, ref["k_cache"], ref["v_cache"], ref["block_tables"], ref["context_lens"], 16,
+        pb.scale, "bf16", seqs=[s])[s], S)
+    _check_all("gqa_prefix", cache, dev(pb.q, "bf16"), tables, ctx, float(pb.scale), want, "bf16")
 
 
-def test_longctx_full():
+def _oracle_threads(fn, n, workers=8):
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(workers) as ex:
+        return np.stack(list(ex.map(fn, range(n))))
+
+
+@functools.lru_cache(maxsize=1)
+def _longctx():
     batch = longctx(0)
+    return batch, stack_oracle(oracle_all(batch, max_workers=4), range(batch.num_seqs))
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 512])
+def test_longctx_full(partition_tokens):
+    """0: the default for so long a table (1024-token partitions, what bench.py
+    times by default); 512: the workload's stated partitions, 1232 of them,
+    up to 256 partials per row in the merge."""
+    import paged_kv_cache_118_gb300 as pk
+    batch, want = _longctx()
     n = _pool(batch.context_lens, 16)
     order = free_order(n, 0)
     cache, tables, ctx = gpu_decode_state(batch, n, order, poison=True)
     _tables_match_oracle(batch, n, order, tables)
-    out = cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale))
-    out32 = torch.empty(out.shape, dtype=torch.float32, device="cuda")
-    cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale), out=out32)
-    torch.cuda.synchronize()
-    seqs = [0, 4, 7]                       # 32k, 128k, 40k tokens
-    want = oracle_sampled(batch, seqs)
-    for s in seqs:
-        assert_close(out[s], want[s], "bf16")
-        assert_close(out32[s], want[s], "bf16")
-    assert cache.err.item() == 0
+    pt = pk.pkv_decode_partition_tokens(tables.shape[1], 16, partition_tokens)
+    assert pt == (1024 if partition_tokens == 0 else 512)
+    if pt == 512:
+        parts = sum(-(-int(L) // 512) for L in batch.context_lens)
+        assert parts == 1232 and -(-int(batch.context_lens.max()) // 512) == 256
+    _check_all(f"longctx partitions={pt}", cache, dev(batch.q, "bf16"), tables, ctx,
+               float(batch.scale), want, "bf16", partition_tokens=partition_tokens)
 
 
 def test_mqa_full():
-    """64 query heads on one KV head (the tensor-memory path): sampled
-    sequences against the oracle, both output types."""
+    """64 query heads on one KV head (the tensor-memory path): every sequence
+    against the oracle, both output types."""
     batch = mqa(0)
     n = _pool(batch.context_lens, 16)
     order = free_order(n, 0)
     cache, tables, ctx = gpu_decode_state(batch, n, order, poison=True)
     _tables_match_oracle(batch, n, order, tables)
-    out = cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale))
-    out32 = torch.empty(out.shape, dtype=torch.float32, device="cuda")
-    cache.attend(dev(batch.q, "bf16"), tables, ctx, float(batch.scale), out=out32)
-    torch.cuda.synchronize()
-    seqs = sample_seqs(batch.context_lens, 6, 1)
-    want = oracle_sampled(batch, seqs)
-    for s in seqs:
-        assert_close(out[s], want[s], "bf16")
-        assert_close(out32[s], want[s], "bf16")
-    assert cache.err.item() == 0
+    want = stack_oracle(oracle_all(batch), range(batch.num_seqs))
+    _check_all("mqa", cache, dev(batch.q, "bf16"), tables, ctx, float(batch.scale), want, "bf16")

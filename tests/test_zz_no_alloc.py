@@ -4,9 +4,14 @@ loop that must not call cudaMalloc once it runs): it takes no workspace and
 keeps its partials in a fixed array inside the library.
 
 Checked through the C ABI against the regular entry point, which takes a
-caller workspace, on two calls in a row with different batches (the array
-keeps the first call's contents when the second one runs). This file is
-collected last on purpose.
+caller workspace, on calls in a row with different batches (the array keeps
+the previous call's contents when the next one runs). Both entry points run
+the same deterministic kernels on the same inputs, so their outputs must be
+identical bit for bit: a read of stale or foreign rows of the shared array
+would show up even where it stayed inside the attention tolerance. The test
+needs nothing from other tests: it passes alone in a fresh process and after
+them. Its file is collected after the others, so that a run which stops at
+the first failure has run every other test first.
 """
 
 import ctypes
@@ -17,7 +22,7 @@ import torch
 
 import paged_kv_cache_118_gb300 as pk
 from oracle.pipeline import pool_demand
-from parity import BOUND, dev, gpu_decode_state
+from parity import dev, gpu_decode_state
 from workloads import decode_batch, free_order
 
 pytestmark = pytest.mark.gpu
@@ -61,8 +66,7 @@ def test_matches_workspace_entry_point_twice_in_a_row():
         outs.append(got)
     torch.cuda.synchronize()
     for (batch, cache, tables, ctx, q, want, dt), got in zip(runs, outs):
-        diff = (got.float() - want.float()).abs().max().item()
-        assert diff <= BOUND[dt], diff
+        assert torch.equal(got, want), (got.float() - want.float()).abs().max().item()
         assert cache.err.item() == 0
 
 

@@ -254,10 +254,9 @@ def gqa_prefix(seed: int = 0, groups: int = 64, beams: int = 4, prefix_tokens: i
     ``prefix_tokens`` + r_g tokens (r_g uniform in [1, max_partial], or 0 when
     ``partial`` is False) and each beam appends a tail of 1..max_tail tokens."""
     H, H_kv, d, B, dtype = 32, 8, 128, 16, "bf16"
-    g_len, g_pk, g_pv, g_tk, g_tv, g_q = _streams(seed, 6)
-    r = g_len.integers(1, max_partial, size=groups, endpoint=True) if partial else np.zeros(groups, np.int64)
-    prefix_lens = (prefix_tokens + r).astype(np.int32)
-    tail_lens = g_len.integers(1, max_tail, size=groups * beams, endpoint=True).astype(np.int32)
+    _, g_pk, g_pv, g_tk, g_tv, g_q = _streams(seed, 6)
+    prefix_lens, tail_lens = gqa_prefix_lengths(seed, groups, beams, prefix_tokens, max_partial,
+                                                max_tail, partial)
     p_off = np.zeros(groups + 1, np.int64)
     np.cumsum(prefix_lens, out=p_off[1:])
     t_off = np.zeros(groups * beams + 1, np.int64)
@@ -270,6 +269,19 @@ def gqa_prefix(seed: int = 0, groups: int = 64, beams: int = 4, prefix_tokens: i
     scale = np.float32(1.0) / np.sqrt(np.float32(d))
     return SharedPrefixBatch("gqa_prefix", dtype, H, H_kv, d, B, np.float32(scale), beams,
                              prefix_lens, p_off, pk, pv, tail_lens, t_off, tk, tv, q, seed)
+
+
+def gqa_prefix_lengths(seed: int = 0, groups: int = 64, beams: int = 4,
+                       prefix_tokens: int = 1024, max_partial: int = 15, max_tail: int = 512,
+                       partial: bool = True):
+    """The shared-prefix workload's lengths alone (the draws ``gqa_prefix``
+    makes first, from the same stream): per group the shared tokens
+    ``prefix_tokens`` + r_g, per beam its tail length."""
+    g_len = _streams(seed, 6)[0]
+    r = g_len.integers(1, max_partial, size=groups, endpoint=True) if partial else np.zeros(groups, np.int64)
+    prefix_lens = (prefix_tokens + r).astype(np.int32)
+    tail_lens = g_len.integers(1, max_tail, size=groups * beams, endpoint=True).astype(np.int32)
+    return prefix_lens, tail_lens
 
 
 def new_tokens(num_seqs: int, num_kv_heads: int, head_size: int, dtype: str,
