@@ -8,6 +8,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 
 #include "pkv_host.h"
 
@@ -17,6 +18,7 @@ namespace {
 std::mutex g_mu;
 std::map<int, int> g_sms;                                      // device -> SM count
 std::map<std::tuple<int, const void*, int>, int> g_occupancy;  // (device, kernel, smem) -> CTAs/SM
+std::map<std::pair<int, const void*>, int> g_smem_limit;        // (device, kernel) -> limit set
 
 template <typename F>
 F driver_entry(const char* name, int version) {
@@ -62,11 +64,17 @@ cudaError_t prepare_kernel(const void* kernel, int threads, int smem_bytes, int*
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_mu);
+  // The limit only ever grows: a launch with less shared memory than the
+  // limit is fine, one with more is refused.
+  int& limit = g_smem_limit[std::make_pair(dev, kernel)];
+  if (smem_bytes > limit) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    limit = smem_bytes;
+  }
   const auto key = std::make_tuple(dev, kernel, smem_bytes);
   auto it = g_occupancy.find(key);
   if (it == g_occupancy.end()) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
     int blocks = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem_bytes);
     if (e != cudaSuccess) return e;
