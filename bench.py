@@ -716,12 +716,13 @@ def _oracle_worker(args):
     lens = np.minimum(all_lens[seqs], max_tokens) if max_tokens else all_lens[seqs]
     sub = wl.decode_batch("sample", lens, H, Hkv, D, B, dtype, seed + 1000 * seqs[0],
                           outlier_frac=0.01 if cfg == "longctx" else 0.0)
-    n = pool_demand(lens + 64, sub.block_size) + 8
+    max_reps = max(min_reps, 2048)           # the pool holds this many appended tokens
+    n = pool_demand(lens + max_reps, sub.block_size) + 8
     st = build_decode_state(sub, n, wl.free_order(n, seed), wl.poison_bits(sub.dtype))
     bm, kc, vc = st["bm"], st["k_cache"], st["v_cache"]
     nk, nv = wl.new_tokens(len(seqs), sub.num_kv_heads, sub.head_size, sub.dtype, seed, 0)
     done_bytes, reps, t0 = 0, 0, time.perf_counter()
-    while reps < min_reps or time.perf_counter() - t0 < budget_s:
+    while reps < min_reps or (time.perf_counter() - t0 < budget_s and reps < max_reps):
         new_slots = np.array([bm.append_slot(s)[0] for s in range(len(seqs))], np.int64)
         reshape_and_cache(nk, nv, kc, vc, new_slots)
         ctx = np.array([bm.length(s) for s in range(len(seqs))], np.int64)
