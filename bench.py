@@ -912,6 +912,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--block-size", type=int, default=0,
                     help="block size of the workload (0: its own, 16); llama13b sweeps 8..128")
+    ap.add_argument("--device-values", action="store_true",
+                    help="draw the cached keys/values on the device (as the per-config runs do)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-config measurements of the default run")
     ap.add_argument("--per-config-steps", type=int, default=10)

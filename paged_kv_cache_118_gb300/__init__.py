@@ -105,11 +105,17 @@ def _ptr(t) -> int | None:
 
 
 def _need_cuda(*ts):
-    devs = {t.device for t in ts if t is not None}
-    if any(d.type != "cuda" for d in devs):
-        raise ValueError("pagedkv kernels take CUDA tensors")
-    if len(devs) > 1:
-        raise ValueError(f"pagedkv tensors must share one device, got {sorted(map(str, devs))}")
+    d0 = None
+    for t in ts:
+        if t is None:
+            continue
+        d = t.device
+        if d0 is None:
+            d0 = d
+        if d != d0 or d.type != "cuda":
+            if d.type != "cuda" or d0.type != "cuda":
+                raise ValueError("pagedkv kernels take CUDA tensors")
+            raise ValueError(f"pagedkv tensors must share one device, got {d0} and {d}")
 
 
 # ---------------------------------------------------------------- argument checks
@@ -154,8 +160,39 @@ def _check_err(where: str, err_flag) -> None:
                  "err_flag must be an int32 tensor of at least one element")
 
 
+_I32, _I64 = torch.int32, torch.int64
+
+
+def _caches_ok(k_cache, v_cache) -> bool:
+    ks = k_cache.shape
+    kd = k_cache.dtype
+    return (len(ks) == 4 and v_cache.shape == ks and (kd is torch.float16 or kd is torch.bfloat16)
+            and v_cache.dtype is kd and k_cache.is_contiguous() and v_cache.is_contiguous())
+
+
+def _err_ok(err_flag) -> bool:
+    return err_flag is None or (err_flag.dtype is _I32 and err_flag.numel() >= 1)
+
+
+def _decode_ok(out, q, k_cache, v_cache, block_tables, context_lens, block_size,
+               err_flag) -> bool:
+    """Every fact _check_decode checks, as one cheap expression (the wrappers
+    run on every decode call; the detailed checks only run when this fails)."""
+    if not _caches_ok(k_cache, v_cache):
+        return False
+    ks, qs, bs = k_cache.shape, q.shape, block_tables.shape
+    return (len(qs) == 3 and q.dtype is k_cache.dtype and qs[2] == ks[3] and qs[1] % ks[2] == 0
+            and block_size == ks[1] and out.shape == qs and out.dtype in _DTYPE
+            and len(bs) == 2 and block_tables.dtype is _I32 and bs[0] == qs[0]
+            and context_lens.dtype is _I32 and context_lens.shape == (qs[0],)
+            and q.is_contiguous() and out.is_contiguous() and block_tables.is_contiguous()
+            and context_lens.is_contiguous() and _err_ok(err_flag))
+
+
 def _check_decode(where: str, out, q, k_cache, v_cache, block_tables, context_lens,
                   block_size, err_flag) -> None:
+    if _decode_ok(out, q, k_cache, v_cache, block_tables, context_lens, block_size, err_flag):
+        return
     _check_caches(where, k_cache, v_cache)
     nb, B, Hkv, D = k_cache.shape
     _require(q.dim() == 3, where, "q must be [num_seqs, num_heads, head_size]")
@@ -172,6 +209,7 @@ def _check_decode(where: str, out, q, k_cache, v_cache, block_tables, context_le
     _check_int(where, "context_lens", context_lens, torch.int32, (S,))
     _contiguous(where, q=q, out=out)
     _check_err(where, err_flag)
+    raise ValueError(f"{where}: arguments rejected")
 
 
 # ---------------------------------------------------------------- kernels
@@ -284,17 +322,24 @@ def pkv_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tenso
                           v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                           err_flag: torch.Tensor | None = None, stream=None) -> None:
     """k_cache[slot // B, slot % B] = k[t] (and v) for every token t with slot >= 0."""
-    where = "pkv_reshape_and_cache"
-    _check_caches(where, k_cache, v_cache)
-    _require(k.dim() == 3 and tuple(v.shape) == tuple(k.shape), where,
-             "k and v must both be [num_tokens, num_kv_heads, head_size]")
-    _require(tuple(k.shape[1:]) == tuple(k_cache.shape[2:]), where,
-             f"k rows {tuple(k.shape[1:])} != cache rows {tuple(k_cache.shape[2:])}")
-    _require(k.dtype == k_cache.dtype and v.dtype == k_cache.dtype, where,
-             f"k/v dtype must be the cache dtype {k_cache.dtype}")
-    _check_int(where, "slot_mapping", slot_mapping, torch.int64, (k.shape[0],))
-    _contiguous(where, k=k, v=v)
-    _check_err(where, err_flag)
+    kshape = k.shape
+    if not (_caches_ok(k_cache, v_cache) and len(kshape) == 3 and v.shape == kshape
+            and kshape[1:] == k_cache.shape[2:] and k.dtype is k_cache.dtype
+            and v.dtype is k_cache.dtype and slot_mapping.dtype is _I64
+            and slot_mapping.shape == kshape[:1] and slot_mapping.is_contiguous()
+            and k.is_contiguous() and v.is_contiguous() and _err_ok(err_flag)):
+        where = "pkv_reshape_and_cache"
+        _check_caches(where, k_cache, v_cache)
+        _require(k.dim() == 3 and tuple(v.shape) == tuple(k.shape), where,
+                 "k and v must both be [num_tokens, num_kv_heads, head_size]")
+        _require(tuple(k.shape[1:]) == tuple(k_cache.shape[2:]), where,
+                 f"k rows {tuple(k.shape[1:])} != cache rows {tuple(k_cache.shape[2:])}")
+        _require(k.dtype == k_cache.dtype and v.dtype == k_cache.dtype, where,
+                 f"k/v dtype must be the cache dtype {k_cache.dtype}")
+        _check_int(where, "slot_mapping", slot_mapping, torch.int64, (k.shape[0],))
+        _contiguous(where, k=k, v=v)
+        _check_err(where, err_flag)
+        raise ValueError(f"{where}: arguments rejected")
     _need_cuda(k, v, k_cache, v_cache, slot_mapping, err_flag)
     T, Hkv, D = k.shape
     nb, B = k_cache.shape[:2]

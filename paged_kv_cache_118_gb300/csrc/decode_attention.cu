@@ -121,9 +121,12 @@ struct DecodeLayout {
   static constexpr int kNumBars = 2 * kStages + 1 + 1 + 2 + 2 * kSchedSlots + 3;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;    // units[1], then sched[]
   static constexpr int kOffFlag = kOffUnits + (1 + kSchedSlots) * sizeof(UnitDesc);
-  static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of partitions per sequence
+  static constexpr int kOffPref = (kOffFlag + 16 + 15) / 16 * 16;  // prefix of whole partitions per sequence
   static constexpr int kOffGroup = kOffPref + ((kCompactMaxSeqs + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kOffSlice = kOffGroup + (kCompactMaxSeqs * 2 + 15) / 16 * 16;  // after group info
+  // the sequences with a partial last partition, largest first (16-bit ids);
+  // on the scalar paths, which form no groups, it takes the group info's place
+  static constexpr int kOffOrder = kOffGroup + (kMma ? (kCompactMaxSeqs * 2 + 15) / 16 * 16 : 0);
+  static constexpr int kOffSlice = kOffOrder + (kCompactMaxSeqs * 2 + 15) / 16 * 16;
   // table_slice: entries of one unit's block-table slice; kSchedSlots are staged
   static int smem_bytes(int table_slice) {
     return 1024 /*alignment slack*/ + kOffSlice + ((kSchedSlots * table_slice * 4 + 15) / 16) * 16;
@@ -502,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   int* issued_tiles = abort_flag + 1;         // copy warp's tile count, read by the scheduler
   int* pref = reinterpret_cast<int*>(smem + Lay::kOffPref);
   uint16_t* ginfo = reinterpret_cast<uint16_t*>(smem + Lay::kOffGroup);
+  uint16_t* porder = reinterpret_cast<uint16_t*>(smem + Lay::kOffOrder);
   int32_t* slice = reinterpret_cast<int32_t*>(smem + Lay::kOffSlice);
 
   const int warp = threadIdx.x >> 5;
@@ -549,9 +553,12 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     }
     const bool grouping = kMma && cap > 1 && compact && p.max_parts <= kMaxGroupParts;
     // The work list. For batches of up to kCompactMaxSeqs sequences only the
-    // units that exist are numbered, sequence-major (a prefix sum of claims
-    // per sequence, then a binary search per claim); larger batches number
-    // every (partition, sequence, slice) and skip the empty ones.
+    // units that exist are numbered: first every whole partition,
+    // sequence-major (a prefix sum of claims per sequence, then a binary
+    // search per claim), then the partial last partitions, largest first, so
+    // that the list ends with its shortest units and the CTAs finish close
+    // together. Larger batches number every (partition, sequence, slice) and
+    // skip the empty ones.
     //
     // Groups (tensor path): consecutive sequences of a window whose first
     // blocks are the same physical block (a shared prefix) form a group. The
@@ -561,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     // for that partition and serves the runs of identical ones (normally one
     // run: the whole group) as units.
     int total = p.total_units;
+    int whole_units = 0;                      // compact list: claims of whole partitions
     if (compact) {
       // all lengths (and first blocks) in one round of loads, then the scan
       int lens[kCompactMaxSeqs / 32], fblk[kCompactMaxSeqs / 32];
@@ -580,10 +588,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
         const int L = lens[it];
         const bool valid = s < p.num_seqs && L >= 1 && L <= max_ctx;
         if (s < p.num_seqs && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-        const int np = valid ? (L + p.partition_tokens - 1) / p.partition_tokens : 0;
-        int c = np;                           // claims of this sequence, in partitions
+        const int whole = valid ? L / p.partition_tokens : 0;
+        int c = whole;                        // claims of this sequence's whole partitions
         if (grouping) {
-          const int whole = valid ? L / p.partition_tokens : 0;
           const int fb = fblk[it];
           const int fb_prev = __shfl_up_sync(0xffffffffu, fb, 1);
           const int valid_prev = __shfl_up_sync(0xffffffffu, valid ? 1 : 0, 1);
@@ -604,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
           uint16_t gi = 0;
           if (nx - hd > 1) {
             const bool member = lane != hd;
-            if (member) c = np - fmin;
+            if (member) c = whole - fmin;
             gi = static_cast<uint16_t>((fmin << 4) | ((nx - hd - 1) << 1) | (member ? 1 : 0));
           }
           if (s < p.num_seqs) ginfo[s] = gi;
@@ -619,8 +626,50 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
         carry += __shfl_sync(0xffffffffu, x, 31);
       }
       if (lane == 0) pref[0] = 0;
+      whole_units = carry;
+      // The partial last partitions, sorted by tile count, largest first
+      // (counting sort; equal counts keep the sequence order): counts per
+      // tile count, their offsets, then each sequence's place.
+      const int nbk = p.partition_tokens / kTile;      // tile counts 1 .. nbk
+      int* cursor = reinterpret_cast<int*>(combine);    // free until the first merge
+      for (int i = lane; i <= nbk; i += 32) cursor[i] = 0;
       __syncwarp();
-      total = carry * p.kv_slices;
+      auto tail_tiles = [&](int s, int L) {
+        const bool valid = s < p.num_seqs && L >= 1 && L <= max_ctx;
+        const int r = valid ? L % p.partition_tokens : 0;
+        return (r + kTile - 1) / kTile;                 // 0: no partial partition
+      };
+#pragma unroll
+      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
+        if (it * 32 >= p.num_seqs) break;
+        const int b = tail_tiles(it * 32 + lane, lens[it]);
+        const unsigned same = __match_any_sync(0xffffffffu, b);
+        if (b > 0 && lane == __ffs(same) - 1) cursor[b] += __popc(same);
+        __syncwarp();
+      }
+      if (lane == 0) {                                  // offsets, largest tile count first
+        int acc = 0;
+        for (int b = nbk; b >= 1; --b) {
+          const int n = cursor[b];
+          cursor[b] = acc;
+          acc += n;
+        }
+        cursor[0] = acc;                                // partial partitions in all
+      }
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
+        if (it * 32 >= p.num_seqs) break;
+        const int b = tail_tiles(it * 32 + lane, lens[it]);
+        const unsigned same = __match_any_sync(0xffffffffu, b);
+        const int base = b > 0 ? cursor[b] : 0;
+        if (b > 0) porder[base + __popc(same & ((1u << lane) - 1u))] = static_cast<uint16_t>(it * 32 + lane);
+        __syncwarp();
+        if (b > 0 && lane == __ffs(same) - 1) cursor[b] = base + __popc(same);
+        __syncwarp();
+      }
+      total = (whole_units + cursor[0]) * p.kv_slices;
+      __syncwarp();
     }
     const int ahead = kMma ? kClaimAheadTilesMma : kClaimAheadTiles;
     bool ok = true;
@@ -692,7 +741,14 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
           int part, seq, kvs;
           int F = 0, gs = 1;
           bool member = false;
-          if (compact) {
+          if (compact && u >= whole_units * p.kv_slices) {
+            // a partial last partition (its index follows from the length)
+            const int w = u - whole_units * p.kv_slices;
+            const int idx = w / p.kv_slices;
+            kvs = w - idx * p.kv_slices;
+            seq = porder[idx];
+            part = -1;
+          } else if (compact) {
             int lo = 0, hi = p.num_seqs;      // largest lo with pref[lo] * slices <= u
             while (hi - lo > 1) {
               const int mid = (lo + hi) >> 1;
@@ -715,9 +771,9 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
             seq = rem / p.kv_slices;
             kvs = rem - seq * p.kv_slices;
           }
-          const int t_begin = part * p.partition_tokens;
-          const int need = t_begin + p.partition_tokens;    // end of a whole partition
-          const int jb0 = t_begin / B;
+          int t_begin = part * p.partition_tokens;
+          int need = t_begin + p.partition_tokens;    // end of a whole partition
+          int jb0 = t_begin / B;
           const int kvh = kvs / p.subs;
           const int head0 = kvh * p.group + (kvs - kvh * p.subs) * p.heads_per_cta;
           if (!member && gs > 1 && part < F) {
@@ -769,6 +825,12 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
             if (lane == 0 && part == 0 && kvs == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
             continue;
           }
+          if (part < 0) {                     // the partial last partition
+            part = L / p.partition_tokens;
+            t_begin = part * p.partition_tokens;
+            need = t_begin + p.partition_tokens;
+            jb0 = t_begin / B;
+          }
           if (t_begin >= L) continue;         // this sequence has no such partition
           const int t_end = min(L, need);
           load_slice(seq, jb0, (t_end - 1) / B - jb0 + 1);
@@ -793,23 +855,27 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
 
   // ------------------------------------------------------------ copy warp
   // Publishes each staged unit to the consumers (its query rows by bulk copy)
-  // and streams its K/V tiles through the ring. One thread.
+  // and streams its K/V tiles through the ring. The lanes issue a tile's
+  // copies (and a unit's query rows) together, each resolving its own block
+  // id, so that issuing a tile costs a few dependent steps of the warp rather
+  // than one thread's chain of every copy. Every lane waits on the barriers
+  // itself (each then reads what the barrier published, or writes into the
+  // space it freed); lane 0 makes the arrivals.
   if (warp == kConsumerWarps) {
-    if (lane != 0) return;
     const uint64_t policy = l2_evict_first_policy();
     const uint32_t copy_bytes = static_cast<uint32_t>(p.box_rows) * Lay::kRowBytes;
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
+    const int bshift = 31 - __clz(B);                 // block_size is a power of two
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
     int issued = 0;                           // tiles issued (ring position)
     int k = 0;                                // units published
-    int ok = 1;
-    int last_issued[kStages];
-#pragma unroll
-    for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
+    bool ok = true;
     while (true) {
       const int sb = k % kSchedSlots;
-      if (!mbar_wait(&sched_full[sb], (k / kSchedSlots) & 1)) {
-        ok = 0;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sched_full[sb], (k / kSchedSlots) & 1))) {
+        ok = false;
         break;
       }
       const UnitDesc d = sched[sb];
@@ -817,68 +883,78 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
       const int t_begin = d.part * p.partition_tokens;
       const int t_end = min(d.len, t_begin + p.partition_tokens);
       const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
-      const int jb0 = t_begin / B;
+      const int jb0 = t_begin >> bshift;
       const int kvh = d.head0 / p.group;
       const int32_t* sl = slice + sb * slice_cap;
       const int qb = 0;                       // one query buffer
-      if (k >= 1 && !mbar_wait(&q_empty[qb], (k - 1) & 1)) {
-        ok = 0;
+      if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(&q_empty[qb], (k - 1) & 1))) {
+        ok = false;
         break;
       }
-      units[qb] = d;
       const uint32_t qbytes = static_cast<uint32_t>(p.heads_per_cta) * D * 2;
-      mbar_arrive_expect_tx(&q_full[qb], qbytes * d.nrun);
-      for (int b = 0; b < d.nrun; ++b)
-        bulk_load(qbuf + qb * GS * D + b * p.heads_per_cta * D,
-                  p.q + (static_cast<int64_t>(d.seq + b) * p.num_heads + d.head0) * D, qbytes,
+      if (lane == 0) {
+        units[qb] = d;
+        mbar_arrive_expect_tx(&q_full[qb], qbytes * d.nrun);
+      }
+      __syncwarp();
+      if (lane < d.nrun)
+        bulk_load(qbuf + qb * GS * D + lane * p.heads_per_cta * D,
+                  p.q + (static_cast<int64_t>(d.seq + lane) * p.num_heads + d.head0) * D, qbytes,
                   &q_full[qb]);
       ++k;
       for (int i = 0; i < n_tiles; ++i, ++issued) {
         const int st = issued % kStages;
-        if (issued >= kStages && !mbar_wait(&empty_bar[st], ((issued / kStages) & 1) ^ 1)) {
-          ok = 0;
+        if (issued >= kStages &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty_bar[st], ((issued / kStages) & 1) ^ 1))) {
+          ok = false;
           break;
         }
-        if (ld_volatile(abort_flag)) {
-          ok = 0;
+        if (__shfl_sync(0xffffffffu, ld_volatile(abort_flag), 0)) {
+          ok = false;
           break;
         }
         const int t0 = t_begin + i * kTile;
         const int valid = min(kTile, t_end - t0);
-        const int copies = B >= kTile ? 1 : (valid + B - 1) / B;
+        const int copies = B >= kTile ? 1 : (valid + B - 1) >> bshift;
         uint8_t* kdst = ring + st * Lay::kStageBytes;
-        uint8_t* vdst = kdst + Lay::kTileBytes;
-        mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
-        for (int c = 0; c < copies; ++c) {
-          const int z = B >= kTile ? sl[t0 / B - jb0] * B + (t0 % B) : sl[t0 / B + c - jb0] * B;
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], 2u * copies * copy_bytes);
+        __syncwarp();
+        // copy j: K (j even) or V (j odd) of the tile's block j / 2
+        for (int j = lane; j < 2 * copies; j += 32) {
+          const int c = j >> 1;
+          const int z = B >= kTile ? (sl[(t0 >> bshift) - jb0] << bshift) + (t0 & (B - 1))
+                                   : sl[(t0 >> bshift) + c - jb0] << bshift;
+          uint8_t* dst = kdst + (j & 1) * Lay::kTileBytes + c * copy_bytes;
+          const CUtensorMap* map = (j & 1) ? &tm_v : &tm_k;
           if constexpr (kMma) {
             // 4-D view (64 elements, slot, head, D/64 lines): whole rows, swizzled
-            tma_load_4d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, z, kvh, 0, policy);
-            tma_load_4d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, z, kvh, 0, policy);
+            tma_load_4d(dst, map, &full_bar[st], 0, z, kvh, 0, policy);
           } else {
-            tma_load_3d(kdst + c * copy_bytes, &tm_k, &full_bar[st], 0, kvh, z, policy);
-            tma_load_3d(vdst + c * copy_bytes, &tm_v, &full_bar[st], 0, kvh, z, policy);
+            tma_load_3d(dst, map, &full_bar[st], 0, kvh, z, policy);
           }
         }
-        last_issued[st] = issued;
-        st_volatile(issued_tiles, issued + 1);
+        if (lane == 0) st_volatile(issued_tiles, issued + 1);
       }
       if (!ok) break;
-      mbar_arrive(&sched_empty[sb]);          // the slice has been read
+      __syncwarp();                           // every lane is done with the slice
+      if (lane == 0) mbar_arrive(&sched_empty[sb]);
     }
-    // Publish the end of the work (or the abort) to the consumers.
-    const int qb = 0;
-    if (ok && k >= 1 && !mbar_wait(&q_empty[qb], (k - 1) & 1)) ok = 0;
-    if (!ok) {
-      flag_error(p.err, PKV_DEVERR_TIMEOUT);
-      st_volatile(abort_flag, 1);
-    }
-    units[qb].seq = ok ? -1 : -2;
-    mbar_arrive(&q_full[qb]);
-    if (!ok) {
-      // Let the copies already in flight land before the CTA can retire.
-      for (int st = 0; st < kStages; ++st)
-        if (last_issued[st] >= 0) mbar_wait(&full_bar[st], (last_issued[st] / kStages) & 1);
+    if (lane == 0) {
+      // Publish the end of the work (or the abort) to the consumers.
+      const int qb = 0;
+      if (ok && k >= 1 && !mbar_wait(&q_empty[qb], (k - 1) & 1)) ok = false;
+      if (!ok) {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        st_volatile(abort_flag, 1);
+      }
+      units[qb].seq = ok ? -1 : -2;
+      mbar_arrive(&q_full[qb]);
+      if (!ok) {
+        // Let the copies in flight (the last kStages tiles issued) land
+        // before the CTA can retire.
+        for (int g = max(0, issued - kStages); g < issued; ++g)
+          mbar_wait(&full_bar[g % kStages], (g / kStages) & 1);
+      }
     }
     return;
   }
