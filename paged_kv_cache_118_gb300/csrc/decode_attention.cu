@@ -468,6 +468,125 @@ struct MmaState {
   }
 };
 
+// Builds the compact work list (see decode_partition_kernel) with all the
+// CTA's threads: per chunk of 32 sequences (one warp each, every load in
+// flight at once) the claims of whole partitions, the group info and the tile
+// count of the partial last partition; then the prefix sums over the chunks,
+// and a counting sort of the partial partitions by tile count, largest first
+// (the order among equal counts is whatever the shared-memory atomics give:
+// it decides which CTA serves a unit, not any result). `scratch` is shared
+// memory that no copy has reached yet (the ring); a proxy fence hands it back
+// to the TMA copies. Ends with a block-wide barrier.
+__device__ __forceinline__ void build_work_list(const DecodeParams& p, int max_ctx, bool grouping,
+                                                int cap, int* scratch, int* pref, uint16_t* ginfo,
+                                                uint16_t* porder, int& whole_units,
+                                                int& partial_units) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kChunksPerWarp = (kCompactMaxSeqs / 32 + kWarps - 1) / kWarps;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = p.num_seqs;
+  const int nchunks = (n + 31) / 32;
+  const int PT = p.partition_tokens;
+  const int nbk = PT / kTile;                          // tile counts of partial partitions: 1 .. nbk
+  int* chunk_sum = scratch;                            // [32]: claims per chunk, then offsets
+  int* totals = scratch + 32;                          // [2]: whole claims, partial partitions
+  int* cursor = scratch + 40;                          // [nbk + 1]: counts, then places
+  uint8_t* tiles_of = reinterpret_cast<uint8_t*>(scratch + 48 + nbk);   // [n] (0: no partial)
+  for (int i = tid; i <= nbk; i += kThreads) cursor[i] = 0;
+  __syncthreads();
+  int L[kChunksPerWarp], fb[kChunksPerWarp];
+#pragma unroll
+  for (int j = 0; j < kChunksPerWarp; ++j) {          // every load of this warp in flight at once
+    const int s = (warp + j * kWarps) * 32 + lane;
+    L[j] = s < n ? __ldg(p.context_lens + s) : 0;
+    fb[j] = (grouping && s < n) ? __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq) : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kChunksPerWarp; ++j) {
+    const int ch = warp + j * kWarps;
+    if (ch >= nchunks) break;
+    const int s = ch * 32 + lane;
+    const bool valid = s < n && L[j] >= 1 && L[j] <= max_ctx;
+    if (s < n && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+    const int whole = valid ? L[j] / PT : 0;
+    int c = whole;                                     // claims of this sequence's whole partitions
+    if (grouping) {
+      const int fb_prev = __shfl_up_sync(0xffffffffu, fb[j], 1);
+      const int valid_prev = __shfl_up_sync(0xffffffffu, valid ? 1 : 0, 1);
+      // windows never straddle the 32 lanes: cap divides 32
+      const bool link = valid && valid_prev && (s & (cap - 1)) != 0 && fb[j] >= 0 && fb[j] == fb_prev;
+      const unsigned starts = __ballot_sync(0xffffffffu, !link);
+      const int hd = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // group's first lane
+      const int wb = lane & ~(cap - 1);
+      const unsigned later = starts & ~(0xffffffffu >> (31 - hd));
+      const int nx = later ? min(__ffs(later) - 1, wb + cap) : wb + cap;  // past the group
+      int fmin = whole;
+#pragma unroll
+      for (int m = 0; m < kMaxRun; ++m) {
+        const int v = __shfl_sync(0xffffffffu, whole, (wb + m) & 31);
+        if (m < cap && wb + m >= hd && wb + m < nx) fmin = min(fmin, v);
+      }
+      uint16_t gi = 0;
+      if (nx - hd > 1) {
+        const bool member = lane != hd;
+        if (member) c = whole - fmin;
+        gi = static_cast<uint16_t>((fmin << 4) | ((nx - hd - 1) << 1) | (member ? 1 : 0));
+      }
+      if (s < n) ginfo[s] = gi;
+    }
+    int x = c;                                         // inclusive scan within the chunk
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (s < n) pref[s + 1] = x;
+    if (lane == 31) chunk_sum[ch] = x;
+    const int r = valid ? L[j] % PT : 0;
+    const int t = (r + kTile - 1) / kTile;
+    if (s < n) tiles_of[s] = static_cast<uint8_t>(t);     // t <= nbk <= 128
+    if (t > 0) atomicAdd(&cursor[t], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {                                     // chunk offsets (exclusive)
+    const int v = lane < nchunks ? chunk_sum[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < nchunks) chunk_sum[lane] = x - v;
+    if (lane == 31) totals[0] = x;
+  } else if (warp == 1) {                              // places of the tile counts, largest first
+    int carry = 0;
+    for (int top = nbk; top >= 1; top -= 32) {
+      const int b = top - lane;
+      const int v = b >= 1 ? cursor[b] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b >= 1) cursor[b] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) totals[1] = carry;
+  }
+  __syncthreads();
+  for (int s = tid; s < n; s += kThreads) {
+    pref[s + 1] += chunk_sum[s >> 5];
+    const int t = tiles_of[s];
+    if (t > 0) porder[atomicAdd(&cursor[t], 1)] = static_cast<uint16_t>(s);
+  }
+  if (tid == 0) pref[0] = 0;
+  whole_units = totals[0];
+  partial_units = totals[1];
+  fence_proxy_async_smem();                            // the ring goes back to the copies
+  __syncthreads();
+}
+
 // Persistent: each CTA takes units of work — (context partition, sequence,
 // KV-head slice), partition-major — from a global counter until none is
 // left. The scheduler and copy warps fetch the next unit, its slice of the
@@ -536,6 +655,33 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   }
   __syncthreads();
 
+  // The work list. For batches of up to kCompactMaxSeqs sequences only the
+  // units that exist are numbered: first every whole partition,
+  // sequence-major (a prefix sum of claims per sequence, then a binary search
+  // per claim), then the partial last partitions, largest first, so that the
+  // list ends with its shortest units and the CTAs finish close together.
+  // Every warp helps build it before taking its role. Larger batches number
+  // every (partition, sequence, slice) and skip the empty ones.
+  //
+  // Groups (tensor path): consecutive sequences of an aligned window of `cap`
+  // (a power of two) whose first blocks are the same physical block (a shared
+  // prefix) form a group. The partitions that are whole for every member, F
+  // of them, are claimed once for the group by its first sequence; each member
+  // claims only its own partitions from F on. A group claim checks the
+  // members' table entries for that partition and serves the runs of identical
+  // ones (normally one run: the whole group) as units.
+  const bool compact = p.num_seqs <= kCompactMaxSeqs;
+  int cap = 1;
+  if (kMma) {
+    const int c = min(kMmaRows / p.heads_per_cta, kMaxRun);
+    cap = 1 << (31 - __clz(c));
+  }
+  const bool grouping = kMma && cap > 1 && compact && p.max_parts <= kMaxGroupParts;
+  int whole_units = 0, partial_units = 0;
+  if (compact)
+    build_work_list(p, max_ctx, grouping, cap, reinterpret_cast<int*>(ring), pref, ginfo, porder,
+                    whole_units, partial_units);
+
   // ------------------------------------------------------------ scheduler warp
   // Claims units from the global counter, resolves each one (sequence,
   // partition, head slice; on the tensor path the run of sequences that share
@@ -543,134 +689,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
   // warp, so that none of this latency falls between two units of the copy
   // stream.
   if (warp == kConsumerWarps + 1) {
-    const bool compact = p.num_seqs <= kCompactMaxSeqs;
-    // Tensor path: the sequences of an aligned window of `cap` (a power of two)
-    // may be served together.
-    int cap = 1;
-    if (kMma) {
-      const int c = min(kMmaRows / p.heads_per_cta, kMaxRun);
-      cap = 1 << (31 - __clz(c));
-    }
-    const bool grouping = kMma && cap > 1 && compact && p.max_parts <= kMaxGroupParts;
-    // The work list. For batches of up to kCompactMaxSeqs sequences only the
-    // units that exist are numbered: first every whole partition,
-    // sequence-major (a prefix sum of claims per sequence, then a binary
-    // search per claim), then the partial last partitions, largest first, so
-    // that the list ends with its shortest units and the CTAs finish close
-    // together. Larger batches number every (partition, sequence, slice) and
-    // skip the empty ones.
-    //
-    // Groups (tensor path): consecutive sequences of a window whose first
-    // blocks are the same physical block (a shared prefix) form a group. The
-    // partitions that are whole for every member, F of them, are claimed once
-    // for the group by its first sequence; each member claims only its own
-    // partitions from F on. A group claim checks the members' table entries
-    // for that partition and serves the runs of identical ones (normally one
-    // run: the whole group) as units.
-    int total = p.total_units;
-    int whole_units = 0;                      // compact list: claims of whole partitions
-    if (compact) {
-      // all lengths (and first blocks) in one round of loads, then the scan
-      int lens[kCompactMaxSeqs / 32], fblk[kCompactMaxSeqs / 32];
-#pragma unroll
-      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
-        const int s = it * 32 + lane;
-        lens[it] = s < p.num_seqs ? __ldg(p.context_lens + s) : 0;
-        fblk[it] = (grouping && s < p.num_seqs)
-                       ? __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq)
-                       : -1;
-      }
-      int carry = 0;
-#pragma unroll
-      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
-        if (it * 32 >= p.num_seqs) break;
-        const int s = it * 32 + lane;
-        const int L = lens[it];
-        const bool valid = s < p.num_seqs && L >= 1 && L <= max_ctx;
-        if (s < p.num_seqs && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-        const int whole = valid ? L / p.partition_tokens : 0;
-        int c = whole;                        // claims of this sequence's whole partitions
-        if (grouping) {
-          const int fb = fblk[it];
-          const int fb_prev = __shfl_up_sync(0xffffffffu, fb, 1);
-          const int valid_prev = __shfl_up_sync(0xffffffffu, valid ? 1 : 0, 1);
-          // windows never straddle the 32 lanes: cap divides 32
-          const bool link = valid && valid_prev && (s & (cap - 1)) != 0 && fb >= 0 && fb == fb_prev;
-          const unsigned starts = __ballot_sync(0xffffffffu, !link);
-          const int hd = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // group's first lane
-          const int wb = lane & ~(cap - 1);
-          const unsigned later = starts & ~(0xffffffffu >> (31 - hd));
-          const int nx = later ? min(__ffs(later) - 1, wb + cap) : wb + cap;  // past the group
-          int fmin = whole;
-#pragma unroll
-          for (int j = 0; j < kMaxRun; ++j) {
-            const int lj = (wb + j) & 31;
-            const int v = __shfl_sync(0xffffffffu, whole, lj);
-            if (j < cap && wb + j >= hd && wb + j < nx) fmin = min(fmin, v);
-          }
-          uint16_t gi = 0;
-          if (nx - hd > 1) {
-            const bool member = lane != hd;
-            if (member) c = whole - fmin;
-            gi = static_cast<uint16_t>((fmin << 4) | ((nx - hd - 1) << 1) | (member ? 1 : 0));
-          }
-          if (s < p.num_seqs) ginfo[s] = gi;
-        }
-        int x = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (s < p.num_seqs) pref[s + 1] = carry + x;
-        carry += __shfl_sync(0xffffffffu, x, 31);
-      }
-      if (lane == 0) pref[0] = 0;
-      whole_units = carry;
-      // The partial last partitions, sorted by tile count, largest first
-      // (counting sort; equal counts keep the sequence order): counts per
-      // tile count, their offsets, then each sequence's place.
-      const int nbk = p.partition_tokens / kTile;      // tile counts 1 .. nbk
-      int* cursor = reinterpret_cast<int*>(combine);    // free until the first merge
-      for (int i = lane; i <= nbk; i += 32) cursor[i] = 0;
-      __syncwarp();
-      auto tail_tiles = [&](int s, int L) {
-        const bool valid = s < p.num_seqs && L >= 1 && L <= max_ctx;
-        const int r = valid ? L % p.partition_tokens : 0;
-        return (r + kTile - 1) / kTile;                 // 0: no partial partition
-      };
-#pragma unroll
-      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
-        if (it * 32 >= p.num_seqs) break;
-        const int b = tail_tiles(it * 32 + lane, lens[it]);
-        const unsigned same = __match_any_sync(0xffffffffu, b);
-        if (b > 0 && lane == __ffs(same) - 1) cursor[b] += __popc(same);
-        __syncwarp();
-      }
-      if (lane == 0) {                                  // offsets, largest tile count first
-        int acc = 0;
-        for (int b = nbk; b >= 1; --b) {
-          const int n = cursor[b];
-          cursor[b] = acc;
-          acc += n;
-        }
-        cursor[0] = acc;                                // partial partitions in all
-      }
-      __syncwarp();
-#pragma unroll
-      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
-        if (it * 32 >= p.num_seqs) break;
-        const int b = tail_tiles(it * 32 + lane, lens[it]);
-        const unsigned same = __match_any_sync(0xffffffffu, b);
-        const int base = b > 0 ? cursor[b] : 0;
-        if (b > 0) porder[base + __popc(same & ((1u << lane) - 1u))] = static_cast<uint16_t>(it * 32 + lane);
-        __syncwarp();
-        if (b > 0 && lane == __ffs(same) - 1) cursor[b] = base + __popc(same);
-        __syncwarp();
-      }
-      total = (whole_units + cursor[0]) * p.kv_slices;
-      __syncwarp();
-    }
+    const int total = compact ? (whole_units + partial_units) * p.kv_slices : p.total_units;
     const int ahead = kMma ? kClaimAheadTilesMma : kClaimAheadTiles;
     bool ok = true;
     int staged = 0;                           // tiles of the units staged so far
