@@ -359,7 +359,7 @@ def run_ours(args, rank, world, local_rank):
     knew, vnew = host["k"].to(dev), host["v"].to(dev)
     out = torch.empty_like(q)
     out_host = torch.empty(out.shape, dtype=tdt).pin_memory()
-    ws = pk.decode_workspace(S, H, D, width, B, pt, dev)
+    ws = pk.decode_workspace(S, H, Hkv, D, width, B, pt, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     seq_ids = np.arange(S, dtype=np.int64)
     d_tab = torch.empty((S, width), dtype=torch.int32, device=dev)
@@ -513,7 +513,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": dtype_name, "data": "synthetic",
         "config": {"workload": f"{args.config}_decode", "num_seqs": S, "num_heads": H,
                    "num_kv_heads": Hkv, "head_size": D, "block_size": B, "layers": layers,
-                   "context_tokens_first_step": int(L0.sum()), "partition_tokens": pk.pkv_decode_partition_tokens(width, B, pt),
+                   "context_tokens_first_step": int(L0.sum()), "partition_tokens": pk.pkv_decode_partition_tokens(S, H, Hkv, D, width, B, pt),
                    "num_blocks": num_blocks, "seed": args.seed,
                    "l2": "inputs larger than L2 (each step reads every layer's pool)",
                    "values": ("drawn on the device (torch generator)"

@@ -71,11 +71,10 @@ const char* pkv_version(void);
  * h / (num_heads / num_kv_heads).
  *
  * The context is processed in partitions of `partition_tokens` tokens (0 picks
- * 512, or 1024 when max_blocks_per_seq * block_size >= 32768, see
- * pkv_decode_partition_tokens; otherwise a positive multiple of 32, at most
- * 4096): each (sequence, KV head, partition) produces an unnormalised partial,
- * and a second kernel merges the partials of each (sequence, head) with the
- * global denominator.
+ * a default, see pkv_decode_partition_tokens; otherwise a positive multiple of
+ * 32, at most 4096): each (sequence, KV head, partition) produces an
+ * unnormalised partial, and a second kernel merges the partials of each
+ * (sequence, head) with the global denominator.
  *
  *   out          device, [num_seqs][num_heads][head_size] of out_dtype (F16, BF16 or F32)
  *   q            device, [num_seqs][num_heads][head_size] of kv_dtype
@@ -96,13 +95,19 @@ const char* pkv_version(void);
  * q, out, k_cache and v_cache must be 16-byte aligned.
  * Errors: PKV_EINVAL (shape/dtype/alignment), PKV_EWORKSPACE, PKV_ECUDA.
  * ------------------------------------------------------------------------ */
-size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_size,
+/* Workspace bytes of a decode call with these arguments (the call's own
+ * shape arguments); 0 for a shape no call accepts. */
+size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                                  int max_blocks_per_seq, int block_size, int partition_tokens);
 
 /* The partition size a decode call with these arguments uses: partition_tokens
- * itself when nonzero, else 512, or 1024 when the tables can hold 32768 tokens
- * or more (long contexts then produce half as many partials). Never fails. */
-int pkv_decode_partition_tokens(int max_blocks_per_seq, int block_size, int partition_tokens);
+ * itself when nonzero. Otherwise 1024 for query groups of 2 to 16 heads per KV
+ * head (block_size >= 8) when num_seqs * num_kv_heads * ceil(max context /
+ * 1024) >= 1024 (enough units to keep every SM busy, each with twice the keys
+ * per merge); else 512, or 1024 when the tables can hold 32768 tokens or more
+ * (long contexts then produce half as many partials). Never fails. */
+int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                int max_blocks_per_seq, int block_size, int partition_tokens);
 
 pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
                                       const void* k_cache, const void* v_cache, int kv_dtype,
@@ -126,7 +131,7 @@ pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
  * library keeps until the process exits. It allocates nothing.
  *
  *  - Limit: PKV_EWORKSPACE (nothing launched) when
- *    pkv_decode_workspace_size(num_seqs, num_heads, head_size,
+ *    pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size,
  *    max_blocks_per_seq, block_size, partition_tokens) > PKV_NOALLOC_SCRATCH_BYTES.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current; host code cannot name device memory

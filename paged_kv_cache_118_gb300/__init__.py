@@ -33,8 +33,8 @@ _c_int, _c_i64, _c_sz, _c_f, _vp = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_
 SIGNATURES = {
     "pkv_status_string": (ctypes.c_char_p, [_c_int]),
     "pkv_version": (ctypes.c_char_p, []),
-    "pkv_decode_workspace_size": (_c_sz, [_c_int] * 6),
-    "pkv_decode_partition_tokens": (_c_int, [_c_int] * 3),
+    "pkv_decode_workspace_size": (_c_sz, [_c_int] * 7),
+    "pkv_decode_partition_tokens": (_c_int, [_c_int] * 7),
     "pkv_paged_attention_decode": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                             _c_int, _c_f, _c_int, _vp, _c_sz, _vp, _vp]),
@@ -214,24 +214,26 @@ def _check_decode(where: str, out, q, k_cache, v_cache, block_tables, context_le
 
 # ---------------------------------------------------------------- kernels
 
-def pkv_decode_partition_tokens(max_blocks_per_seq: int, block_size: int,
+def pkv_decode_partition_tokens(num_seqs: int, num_heads: int, num_kv_heads: int,
+                                head_size: int, max_blocks_per_seq: int, block_size: int,
                                 partition_tokens: int = 0) -> int:
     """The partition size a decode call with these arguments uses (0 = the default)."""
-    return int(lib.pkv_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens))
+    return int(lib.pkv_decode_partition_tokens(num_seqs, num_heads, num_kv_heads, head_size,
+                                               max_blocks_per_seq, block_size, partition_tokens))
 
 
-def pkv_decode_workspace_size(num_seqs: int, num_heads: int, head_size: int,
-                              max_blocks_per_seq: int, block_size: int,
+def pkv_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,
+                              head_size: int, max_blocks_per_seq: int, block_size: int,
                               partition_tokens: int = 0) -> int:
-    return int(lib.pkv_decode_workspace_size(num_seqs, num_heads, head_size,
+    return int(lib.pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size,
                                              max_blocks_per_seq, block_size, partition_tokens))
 
 
-def decode_workspace(num_seqs, num_heads, head_size, max_blocks_per_seq, block_size,
-                     partition_tokens=0, device="cuda") -> torch.Tensor:
+def decode_workspace(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq,
+                     block_size, partition_tokens=0, device="cuda") -> torch.Tensor:
     """A caller-owned scratch buffer of the size the decode call needs."""
-    n = pkv_decode_workspace_size(num_seqs, num_heads, head_size, max_blocks_per_seq,
-                                  block_size, partition_tokens)
+    n = pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size,
+                                  max_blocks_per_seq, block_size, partition_tokens)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 

@@ -80,11 +80,12 @@ class PagedKVCache:
 
     def workspace(self, num_seqs, num_heads, max_blocks, partition_tokens=0) -> torch.Tensor:
         from . import pkv_decode_workspace_size
-        need = pkv_decode_workspace_size(num_seqs, num_heads, self.head_size, max_blocks,
-                                         self.block_size, partition_tokens)
+        need = pkv_decode_workspace_size(num_seqs, num_heads, self.num_kv_heads, self.head_size,
+                                         max_blocks, self.block_size, partition_tokens)
         if self._ws is None or self._ws.numel() < need:
-            self._ws = decode_workspace(num_seqs, num_heads, self.head_size, max_blocks,
-                                        self.block_size, partition_tokens, self.device)
+            self._ws = decode_workspace(num_seqs, num_heads, self.num_kv_heads, self.head_size,
+                                        max_blocks, self.block_size, partition_tokens,
+                                        self.device)
         return self._ws
 
     def attend(self, q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,

@@ -34,16 +34,37 @@ def test_status_strings_and_version():
     assert b"sm_103a" in pk.lib.pkv_version()
 
 
+def _default_partition(S, H, Hkv, D, mb, B):
+    """The default partition as the header states it: 1024 tokens for query
+    groups of 2 to 16 heads per KV head (B >= 8) when S * Hkv * ceil(max/1024)
+    >= 1024; else 512, or 1024 for tables of 32768 tokens or more."""
+    group = H // Hkv
+    warp_tensor = 2 <= group and B >= 8 and not (group >= 32 and 128 % group == 0)
+    if warp_tensor and S * Hkv * -(-(mb * B) // 1024) >= 1024:
+        return 1024
+    return 1024 if mb * B >= 32768 else 512
+
+
 def test_workspace_size_formula():
     # rows = S * H * ceil(max_blocks * B / partition); each row holds D floats and an
     # (m, l) pair (the pairs padded to 16 bytes), then a 16-byte work counter
-    for S, H, D, mb, B, pt in [(64, 40, 128, 128, 16, 512), (8, 32, 128, 8192, 16, 512),
-                               (3, 4, 64, 5, 4, 32), (1, 1, 64, 1, 8, 0), (8, 32, 128, 8192, 16, 0)]:
-        eff = pt or (1024 if mb * B >= 32768 else 512)
-        assert pk.pkv_decode_partition_tokens(mb, B, pt) == eff
+    for S, H, Hkv, D, mb, B, pt in [(64, 40, 40, 128, 128, 16, 512), (8, 32, 8, 128, 8192, 16, 512),
+                                    (3, 4, 4, 64, 5, 4, 32), (1, 1, 1, 64, 1, 8, 0),
+                                    (8, 32, 8, 128, 8192, 16, 0), (64, 40, 40, 128, 128, 16, 0),
+                                    (256, 32, 8, 128, 98, 16, 0), (16, 32, 8, 128, 98, 16, 0),
+                                    (128, 64, 1, 128, 256, 16, 0), (256, 32, 8, 128, 98, 4, 0)]:
+        eff = pt or _default_partition(S, H, Hkv, D, mb, B)
+        assert pk.pkv_decode_partition_tokens(S, H, Hkv, D, mb, B, pt) == eff
         parts = -(-(mb * B) // eff)
         rows = S * H * parts
-        assert pk.pkv_decode_workspace_size(S, H, D, mb, B, pt) == rows * D * 4 + -(-rows * 8 // 16) * 16 + 16
+        assert (pk.pkv_decode_workspace_size(S, H, Hkv, D, mb, B, pt)
+                == rows * D * 4 + -(-rows * 8 // 16) * 16 + 16)
+    # the shared-prefix batch (256 beams, 32/8 heads) takes 1024-token partitions,
+    # the same heads over 16 sequences 512, MHA 512
+    assert pk.pkv_decode_partition_tokens(256, 32, 8, 128, 98, 16, 0) == 1024
+    assert pk.pkv_decode_partition_tokens(16, 32, 8, 128, 98, 16, 0) == 512
+    assert pk.pkv_decode_partition_tokens(64, 40, 40, 128, 128, 16, 0) == 512
+    assert pk.pkv_decode_workspace_size(4, 8, 0, 128, 10, 16, 0) == 0
 
 
 def _decode_status(**over):

@@ -293,7 +293,7 @@ def test_shared_prefix_runs(case):
     for tab, k, v in ((tables, kc, vc), (ptab, pk_, pv_)):
         out = torch.empty(q.shape, dtype=TORCH_DTYPE[dt], device="cuda")
         tt = torch.from_numpy(tab).cuda()
-        ws = pk.decode_workspace(len(lens), H, D, tab.shape[1], B, pt)
+        ws = pk.decode_workspace(len(lens), H, Hkv, D, tab.shape[1], B, pt)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         pk.pkv_paged_attention_decode(out, dev(q, dt), dev(k, dt), dev(v, dt), tt,
                                       torch.from_numpy(lens).cuda(), B, float(scale), ws,

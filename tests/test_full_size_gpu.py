@@ -154,7 +154,8 @@ def test_longctx_full(partition_tokens):
     order = free_order(n, 0)
     cache, tables, ctx = gpu_decode_state(batch, n, order, poison=True)
     _tables_match_oracle(batch, n, order, tables)
-    pt = pk.pkv_decode_partition_tokens(tables.shape[1], 16, partition_tokens)
+    pt = pk.pkv_decode_partition_tokens(batch.num_seqs, 32, 8, 128, tables.shape[1], 16,
+                                        partition_tokens)
     assert pt == (1024 if partition_tokens == 0 else 512)
     if pt == 512:
         parts = sum(-(-int(L) // 512) for L in batch.context_lens)

@@ -54,7 +54,7 @@ def test_matches_workspace_entry_point_twice_in_a_row():
     for lens, H, Hkv, B, dt, seed in cases:
         batch, cache, tables, ctx = _case(lens, H, Hkv, B, dt, seed)
         q = dev(batch.q, dt)
-        need = pk.pkv_decode_workspace_size(batch.num_seqs, H, 128, tables.shape[1], B)
+        need = pk.pkv_decode_workspace_size(batch.num_seqs, H, Hkv, 128, tables.shape[1], B)
         assert need <= pk.NOALLOC_SCRATCH_BYTES
         want = cache.attend(q, tables, ctx, float(batch.scale)).clone()
         runs.append((batch, cache, tables, ctx, q, want, dt))
@@ -78,10 +78,10 @@ def test_refuses_batches_beyond_the_built_in_scratch():
     # in partitions of the default size for so wide a table (1024 tokens)
     parts = pk.NOALLOC_SCRATCH_BYTES // (8 * (128 * 4 + 8)) + 1
     width = parts * 1024 // 16
-    assert pk.pkv_decode_partition_tokens(width, 16) == 1024
+    assert pk.pkv_decode_partition_tokens(1, 8, 8, 128, width, 16) == 1024
     wide = torch.full((1, width), -1, dtype=torch.int32, device="cuda")
     wide[0, :tables.shape[1]] = tables[0]
-    assert pk.pkv_decode_workspace_size(1, 8, 128, width, 16) > pk.NOALLOC_SCRATCH_BYTES
+    assert pk.pkv_decode_workspace_size(1, 8, 8, 128, width, 16) > pk.NOALLOC_SCRATCH_BYTES
     assert _noalloc(out, q, cache, wide, ctx, batch.scale) == pk.PKV_EWORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 0)
