@@ -472,28 +472,35 @@ struct MmaState {
 // CTA's threads: per chunk of 32 sequences (one warp each, every load in
 // flight at once) the claims of whole partitions, the group info and the tile
 // count of the partial last partition; then the prefix sums over the chunks,
-// and a counting sort of the partial partitions by tile count, largest first
-// (the order among equal counts is whatever the shared-memory atomics give:
-// it decides which CTA serves a unit, not any result). `scratch` is shared
-// memory that no copy has reached yet (the ring); a proxy fence hands it back
-// to the TMA copies. Ends with a block-wide barrier.
+// and a stable counting sort of the partial partitions by tile count, largest
+// first, equal counts in sequence order. Every CTA builds the list on its own
+// and claims index into it, so it must come out the same in every CTA: no
+// step depends on the order of concurrent events. `scratch` is shared memory
+// that no copy has reached yet (the ring); a proxy fence hands it back to the
+// TMA copies. Ends with a block-wide barrier.
 __device__ __forceinline__ void build_work_list(const DecodeParams& p, int max_ctx, bool grouping,
                                                 int cap, int* scratch, int* pref, uint16_t* ginfo,
                                                 uint16_t* porder, int& whole_units,
                                                 int& partial_units) {
   constexpr int kWarps = kThreads / 32;
-  constexpr int kChunksPerWarp = (kCompactMaxSeqs / 32 + kWarps - 1) / kWarps;
+  constexpr int kChunks = kCompactMaxSeqs / 32;
+  constexpr int kChunksPerWarp = (kChunks + kWarps - 1) / kWarps;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = p.num_seqs;
   const int nchunks = (n + 31) / 32;
   const int PT = p.partition_tokens;
   const int nbk = PT / kTile;                          // tile counts of partial partitions: 1 .. nbk
-  int* chunk_sum = scratch;                            // [32]: claims per chunk, then offsets
-  int* totals = scratch + 32;                          // [2]: whole claims, partial partitions
-  int* cursor = scratch + 40;                          // [nbk + 1]: counts, then places
-  uint8_t* tiles_of = reinterpret_cast<uint8_t*>(scratch + 48 + nbk);   // [n] (0: no partial)
-  for (int i = tid; i <= nbk; i += kThreads) cursor[i] = 0;
-  __syncthreads();
+  // scratch: claims per chunk, then their offsets [32]; totals [2]; per tile
+  // count its first place [nbk + 1]; per (tile count, chunk) the count, then
+  // the place of the chunk's first one [(nbk + 1) * 32]; per sequence its
+  // tile count and its rank among the chunk's equal counts [n] bytes each
+  int* chunk_sum = scratch;
+  int* totals = scratch + 32;
+  int* base = scratch + 40;
+  int* cnt = base + (nbk + 1);
+  uint8_t* tiles_of = reinterpret_cast<uint8_t*>(cnt + (nbk + 1) * kChunks);
+  uint8_t* rank_of = tiles_of + kCompactMaxSeqs;
+  for (int i = tid; i < (nbk + 1) * kChunks; i += kThreads) cnt[i] = 0;
   int L[kChunksPerWarp], fb[kChunksPerWarp];
 #pragma unroll
   for (int j = 0; j < kChunksPerWarp; ++j) {          // every load of this warp in flight at once
@@ -501,6 +508,7 @@ __device__ __forceinline__ void build_work_list(const DecodeParams& p, int max_c
     L[j] = s < n ? __ldg(p.context_lens + s) : 0;
     fb[j] = (grouping && s < n) ? __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq) : -1;
   }
+  __syncthreads();                                     // cnt is zero
 #pragma unroll
   for (int j = 0; j < kChunksPerWarp; ++j) {
     const int ch = warp + j * kWarps;
@@ -542,13 +550,19 @@ __device__ __forceinline__ void build_work_list(const DecodeParams& p, int max_c
     }
     if (s < n) pref[s + 1] = x;
     if (lane == 31) chunk_sum[ch] = x;
+    // the partial partition's tile count, and its rank among the chunk's
+    // sequences with the same count (in lane order)
     const int r = valid ? L[j] % PT : 0;
-    const int t = (r + kTile - 1) / kTile;
-    if (s < n) tiles_of[s] = static_cast<uint8_t>(t);     // t <= nbk <= 128
-    if (t > 0) atomicAdd(&cursor[t], 1);
+    const int t = (r + kTile - 1) / kTile;           // 0: none; at most nbk <= 128
+    const unsigned same = __match_any_sync(0xffffffffu, t);
+    if (s < n) {
+      tiles_of[s] = static_cast<uint8_t>(t);
+      rank_of[s] = static_cast<uint8_t>(__popc(same & ((1u << lane) - 1u)));
+    }
+    if (t > 0 && lane == __ffs(same) - 1) cnt[t * kChunks + ch] = __popc(same);
   }
   __syncthreads();
-  if (warp == 0) {                                     // chunk offsets (exclusive)
+  if (warp == 0) {                                     // chunk offsets of the claims (exclusive)
     const int v = lane < nchunks ? chunk_sum[lane] : 0;
     int x = v;
 #pragma unroll
@@ -558,18 +572,31 @@ __device__ __forceinline__ void build_work_list(const DecodeParams& p, int max_c
     }
     if (lane < nchunks) chunk_sum[lane] = x - v;
     if (lane == 31) totals[0] = x;
-  } else if (warp == 1) {                              // places of the tile counts, largest first
+  }
+  // per tile count: its chunks' counts become places within the count
+  for (int b = 1 + tid; b <= nbk; b += kThreads) {
+    int acc = 0;
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int v = cnt[b * kChunks + ch];
+      cnt[b * kChunks + ch] = acc;
+      acc += v;
+    }
+    base[b] = acc;                                     // total of this count, for now
+  }
+  __syncthreads();
+  if (warp == 0) {                                     // first place of each count, largest first
     int carry = 0;
     for (int top = nbk; top >= 1; top -= 32) {
       const int b = top - lane;
-      const int v = b >= 1 ? cursor[b] : 0;
+      const int v = b >= 1 ? base[b] : 0;
       int x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      if (b >= 1) cursor[b] = carry + x - v;
+      __syncwarp();
+      if (b >= 1) base[b] = carry + x - v;
       carry += __shfl_sync(0xffffffffu, x, 31);
     }
     if (lane == 0) totals[1] = carry;
@@ -578,7 +605,7 @@ __device__ __forceinline__ void build_work_list(const DecodeParams& p, int max_c
   for (int s = tid; s < n; s += kThreads) {
     pref[s + 1] += chunk_sum[s >> 5];
     const int t = tiles_of[s];
-    if (t > 0) porder[atomicAdd(&cursor[t], 1)] = static_cast<uint16_t>(s);
+    if (t > 0) porder[base[t] + cnt[t * kChunks + (s >> 5)] + rank_of[s]] = static_cast<uint16_t>(s);
   }
   if (tid == 0) pref[0] = 0;
   whole_units = totals[0];

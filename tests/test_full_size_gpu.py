@@ -47,11 +47,16 @@ def _tables_match_oracle(batch, n, order, tables):
 
 
 def _check_all(name, cache, q, tables, ctx, scale, want, dtype, partition_tokens=0):
-    """Both output types of one decode call against the oracle, every element."""
+    """Both output types of one decode call against the oracle, every element;
+    and the same call again, bit for bit (every CTA must derive the same work
+    list, whatever order its threads run in)."""
     out = cache.attend(q, tables, ctx, scale, partition_tokens=partition_tokens)
     out32 = torch.empty(out.shape, dtype=torch.float32, device="cuda")
     cache.attend(q, tables, ctx, scale, out=out32, partition_tokens=partition_tokens)
+    again = torch.empty_like(out32)
+    cache.attend(q, tables, ctx, scale, out=again, partition_tokens=partition_tokens)
     torch.cuda.synchronize()
+    assert torch.equal(again, out32)
     record_max_err(f"{name} ({dtype} out)", assert_close(out, want, dtype))
     record_max_err(f"{name} (fp32 out)", assert_close(out32, want, dtype))
     assert cache.err.item() == 0
