@@ -123,6 +123,17 @@ def profile_traffic(config: str, bytes_per_launch: float):
     return round(float(t.group(1)) * bytes_per_launch / float(a.group(1)))
 
 
+def profile_key(args, B, pt):
+    """Name of the ncu summary of a workload (profiles/decode_partition_<key>.md):
+    the block size for the LLaMA-shaped sweep, the partition size for the
+    long-context batch."""
+    if args.config == "llama13b":
+        return f"llama13b_b{B}"
+    if args.config == "longctx":
+        return f"longctx_p{pt}"
+    return args.config
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
 
@@ -295,6 +306,10 @@ def setup_pools(args, rank, dev, layers, total_steps):
                     beams=beams)
     else:
         lens, H, Hkv, D, B, dname = workload_shape(args.config, seed, args.block_size)
+        if getattr(args, "seqs", 0):
+            if not getattr(args, "device_values", False):
+                raise SystemExit("--seqs needs --device-values")
+            lens = lens[:args.seqs]
         S = len(lens)
         tdt = torch.float16 if dname == "f16" else torch.bfloat16
         L0 = lens.astype(np.int64)                          # context at the first step
@@ -504,8 +519,8 @@ def run_ours(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2)}
 
     peak, peak_kind = load_peaks()
-    traffic = profile_traffic(getattr(args, "profile_key", None) or args.config,
-                              float(np.mean(per_call)))
+    traffic = profile_traffic(profile_key(args, B, pk.pkv_decode_partition_tokens(
+        S, H, Hkv, D, width, B, pt)), float(np.mean(per_call)))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
@@ -515,6 +530,7 @@ def run_ours(args, rank, world, local_rank):
                    "num_kv_heads": Hkv, "head_size": D, "block_size": B, "layers": layers,
                    "context_tokens_first_step": int(L0.sum()), "partition_tokens": pk.pkv_decode_partition_tokens(S, H, Hkv, D, width, B, pt),
                    "num_blocks": num_blocks, "seed": args.seed,
+                   **({"first_seqs": args.seqs} if getattr(args, "seqs", 0) else {}),
                    "l2": "inputs larger than L2 (each step reads every layer's pool)",
                    "values": ("drawn on the device (torch generator)"
                               if getattr(args, "device_values", False) else
@@ -864,7 +880,7 @@ def run_per_config(args, cpu):
         sub = argparse.Namespace(**vars(args))
         sub.config, sub.block_size, sub.partition_tokens, sub.layers = cfg, bs, pt, layers
         sub.steps, sub.warmup = args.per_config_steps, 3
-        sub.device_values, sub.profile_key = True, key
+        sub.device_values = True
         try:
             line = _summary(run_ours(sub, 0, 1, 0))
             line["cpu_baseline"] = cpu.get(key)
@@ -912,6 +928,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--block-size", type=int, default=0,
                     help="block size of the workload (0: its own, 16); llama13b sweeps 8..128")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="only the first N sequences of the batch (smaller profiling cases)")
     ap.add_argument("--device-values", action="store_true",
                     help="draw the cached keys/values on the device (as the per-config runs do)")
     ap.add_argument("--no-per-config", action="store_true",
@@ -949,7 +967,7 @@ def main():
 
     per_config = (world == 1 and not args.no_per_config and args.config == "opt13b"
                   and args.block_size in (0, 16) and args.partition_tokens == 0
-                  and args.layers == 0)
+                  and args.layers == 0 and args.seqs == 0)
     cpu = None
     cpu_per = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
