@@ -722,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
     int staged = 0;                           // tiles of the units staged so far
     // runs of the last group claim still to be staged
     unsigned pend = 0, plink = 0;
+    bool claimed = false;                     // the first unit is the CTA's index
     int pseq = 0, ppart = 0, pkvs = 0, pLm = 0, pgs = 0;
     for (int k = 0;; ++k) {
       if (k >= 1) {                           // wait until the staged backlog runs low
@@ -780,9 +781,13 @@ __global__ void __launch_bounds__(kThreads, (GS >= 2 || kMma) ? 2 : 3)
         staged += p.partition_tokens / kTile;
       } else {
         while (true) {
-          int u = 0;
-          if (lane == 0) u = atomicAdd(p.counter, 1);
-          u = __shfl_sync(0xffffffffu, u, 0);
+          // the CTA's own index first (no round trip), then the shared counter
+          int u = static_cast<int>(blockIdx.x);
+          if (claimed) {
+            if (lane == 0) u = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+          }
+          claimed = true;
           if (u >= total) break;
           int part, seq, kvs;
           int F = 0, gs = 1;
@@ -1442,25 +1447,29 @@ static cudaError_t launch_reduce(void* out, int out_dtype, const ReduceParams& r
 
 using namespace pkv;
 
-// The partition size a call uses. 0 picks 1024 tokens on the warp-level
-// tensor path (query groups of 2 to 16 heads) when the batch has at least
-// kBigPartitionUnits (sequence, KV head, 1024-token partition) units, which
-// keeps every SM busy: each unit then carries twice the keys for one merge,
-// one partial and one claim (measured: 0.82 against 0.80 of the HBM copy rate
-// on the 256-beam shared-prefix batch, 0.99 against 0.95 on the long-context
-// one). Otherwise 512, or 1024 when the tables can hold 32K tokens or more.
+// The partition size a call uses. 0 picks 1024 tokens on the tensor paths
+// when the batch has enough (sequence, KV head, 1024-token partition) units to
+// keep every SM busy: kBigPartitionUnits on the warp-level path (query groups
+// of 2 to 16 heads; two CTAs per SM), kBigPartitionUnitsTc on the tcgen05 path
+// (groups of 32 or more; one CTA per SM). Each unit then carries twice the keys
+// for one merge, one partial and one claim. Measured, fraction of the HBM copy
+// rate: 0.82 against 0.80 on the 256-beam shared-prefix batch, 0.99 against
+// 0.95 on the long-context one, 0.42 against 0.38 with 64 query heads on one KV
+// head. Otherwise 512, or 1024 when the tables can hold 32K tokens or more.
 constexpr int64_t kBigPartitionUnits = 1024;
+constexpr int64_t kBigPartitionUnitsTc = 256;
 static int effective_partition(int partition_tokens, int num_seqs, int num_heads,
                                int num_kv_heads, int head_size, int max_blocks_per_seq,
                                int block_size) {
   if (partition_tokens != 0) return partition_tokens;
   const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * block_size;
   const int group = num_kv_heads >= 1 ? num_heads / num_kv_heads : 1;
+  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 1023) / 1024);
+  if (group >= 2 && decode_tc_supported(group, head_size, block_size, 1024))
+    return units >= kBigPartitionUnitsTc ? 1024 : (max_ctx >= 32768 ? 1024 : 512);
   const bool warp_tensor = group >= 2 && block_size >= 8 &&
                            !decode_tc_supported(group, head_size, block_size, 512);
-  if (warp_tensor && static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 1023) / 1024) >=
-                         kBigPartitionUnits)
-    return 1024;
+  if (warp_tensor && units >= kBigPartitionUnits) return 1024;
   return max_ctx >= 32768 ? 1024 : 512;
 }
 

@@ -14,11 +14,12 @@
 // product, and each K/V byte is read once.
 //
 // How (persistent CTAs, one per SM, 256 threads):
-//  * warp 0 claims units (sequence, partition, KV head) from a global counter.
-//    Up to 1024 sequences, only units that exist are numbered: every whole
-//    partition first, then the partial last ones, which fill the end of the
-//    run (prefix sums per sequence); larger batches number them all and skip
-//    the empty ones. Per unit it reads the partition's block ids (one per lane),
+//  * all warps first build the call's work list: up to 1024 sequences, only
+//    units (sequence, partition, KV head) that exist are numbered, every whole
+//    partition first, then the partial last ones largest first, so that the
+//    run ends with its shortest units; larger batches number them all and skip
+//    the empty ones. Warp 0 then takes units: its CTA's index first, then
+//    claims from a global counter. Per unit it reads the partition's block ids (one per lane),
 //    loads the G query rows by TMA into a staging buffer and streams
 //    the partition's 64-key K/V tiles into a ring of 4 to 6 stages (as many
 //    as shared memory holds beside the rest), one TMA copy per
@@ -100,7 +101,8 @@ struct UnitInfo {
 //  a warp writing its rows meets no bank conflict), then the rows' (m, l):
 //  with two copies every row passes the half of D its partner writes; with
 //  four the rows of copies 1-3 pass half of D per round to copy 0;
-//  then the barriers, the unit slots and the work list.
+//  then the barriers, the unit slots and the work list (the Q staging buffer
+//  serves as scratch while the list is built, before the first query copy).
 // The ring takes as many stages (up to kMaxStages) as the rest leaves room for.
 template <int D, int C>
 struct Layout {
@@ -121,7 +123,8 @@ struct Layout {
   // mrg_full, mrg_free
   static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 3) * 8 +
                                     2 * static_cast<int>(sizeof(UnitInfo)) + kMaxIds * 4 +
-                                    2 * (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 4 + 16;
+                                    (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 2 +
+                                    kCompactMaxSeqs * 4 + 16;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kOffStages - kMergeBytes - kTailBytes - 16) / kStageBytes;
   static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
@@ -130,13 +133,125 @@ struct Layout {
   static constexpr int kNumBars = 2 * kStages + 2 * 8 + 3;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;
   static constexpr int kOffIds = kOffUnits + 2 * static_cast<int>(sizeof(UnitInfo));
-  static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions
-  static constexpr int kOffTail = kOffPref + (kCompactMaxSeqs + 4) * 4;   // last, partial ones
-  static constexpr int kOffLens = kOffTail + (kCompactMaxSeqs + 4) * 4;
+  static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions per sequence
+  static constexpr int kOffOrder = kOffPref + (kCompactMaxSeqs + 4) * 4;  // partial ones, largest first
+  static constexpr int kOffLens = kOffOrder + kCompactMaxSeqs * 2;
   static constexpr int kOffTmem = kOffLens + kCompactMaxSeqs * 4;
   static constexpr int kSmem = 1024 + kOffTmem + 16;
   static_assert(kStages >= 3 && kSmem <= kSmemLimit, "shared memory of one CTA");
 };
+
+// Builds the compact work list with all the CTA's threads (every CTA builds
+// the same list: claims index into it, so no step may depend on the order of
+// concurrent events): per sequence its length, the prefix of whole
+// partitions, and the sequences with a partial last partition in a stable
+// counting sort by tile count, largest first. `scratch` is the Q staging
+// buffer, before any query copy reaches it; a proxy fence hands it back.
+// Ends with a block-wide barrier.
+__device__ __forceinline__ void build_list(const Params& p, int max_ctx, int* scratch, int* pref,
+                                           uint16_t* porder, int* lens, int& whole_units,
+                                           int& partial_units) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kChunks = kCompactMaxSeqs / 32;
+  constexpr int kChunksPerWarp = (kChunks + kWarps - 1) / kWarps;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = p.num_seqs;
+  const int nchunks = (n + 31) / 32;
+  const int PT = p.partition_tokens;
+  const int nbk = PT / kKeys;                          // tile counts 1 .. nbk <= 64
+  int* chunk_sum = scratch;                            // [32]
+  int* totals = scratch + 32;                          // [2]
+  int* base = scratch + 40;                            // [nbk + 1]
+  int* cnt = base + (nbk + 1);                         // [(nbk + 1) * 32]
+  uint8_t* tiles_of = reinterpret_cast<uint8_t*>(cnt + (nbk + 1) * kChunks);
+  uint8_t* rank_of = tiles_of + kCompactMaxSeqs;
+  for (int i = tid; i < (nbk + 1) * kChunks; i += kThreads) cnt[i] = 0;
+  int Ls[kChunksPerWarp];
+#pragma unroll
+  for (int j = 0; j < kChunksPerWarp; ++j) {          // every load of this warp in flight at once
+    const int s = (warp + j * kWarps) * 32 + lane;
+    Ls[j] = s < n ? __ldg(p.context_lens + s) : 0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kChunksPerWarp; ++j) {
+    const int ch = warp + j * kWarps;
+    if (ch >= nchunks) break;
+    const int s = ch * 32 + lane;
+    const int L = Ls[j];
+    const bool valid = s < n && L >= 1 && L <= max_ctx;
+    if (s < n && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+    int x = valid ? L / PT : 0;                        // whole partitions
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (s < n) {
+      pref[s + 1] = x;
+      lens[s] = L;
+    }
+    if (lane == 31) chunk_sum[ch] = x;
+    const int r = valid ? L % PT : 0;
+    const int t = (r + kKeys - 1) / kKeys;
+    const unsigned same = __match_any_sync(0xffffffffu, t);
+    if (s < n) {
+      tiles_of[s] = static_cast<uint8_t>(t);
+      rank_of[s] = static_cast<uint8_t>(__popc(same & ((1u << lane) - 1u)));
+    }
+    if (t > 0 && lane == __ffs(same) - 1) cnt[t * kChunks + ch] = __popc(same);
+  }
+  __syncthreads();
+  if (warp == 0) {                                     // chunk offsets of the whole partitions
+    const int v = lane < nchunks ? chunk_sum[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < nchunks) chunk_sum[lane] = x - v;
+    if (lane == 31) totals[0] = x;
+  }
+  for (int b = 1 + tid; b <= nbk; b += kThreads) {    // places within each tile count
+    int acc = 0;
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int v = cnt[b * kChunks + ch];
+      cnt[b * kChunks + ch] = acc;
+      acc += v;
+    }
+    base[b] = acc;
+  }
+  __syncthreads();
+  if (warp == 0) {                                     // first place of each count, largest first
+    int carry = 0;
+    for (int top = nbk; top >= 1; top -= 32) {
+      const int b = top - lane;
+      const int v = b >= 1 ? base[b] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      __syncwarp();
+      if (b >= 1) base[b] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) totals[1] = carry;
+  }
+  __syncthreads();
+  for (int s = tid; s < n; s += kThreads) {
+    pref[s + 1] += chunk_sum[s >> 5];
+    const int t = tiles_of[s];
+    if (t > 0) porder[base[t] + cnt[t * kChunks + (s >> 5)] + rank_of[s]] = static_cast<uint16_t>(s);
+  }
+  if (tid == 0) pref[0] = 0;
+  whole_units = totals[0];
+  partial_units = totals[1];
+  fence_proxy_async_smem();
+  __syncthreads();
+}
 
 // C: copies of the G = 128 / C query rows in the product's rows.
 template <int D, typename T, int C>
@@ -171,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + Lay::kOffUnits);
   int32_t* ids = reinterpret_cast<int32_t*>(smem + Lay::kOffIds);
   int32_t* pref = reinterpret_cast<int32_t*>(smem + Lay::kOffPref);
-  int32_t* tpref = reinterpret_cast<int32_t*>(smem + Lay::kOffTail);
+  uint16_t* porder = reinterpret_cast<uint16_t*>(smem + Lay::kOffOrder);
   int32_t* lens = reinterpret_cast<int32_t*>(smem + Lay::kOffLens);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
 
@@ -208,6 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const bool compact = p.num_seqs <= kCompactMaxSeqs;
+  int whole_units = 0, partial_units = 0;
+  if (compact)
+    build_list(p, max_ctx, reinterpret_cast<int*>(qstage), pref, porder, lens, whole_units,
+               partial_units);
 
   if (warp == 0) {
     // ---------------------------------------------------------- claims, copies
@@ -220,85 +340,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R = p.box_rows;
     const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
     const int Hkv = p.num_kv_heads;
-    // The work list. Batches of up to kCompactMaxSeqs sequences number only
-    // the units that exist: first every whole partition, sequence-major, then
-    // the partial last partitions, shorter on average, so that they fill the
-    // end of the run (prefix sums per sequence, then a binary search per
-    // claim). Larger batches number every (partition, sequence, KV head),
-    // partition-major, and skip the empty ones.
-    const bool compact = p.num_seqs <= kCompactMaxSeqs;
-    int total = p.total_units;
-    int whole_units = 0;
-    if (compact) {
-      int lv[kCompactMaxSeqs / 32];                        // all lengths in one round of loads
-#pragma unroll
-      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
-        const int sq = it * 32 + lane;
-        lv[it] = sq < p.num_seqs ? __ldg(p.context_lens + sq) : 0;
-      }
-      int carry = 0, tcarry = 0;
-#pragma unroll
-      for (int it = 0; it < kCompactMaxSeqs / 32; ++it) {
-        if (it * 32 >= p.num_seqs) break;
-        const int sq = it * 32 + lane;
-        const int L = lv[it];
-        const bool valid = sq < p.num_seqs && L >= 1 && L <= max_ctx;
-        if (sq < p.num_seqs && !valid && blockIdx.x == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-        int x = valid ? L / PT : 0;                        // whole partitions
-        int y = valid && L % PT != 0 ? 1 : 0;              // a partial last one
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int xo = __shfl_up_sync(0xffffffffu, x, o);
-          const int yo = __shfl_up_sync(0xffffffffu, y, o);
-          if (lane >= o) {
-            x += xo;
-            y += yo;
-          }
-        }
-        if (sq < p.num_seqs) {
-          pref[sq + 1] = carry + x;
-          tpref[sq + 1] = tcarry + y;
-          lens[sq] = L;
-        }
-        carry += __shfl_sync(0xffffffffu, x, 31);
-        tcarry += __shfl_sync(0xffffffffu, y, 31);
-      }
-      if (lane == 0) {
-        pref[0] = 0;
-        tpref[0] = 0;
-      }
-      whole_units = carry;
-      total = (carry + tcarry) * Hkv;
-      __syncwarp();
-    }
+    const int total = compact ? (whole_units + partial_units) * Hkv : p.total_units;
     int g = 0;                                             // tiles issued
     int k = 0;                                             // units published
     int last_issued[kStages];
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
     bool ok = true;
-    while (ok) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(p.counter, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
+    for (int claim = 0; ok; ++claim) {
+      // the CTA's own index first (no round trip), then the shared counter
+      int u = blockIdx.x;
+      if (claim > 0) {
+        if (lane == 0) u = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+      }
       UnitInfo info{-1, 0, 0, 0};
       int t_begin = 0, t_end = 0;
       if (u < total) {
         int seq, kvh, part, L;
         if (compact) {
-          int w = u / Hkv;
+          const int w = u / Hkv;
           kvh = u - w * Hkv;
-          const bool tail = w >= whole_units;
-          const int32_t* pf = tail ? tpref : pref;
-          if (tail) w -= whole_units;
-          int lo = 0, hi = p.num_seqs;                     // largest lo with pf[lo] <= w
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (pf[mid] <= w) lo = mid; else hi = mid;
+          if (w >= whole_units) {                          // a partial last partition
+            seq = porder[w - whole_units];
+            L = lens[seq];
+            part = L / PT;
+          } else {
+            int lo = 0, hi = p.num_seqs;                   // largest lo with pref[lo] <= w
+            while (hi - lo > 1) {
+              const int mid = (lo + hi) >> 1;
+              if (pref[mid] <= w) lo = mid; else hi = mid;
+            }
+            seq = lo;
+            L = lens[lo];
+            part = w - pref[lo];
           }
-          seq = lo;
-          L = lens[lo];
-          part = tail ? L / PT : w - pref[lo];
         } else {
           const int per_part = p.num_seqs * Hkv;
           part = u / per_part;
