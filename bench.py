@@ -385,6 +385,11 @@ def run_ours(args, rank, world, local_rank):
     ctx_log = []
     ev_pairs = []
 
+    # events of the timed region's decode calls, created up front (creating
+    # them inside the layer loop costs host time the GPU may wait for)
+    ev_pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps * layers)]
+
     def step(timed_kernels: bool, before=None, after=None):
         new_slots, cow = bm.append_slots(seq_ids)                       # host block manager
         tab, lens = bm.fill_tables(seq_ids, width)
@@ -400,8 +405,7 @@ def run_ours(args, rank, world, local_rank):
                 launches[0] += -(-len(cow) // 1024)
             pk.pkv_reshape_and_cache(knew[l], vnew[l], kc[l], vc[l], d_new, err)
             if timed_kernels:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
+                a, b = ev_pool[len(ev_pairs)]
                 a.record(stream)
             pk.pkv_paged_attention_decode(out[l], q[l], kc[l], vc[l], d_tab, d_lens, B,
                                           scale, ws, pt, err)

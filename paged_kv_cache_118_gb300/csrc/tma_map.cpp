@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "pkv_host.h"
 
@@ -25,8 +26,47 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Recently encoded maps, keyed by every argument of the encoding (a map is a
+// pure function of them): a decode loop passes the same caches call after
+// call, and the encoder costs a few microseconds of host time per map.
+namespace {
+struct MapKey {
+  const void* base;
+  int64_t extent;                      // slots (caches) or rows (queries)
+  int d, heads, box, view;             // view -1: a query map
+  bool operator==(const MapKey& o) const {
+    return base == o.base && extent == o.extent && d == o.d && heads == o.heads &&
+           box == o.box && view == o.view;
+  }
+};
+constexpr int kMapCache = 32;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+CUtensorMap g_map_val[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+bool cached_map(const MapKey& k, CUtensorMap* out) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < g_map_used; ++i)
+    if (g_map_key[i] == k) {
+      *out = g_map_val[i];
+      return true;
+    }
+  return false;
+}
+
+void remember_map(const MapKey& k, const CUtensorMap& m) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  const int i = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+  g_map_key[i] = k;
+  g_map_val[i] = m;
+}
+}  // namespace
+
 bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads,
                              int64_t slots, int box_rows, CacheView view) {
+  const MapKey key{base, slots, D, num_kv_heads, box_rows, static_cast<int>(view)};
+  if (cached_map(key, tm)) return true;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   CUresult r;
@@ -58,10 +98,14 @@ bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  remember_map(key, *tm);
+  return true;
 }
 
 bool encode_query_map(CUtensorMap* tm, const void* base, int D, int64_t rows, int box_rows) {
+  const MapKey key{base, rows, D, 0, box_rows, -1};
+  if (cached_map(key, tm)) return true;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(rows)};
@@ -72,7 +116,9 @@ bool encode_query_map(CUtensorMap* tm, const void* base, int D, int64_t rows, in
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  remember_map(key, *tm);
+  return true;
 }
 
 }  // namespace pkv
