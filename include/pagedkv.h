@@ -120,6 +120,28 @@ pkv_status pkv_paged_attention_decode(void* out, int out_dtype, const void* q,
                                       size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Test hook of the failure path (no counterpart on the pages): runs the
+ * decode call's tensor-memory path (query groups of 32, 64 or 128 heads per
+ * KV head; anything else gives PKV_EINVAL) with every pipeline wait limited to
+ * wait_limit_ns (1000 .. 1e9) and the softmax warps of every CTA waiting, at
+ * their first unit, on a barrier that no copy, product or thread completes.
+ * That wait runs out, and then so do the waits of the threads that depended on
+ * it: the kernel sets PKV_DEVERR_TIMEOUT in *err_flag (which must not be
+ * NULL), lets its copies and products in flight finish, frees its tensor
+ * memory and returns; the next call on the device runs normally. The outputs
+ * of this call are undefined. Arguments otherwise as for
+ * pkv_paged_attention_decode.
+ * ------------------------------------------------------------------------ */
+pkv_status pkv_test_decode_wait_timeout(void* out, int out_dtype, const void* q,
+                                        const void* k_cache, const void* v_cache, int kv_dtype,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        int num_seqs, int num_heads, int num_kv_heads,
+                                        int head_size, int num_blocks, int block_size,
+                                        int max_blocks_per_seq, float scale, int partition_tokens,
+                                        void* workspace, size_t workspace_bytes,
+                                        int32_t* err_flag, uint64_t wait_limit_ns, void* stream);
+
+/* ------------------------------------------------------------------------
  * Decode attention without a caller workspace.
  *
  * No counterpart on the pages: this is a convenience of this library. It is

@@ -41,6 +41,10 @@ SIGNATURES = {
     "pkv_paged_attention_decode_noalloc": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp,
                                                     _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                     _c_int, _c_int, _c_f, _c_int, _vp, _vp]),
+    "pkv_test_decode_wait_timeout": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
+                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                              _c_int, _c_f, _c_int, _vp, _c_sz, _vp,
+                                              ctypes.c_uint64, _vp]),
     "pkv_paged_attention_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _vp,
                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                              _c_int, _c_int, _c_f, _vp, _vp]),

@@ -1498,12 +1498,17 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num
   return static_cast<size_t>(rows * head_size * 4 + ((rows * 8 + 15) / 16) * 16 + 16);
 }
 
-extern "C" pkv_status pkv_paged_attention_decode(
-    void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
-    int kv_dtype, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
-    int num_heads, int num_kv_heads, int head_size, int num_blocks, int block_size,
-    int max_blocks_per_seq, float scale, int partition_tokens, void* workspace,
-    size_t workspace_bytes, int32_t* err_flag, void* stream) {
+// The decode call. wait_ns limits every pipeline wait of the tensor-memory
+// path and stall_unit (>= 0) makes its softmax warps wait out that unit; both
+// exist for pkv_test_decode_wait_timeout, whose call must take that path
+// (tc_only).
+static pkv_status decode_impl(void* out, int out_dtype, const void* q, const void* k_cache,
+                              const void* v_cache, int kv_dtype, const int32_t* block_tables,
+                              const int32_t* context_lens, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_size, int num_blocks, int block_size,
+                              int max_blocks_per_seq, float scale, int partition_tokens,
+                              void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                              void* stream, uint64_t wait_ns, int stall_unit, bool tc_only) {
   if (num_seqs < 0 || num_seqs > 65535) return PKV_EINVAL;
   if (num_kv_heads < 1) return PKV_EINVAL;
   const int pt = effective_partition(partition_tokens, num_seqs, num_heads, num_kv_heads,
@@ -1571,11 +1576,15 @@ extern "C" pkv_status pkv_paged_attention_decode(
     a.max_parts = static_cast<int>(parts);
     a.bf16 = kv_dtype == PKV_BF16;
     a.q_scale = scale * kLog2e;
+    a.wait_ns = wait_ns;
+    a.stall_unit = stall_unit;
     if (launch_decode_tc(a, st) != cudaSuccess) return PKV_ECUDA;
     const cudaError_t er = head_size == 128 ? launch_reduce<128>(out, out_dtype, rp, st)
                                             : launch_reduce<64>(out, out_dtype, rp, st);
     return er == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
+
+  if (tc_only) return PKV_EINVAL;
 
   // Grouped query heads go to the warp-level tensor path when every TMA copy
   // lands on a 1 KB boundary of a tile half (block_size >= 8), else to the
@@ -1634,6 +1643,32 @@ extern "C" pkv_status pkv_paged_attention_decode(
   e = head_size == 128 ? launch_reduce<128>(out, out_dtype, rp, s)
                        : launch_reduce<64>(out, out_dtype, rp, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+extern "C" pkv_status pkv_paged_attention_decode(
+    void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+    int kv_dtype, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_heads, int num_kv_heads, int head_size, int num_blocks, int block_size,
+    int max_blocks_per_seq, float scale, int partition_tokens, void* workspace,
+    size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return decode_impl(out, out_dtype, q, k_cache, v_cache, kv_dtype, block_tables, context_lens,
+                     num_seqs, num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                     max_blocks_per_seq, scale, partition_tokens, workspace, workspace_bytes,
+                     err_flag, stream, kWaitLimitNs, -1, false);
+}
+
+extern "C" pkv_status pkv_test_decode_wait_timeout(
+    void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+    int kv_dtype, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_heads, int num_kv_heads, int head_size, int num_blocks, int block_size,
+    int max_blocks_per_seq, float scale, int partition_tokens, void* workspace,
+    size_t workspace_bytes, int32_t* err_flag, uint64_t wait_limit_ns, void* stream) {
+  if (err_flag == nullptr || wait_limit_ns < 1000 || wait_limit_ns > kWaitLimitNs)
+    return PKV_EINVAL;
+  return decode_impl(out, out_dtype, q, k_cache, v_cache, kv_dtype, block_tables, context_lens,
+                     num_seqs, num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                     max_blocks_per_seq, scale, partition_tokens, workspace, workspace_bytes,
+                     err_flag, stream, wait_limit_ns, 0, true);
 }
 
 // ---------------------------------------------------------------------------

@@ -82,6 +82,8 @@ struct Params {
   int num_blocks, block_size, max_blocks_per_seq;
   int partition_tokens, max_parts, total_units, box_rows;
   float q_scale;
+  uint64_t wait_ns;                    // limit of every pipeline wait
+  int stall_unit;                      // test hook: the softmax warps wait out this unit; -1: none
 };
 
 struct UnitInfo {
@@ -120,8 +122,8 @@ struct Layout {
   static constexpr int kMergeBytes = kMergeRows * (kMergeStride + 2) * 4;
   // barriers: stage_full[S], stage_empty[S], unit_full[2], unit_empty[2],
   // q_full, q_free, s_full[2], p_full[2], pv_done[2], o_free[2], drain,
-  // mrg_full, mrg_free
-  static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 3) * 8 +
+  // mrg_full, mrg_free, never (one that nothing completes: the test hook's)
+  static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 4) * 8 +
                                     2 * static_cast<int>(sizeof(UnitInfo)) + kMaxIds * 4 +
                                     (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 2 +
                                     kCompactMaxSeqs * 4 + 16;
@@ -130,7 +132,7 @@ struct Layout {
   static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
   static constexpr int kOffMerge = kOffStages + kStages * kStageBytes;
   static constexpr int kOffBars = (kOffMerge + kMergeBytes + 15) / 16 * 16;
-  static constexpr int kNumBars = 2 * kStages + 2 * 8 + 3;
+  static constexpr int kNumBars = 2 * kStages + 2 * 8 + 4;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;
   static constexpr int kOffIds = kOffUnits + 2 * static_cast<int>(sizeof(UnitInfo));
   static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions per sequence
@@ -281,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = o_free + 2;
   uint64_t* mrg_full = drain + 1;
   uint64_t* mrg_free = mrg_full + 1;
+  uint64_t* never = mrg_free + 1;
   float* merge = reinterpret_cast<float*>(smem + Lay::kOffMerge);
   float2* mrg_ml = reinterpret_cast<float2*>(merge + Lay::kMergeRows * Lay::kMergeStride);
   UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + Lay::kOffUnits);
@@ -316,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two copies: every row; four: the copies past the first, then the first
     mbar_init(mrg_full, C == 2 ? kRows : (C > 1 ? kRows - kRows / C : 1));
     mbar_init(mrg_free, C == 2 ? kRows : kRows / C);
+    mbar_init(never, 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -411,9 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       const int slot = k & 1;
       bool w_ok = true;
-      if (lane == 0 && k >= 2) w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1);
+      if (lane == 0 && k >= 2) w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1, p.wait_ns);
       // the staging buffer, once the previous unit's rows are in tensor memory
-      if (lane == 0 && k >= 1 && info.seq >= 0) w_ok = w_ok && mbar_wait(q_free, (k - 1) & 1);
+      if (lane == 0 && k >= 1 && info.seq >= 0) w_ok = w_ok && mbar_wait(q_free, (k - 1) & 1, p.wait_ns);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
         ok = false;
         break;
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_tiles; ++i, ++g) {
         const int st = g % kStages;
         bool e_ok = true;
-        if (lane == 0 && g >= kStages) e_ok = mbar_wait(&stage_empty[st], ((g / kStages) & 1) ^ 1);
+        if (lane == 0 && g >= kStages) e_ok = mbar_wait(&stage_empty[st], ((g / kStages) & 1) ^ 1, p.wait_ns);
         if (!__shfl_sync(0xffffffffu, e_ok, 0)) {
           ok = false;
           break;
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) {
       flag_error(p.err, PKV_DEVERR_TIMEOUT);
       for (int st = 0; st < kStages; ++st)
-        if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1);
+        if (last_issued[st] >= 0) mbar_wait(&stage_full[st], (last_issued[st] / kStages) & 1, p.wait_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
@@ -485,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S of global tile gi (its stage, score buffer gi % 2) from query buffer qb
       auto issue_s = [&](int gi, int qb) -> bool {
         const int st = gi % kStages, b = gi & 1;
-        if (!mbar_wait(&stage_full[st], (gi / kStages) & 1)) return false;
+        if (!mbar_wait(&stage_full[st], (gi / kStages) & 1, p.wait_ns)) return false;
         // the score buffer's P was read by the P V product two tiles back
-        if (gi >= 2 && !mbar_wait(&pv_done[b], ((gi - 2) >> 1) & 1)) return false;
+        if (gi >= 2 && !mbar_wait(&pv_done[b], ((gi - 2) >> 1) & 1, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t qt = tbase + kQCol + qb * (D / 2);
         const uint64_t dk = dk0 + ((st * Lay::kStageBytes) >> 4);
@@ -502,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O of output buffer ob (+)= P V of global tile gi
       auto issue_pv = [&](int gi, int ob, bool first) -> bool {
         const int st = gi % kStages, b = gi & 1;
-        if (!mbar_wait(&p_full[b], (gi >> 1) & 1)) return false;
+        if (!mbar_wait(&p_full[b], (gi >> 1) & 1, p.wait_ns)) return false;
         tc_fence_after();
         const uint64_t dv = dv0 + ((st * Lay::kStageBytes) >> 4);
         const uint32_t a = tbase + b * kKeys;
@@ -522,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int k = 0; ok; ++k) {
         const int slot = k & 1;
-        if (!mbar_wait(&unit_full[slot], (k >> 1) & 1)) {
+        if (!mbar_wait(&unit_full[slot], (k >> 1) & 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -531,12 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (info.seq < 0) break;
         const int t_begin = info.part * PT;
         const int n_tiles = (min(info.len, t_begin + PT) - t_begin + kKeys - 1) / kKeys;
-        if (!mbar_wait(q_full, k & 1)) {
+        if (!mbar_wait(q_full, k & 1, p.wait_ns)) {
           ok = false;
           break;
         }
         // the output buffer was read out at the end of the unit two back
-        if (k >= 2 && !mbar_wait(&o_free[slot], ((k >> 1) & 1) ^ 1)) {
+        if (k >= 2 && !mbar_wait(&o_free[slot], ((k >> 1) & 1) ^ 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -559,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
       tc_commit(drain);
-      if (!mbar_wait(drain, 0)) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+      if (!mbar_wait(drain, 0, p.wait_ns)) flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- softmax
@@ -572,13 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int slot = k & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&unit_full[slot], (k >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&unit_full[slot], (k >> 1) & 1, p.wait_ns))) {
         ok = false;
         break;
       }
       const UnitInfo info = units[slot];
       mbar_arrive(&unit_empty[slot]);
       if (info.seq < 0) break;
+      // test hook: wait on a barrier nothing completes, so that this wait (and
+      // then the MMA thread's and the copy warp's) runs out
+      if (k == p.stall_unit && !__all_sync(0xffffffffu, mbar_wait(never, 0, p.wait_ns))) {
+        ok = false;
+        break;
+      }
       const int t_begin = info.part * PT;
       const int t_end = min(info.len, t_begin + PT);
       const int n_tiles = (t_end - t_begin + kKeys - 1) / kKeys;
@@ -587,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_tiles; ++i, ++g) {
         const int b = g & 1;
         // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (g >> 1) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (g >> 1) & 1, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -627,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i > 0) {
             // the output rows hold earlier tiles of the unit: rescale them
             // once their P V is done (factor 1 on rows that keep their max)
-            if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.wait_ns))) {
               ok = false;
               break;
             }
@@ -692,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // the unit's partials, once its last P V is done
-      if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.wait_ns))) {
         ok = false;
         break;
       }
@@ -714,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (C == 2) {
         // Copy c merges and writes the half [c D/2, (c + 1) D/2) of the head's
         // row; it hands its other half, with its (m, l), to the other copy.
-        if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (k - 1) & 1))) {
+        if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (k - 1) & 1, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -728,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mrg_ml[cp * G + hr] = make_float2(m, l);
         mbar_arrive(mrg_full);
-        if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, k & 1, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -760,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hf = 0; hf < 2 && ok; ++hf) {
           const int round = 2 * k + hf;
           if (cp > 0) {
-            if (round >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (round - 1) & 1))) {
+            if (round >= 1 && !__all_sync(0xffffffffu, mbar_wait(mrg_free, (round - 1) & 1, p.wait_ns))) {
               ok = false;
               break;
             }
@@ -775,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (hf == 0) mrg_ml[(cp - 1) * G + hr] = make_float2(m, l);
             mbar_arrive(mrg_full);
           } else {
-            if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, round & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(mrg_full, round & 1, p.wait_ns))) {
               ok = false;
               break;
             }
@@ -909,6 +919,8 @@ cudaError_t launch_decode_tc(const DecodeTcArgs& a, cudaStream_t s) {
   p.total_units = a.max_parts * a.num_seqs * a.num_kv_heads;
   p.box_rows = box_rows;
   p.q_scale = a.q_scale;
+  p.wait_ns = a.wait_ns;
+  p.stall_unit = a.stall_unit;
   return dispatch_copies(a.head_size, a.bf16, tcdec::kRows / group, tk, tv, tq, p, s);
 }
 

@@ -60,13 +60,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed, for at most
-// kWaitLimitNs. Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// limit_ns (kWaitLimitNs unless a kernel takes its limit as a parameter).
+// Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 31u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

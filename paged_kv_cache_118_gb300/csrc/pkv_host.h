@@ -52,6 +52,8 @@ struct DecodeTcArgs {
   int partition_tokens, max_parts;
   bool bf16;
   float q_scale;                       // scale * log2(e)
+  uint64_t wait_ns;                    // limit of every pipeline wait (1 s normally)
+  int stall_unit;                      // test hook (see pkv_test_decode_wait_timeout); -1: none
 };
 // The tensor-memory decode path for large query groups (decode_tc.cu): writes
 // the same partition partials as the other decode paths.

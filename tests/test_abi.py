@@ -146,3 +146,16 @@ def test_prefill_rejects_bad_arguments_on_host(over):
 
 def test_prefill_accepts_an_empty_batch():
     assert _prefill_status(S=0, q=None) == pk.PKV_OK
+
+
+def test_wait_timeout_hook_refuses_other_paths_and_bad_limits():
+    """The failure-path test hook runs only the tensor-memory decode path, with a
+    limit from 1 us to 1 s and an error flag to report through; everything else
+    is refused before anything is queued."""
+    f = pk.lib.pkv_test_decode_wait_timeout
+    args = lambda H, Hkv, err, lim: (16, 0, 16, 16, 16, 1, 16, 16, 2, H, Hkv, 128, 8, 16, 4,
+                                     0.125, 0, 16, 1 << 20, err, lim, None)
+    assert f(*args(4, 4, 16, 2_000_000)) == pk.PKV_EINVAL       # not the tensor-memory path
+    assert f(*args(64, 1, None, 2_000_000)) == pk.PKV_EINVAL    # no error flag
+    assert f(*args(64, 1, 16, 10)) == pk.PKV_EINVAL             # limit below 1 us
+    assert f(*args(64, 1, 16, 2 * 10 ** 9)) == pk.PKV_EINVAL    # above 1 s
