@@ -646,8 +646,10 @@ def run_prefill(args):
     scale = 1.0 / math.sqrt(D)
     visible = sum(int(np.sum(L - C + np.arange(C) + 1)) for L in lens)
     flops = 4 * D * H * visible
+    ws = pk.prefill_workspace()
     call = lambda: pk.pkv_paged_attention_prefill(out, q, cache.k_cache, cache.v_cache, tables,
-                                                  ctx, starts, C, B, scale, cache.err)
+                                                  ctx, starts, C, B, scale, workspace=ws,
+                                                  err_flag=cache.err)
     for _ in range(3):
         call()
     torch.cuda.synchronize()

@@ -199,18 +199,29 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, int out_dtype, const vo
  *   max_query_len host int >= every C (sizes the grid)
  *   head_size 64 or 128; block_size a power of two from 8 to 256;
  *   128 % (num_heads / num_kv_heads) == 0; scale > 0
+ *   workspace     device, >= pkv_prefill_workspace_size() bytes, 16-byte
+ *                 aligned, owned by the caller: holds the counter the
+ *                 persistent CTAs claim work from (zeroed by the call on
+ *                 `stream`); it must not be shared by calls that may run at
+ *                 the same time
+ * Work: one item per 256 query rows (chunk tokens x the KV head's query
+ * heads), KV head and sequence; at most one CTA per SM takes items, those
+ * with the most keys first.
  * Device checks: 0 <= C <= min(L, max_query_len) and L <= max_blocks_per_seq *
  * block_size, else the sequence is skipped (its rows untouched) and
- * PKV_DEVERR_CONTEXT set; bad block ids as for decode. Needs no workspace.
- * Errors: PKV_EINVAL, PKV_ECUDA.
+ * PKV_DEVERR_CONTEXT set; bad block ids as for decode.
+ * Errors: PKV_EINVAL (also a missing, short or unaligned workspace),
+ * PKV_ECUDA.
  * ------------------------------------------------------------------------ */
+size_t pkv_prefill_workspace_size(void);
 pkv_status pkv_paged_attention_prefill(void* out, int out_dtype, const void* q,
                                        const void* k_cache, const void* v_cache, int kv_dtype,
                                        const int32_t* block_tables, const int32_t* context_lens,
                                        const int32_t* query_start, int num_seqs, int num_heads,
                                        int num_kv_heads, int head_size, int num_blocks,
                                        int block_size, int max_blocks_per_seq, int max_query_len,
-                                       float scale, int32_t* err_flag, void* stream);
+                                       float scale, void* workspace, size_t workspace_bytes,
+                                       int32_t* err_flag, void* stream);
 
 /* ------------------------------------------------------------------------
  * reshape_and_cache: write new tokens' keys and values into their slots.

@@ -45,9 +45,10 @@ SIGNATURES = {
                                               _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                               _c_int, _c_f, _c_int, _vp, _c_sz, _vp,
                                               ctypes.c_uint64, _vp]),
+    "pkv_prefill_workspace_size": (_c_sz, []),
     "pkv_paged_attention_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _vp,
                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                             _c_int, _c_int, _c_f, _vp, _vp]),
+                                             _c_int, _c_int, _c_f, _vp, _c_sz, _vp, _vp]),
     "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _vp, _vp]),
     "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_sz, _vp]),
@@ -241,6 +242,11 @@ def decode_workspace(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_pe
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
+def prefill_workspace(device="cuda") -> torch.Tensor:
+    """A caller-owned scratch buffer of the size the prefill call needs."""
+    return torch.empty(lib.pkv_prefill_workspace_size(), dtype=torch.uint8, device=device)
+
+
 def pkv_paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                                v_cache: torch.Tensor, block_tables: torch.Tensor,
                                context_lens: torch.Tensor, block_size: int, scale: float,
@@ -294,10 +300,13 @@ def pkv_paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: tor
                                 v_cache: torch.Tensor, block_tables: torch.Tensor,
                                 context_lens: torch.Tensor, query_start: torch.Tensor,
                                 max_query_len: int, block_size: int, scale: float,
+                                workspace: torch.Tensor | None = None,
                                 err_flag: torch.Tensor | None = None, stream=None) -> None:
     """Causal attention of each sequence's query chunk (its last C tokens) over
     its paged history. q, out: [total_queries, num_heads, head_size];
-    query_start: int32 [num_seqs + 1]."""
+    query_start: int32 [num_seqs + 1]; workspace: uint8, at least
+    pkv_prefill_workspace_size() bytes (prefill_workspace() makes one; the
+    call allocates one when it is None)."""
     where = "pkv_paged_attention_prefill"
     _check_caches(where, k_cache, v_cache)
     nb, B, Hkv, D = k_cache.shape
@@ -314,13 +323,19 @@ def pkv_paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: tor
     _check_int(where, "query_start", query_start, torch.int32, (S + 1,))
     _contiguous(where, q=q, out=out)
     _check_err(where, err_flag)
-    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start, err_flag)
+    if workspace is not None:
+        _require(workspace.dtype == torch.uint8 and workspace.is_contiguous(), where,
+                 "workspace must be a contiguous uint8 tensor")
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start, err_flag,
+               workspace)
+    if workspace is None:
+        workspace = prefill_workspace(out.device)
     _, H, D = q.shape
     st = lib.pkv_paged_attention_prefill(
         _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
         _ptr(block_tables), _ptr(context_lens), _ptr(query_start), context_lens.shape[0], H,
         Hkv, D, nb, block_size, block_tables.shape[1], int(max_query_len), float(scale),
-        _ptr(err_flag), _stream(stream))
+        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream))
     _check(st, "pkv_paged_attention_prefill")
 
 

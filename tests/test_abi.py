@@ -125,27 +125,35 @@ def test_reshape_and_cache_host_validation():
 
 def _prefill_status(**over):
     a = dict(out=16, out_dtype=0, q=16, k=16, v=16, kv_dtype=0, bt=16, cl=16, qs=16, S=2, H=8,
-             Hkv=8, D=128, nb=8, B=16, mb=4, mq=64, scale=0.125, err=None)
+             Hkv=8, D=128, nb=8, B=16, mb=4, mq=64, scale=0.125, ws=16, ws_bytes=16, err=None)
     a.update(over)
     return pk.lib.pkv_paged_attention_prefill(a["out"], a["out_dtype"], a["q"], a["k"], a["v"],
                                               a["kv_dtype"], a["bt"], a["cl"], a["qs"], a["S"],
                                               a["H"], a["Hkv"], a["D"], a["nb"], a["B"], a["mb"],
-                                              a["mq"], a["scale"], a["err"], None)
+                                              a["mq"], a["scale"], a["ws"], a["ws_bytes"],
+                                              a["err"], None)
 
 
 @pytest.mark.parametrize("over", [
     dict(q=None), dict(qs=None), dict(kv_dtype=2), dict(out_dtype=7), dict(D=96), dict(B=4),
     dict(B=12), dict(B=512), dict(H=24, Hkv=8), dict(H=6, Hkv=4), dict(mq=0), dict(S=-1),
-    dict(scale=0.0), dict(scale=-0.125), dict(scale=float("inf")), dict(out=24)])
+    dict(scale=0.0), dict(scale=-0.125), dict(scale=float("inf")), dict(out=24),
+    dict(ws=None), dict(ws=24), dict(ws_bytes=8)])
 def test_prefill_rejects_bad_arguments_on_host(over):
     """Host checks: head size 64/128, block sizes 8..256 (powers of two), a
     query-head group that divides the 128 rows of a query tile, a positive
-    finite scale, 16-byte aligned buffers."""
+    finite scale, 16-byte aligned buffers, a workspace of the stated size."""
     assert _prefill_status(**over) == pk.PKV_EINVAL
 
 
 def test_prefill_accepts_an_empty_batch():
     assert _prefill_status(S=0, q=None) == pk.PKV_OK
+
+
+def test_prefill_workspace_size():
+    """One claim counter, padded to 16 bytes."""
+    assert pk.lib.pkv_prefill_workspace_size() == 16
+    assert pk.prefill_workspace("cpu").numel() == 16
 
 
 def test_wait_timeout_hook_refuses_other_paths_and_bad_limits():

@@ -131,6 +131,11 @@ def test_prefill_rejects(over, msg):
         pk.pkv_paged_attention_prefill(**_pf_args(**over))
 
 
+def test_prefill_rejects_a_wrong_workspace():
+    with pytest.raises(ValueError, match="workspace"):
+        pk.pkv_paged_attention_prefill(**_pf_args(), workspace=torch.empty(16, dtype=torch.int32))
+
+
 def test_copy_blocks_rejects_mismatched_caches():
     k = torch.empty(NB, B, HKV, D, dtype=torch.float16)
     with pytest.raises(ValueError, match="v_cache shape"):

@@ -28,6 +28,14 @@ CASES = [
     ((300, 50), (300, 7), 128, 1, 64, 16, "bf16"),
     ((600, 70), (600, 70), 8, 2, 128, 256, "f16"),
     ((1000,), (1000,), 8, 8, 128, 8, "bf16"),
+    # more work items than SMs, so CTAs claim items from the counter and run
+    # several in turn: 12 sequences x 16 KV heads x 2 query blocks (MHA,
+    # chunks of 0, 1 and up to 300 tokens, so some items are empty), and
+    # 4-way GQA over 10 sequences with up to 4 query blocks each
+    ((620, 610, 700, 333, 900, 640, 777, 1200, 301, 512, 450, 1000),
+     (300, 0, 1, 333, 299, 250, 17, 300, 300, 256, 257, 129), 16, 16, 64, 16, "f16"),
+    ((800, 1024, 260, 999, 512, 700, 1300, 257, 640, 900),
+     (256, 255, 1, 200, 64, 65, 256, 257, 128, 190), 32, 8, 128, 16, "bf16"),
 ]
 
 
@@ -44,12 +52,22 @@ def _run(case, seed=0):
                                    batch.context_lens, starts, B, batch.scale, dt)
     qd = dev(q, dt)
     qsd = torch.from_numpy(starts).cuda()
+    ws = pk.prefill_workspace()
     for od in (TORCH_DTYPE[dt], torch.float32):
         out = torch.full(qd.shape, float("nan"), dtype=od, device="cuda")
         pk.pkv_paged_attention_prefill(out, qd, cache.k_cache, cache.v_cache, tables, ctx, qsd,
-                                       max(chunks), B, float(batch.scale), cache.err)
+                                       max(chunks), B, float(batch.scale), workspace=ws,
+                                       err_flag=cache.err)
         torch.cuda.synchronize()
         assert_close(out, want, dt)
+        if od == torch.float32:
+            # the same call again, bit for bit, whichever CTA claims which item
+            again = torch.empty_like(out)
+            pk.pkv_paged_attention_prefill(again, qd, cache.k_cache, cache.v_cache, tables, ctx,
+                                           qsd, max(chunks), B, float(batch.scale),
+                                           workspace=ws, err_flag=cache.err)
+            torch.cuda.synchronize()
+            assert torch.equal(again, out)
     assert cache.err.item() == 0
 
 
@@ -66,7 +84,7 @@ def test_bad_chunk_is_reported_and_skipped():
     q = torch.randn(70, 4, 64, dtype=torch.float16, device="cuda")
     out = torch.zeros_like(q)
     pk.pkv_paged_attention_prefill(out, q, cache.k_cache, cache.v_cache, tables, ctx, starts,
-                                   60, 16, 0.125, cache.err)
+                                   60, 16, 0.125, err_flag=cache.err)
     torch.cuda.synchronize()
     assert cache.err.item() & pk.PKV_DEVERR_CONTEXT
     assert torch.all(out[10:] == 0) and torch.all(torch.isfinite(out[:10]))
