@@ -15,25 +15,29 @@
 // items with more keys first, the CTA's own index first, then claims from a
 // counter in the caller's workspace):
 //  * warp 0 claims items and publishes them to the other warps, then streams
-//    each item's 64-key tiles of K and V over the causal range only, one TMA
-//    copy per physical block and 128-byte line (128-byte swizzle), each lane
-//    issuing one, into a 5-stage ring completing on mbarriers; both query
-//    tiles use each K/V tile, and the ring runs on from one item into the
-//    next;
-//  * warp 1 owns the tensor memory (per query tile: two 64-column score
-//    buffers and the D-column output) and issues, from one thread, S = Q K^T
-//    (M = 128, N = 64, K = D) into a score buffer and O += P V (M = 128,
-//    N = D, K = 64, P read from tensor memory) into the output, each
-//    followed by a commit to an mbarrier; the next tile's S is issued before
-//    this tile's P V, and the next item's S as soon as its query rows are in;
+//    each item's causal key range in 128-key tiles, K and V of a tile into
+//    two slots of one ring (so a K tile is released as soon as its score
+//    products are done), one TMA copy per physical block and 128-byte line
+//    (128-byte swizzle), each lane issuing one; both query tiles use each
+//    K/V tile, and the ring runs on from one item into the next;
+//  * warp 1 owns the tensor memory (per query tile: a 128-column score
+//    buffer and the D-column output) and issues, from one thread,
+//    S = Q K^T (M = 128, N = 128, K = D) and O += P V (M = 128, N = D,
+//    K = 128, P read from tensor memory), each followed by a commit to an
+//    mbarrier; a query tile's next S follows its P V, so one tile's
+//    softmax runs while the other tile's products are computed. A product
+//    issue costs one thread tens of cycles whatever its size, so the
+//    products are made as wide as tensor memory allows;
 //  * a softmax warpgroup per query tile, one thread per query row (its TMEM
 //    lane): it writes the row's query into shared memory once the previous
-//    item's S products are done; the row's 64 scores come out of tensor
-//    memory, the causal mask and a base-2 online softmax with lazy rescale
-//    (the output row is rescaled in place only when the running maximum grows
-//    by more than 2^8) give P, written back over the scores as 16-bit pairs,
-//    where the P V product reads it; the output row is divided by the row sum
-//    at the item's end and the output columns are handed back to the MMA.
+//    item's S products are done; it reads the row's 128 scores from tensor
+//    memory in one load (a tensor-memory round trip costs hundreds of
+//    cycles under load, so a tile takes one load and one store), runs a
+//    base-2 online softmax with lazy rescale (the output row is rescaled in
+//    place only when the running maximum grows by more than 2^8) and writes
+//    P back over the scores as 16-bit pairs, where the P V product reads it;
+//    the output row is divided by the row sum at the item's end and the
+//    output columns are handed back to the MMA.
 // Every wait is bounded; a chunk or context length out of range is skipped
 // and reported.
 
@@ -55,11 +59,10 @@ namespace prefill {
 
 constexpr int kRows = 128;             // query rows of one query tile: the TMEM lanes
 constexpr int kQTiles = 2;             // query tiles per item, sharing every K/V tile
-constexpr int kKeys = 64;              // keys per tile
-constexpr int kStages = 5;
+constexpr int kKeys = 128;             // keys per tile
 constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: items, copies; warp 1: MMA; 4 warps per query tile
 constexpr int kSoftmaxWarp0 = 4;
-// per query tile t, from column 256 t: S0 [0, 64), S1 [64, 128), O [128, 128 + D)
+// per query tile t, from column 256 t: S (P over it) [0, 128), O [128, 128 + D)
 constexpr uint32_t kTmemCols = 256 * kQTiles;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -83,7 +86,7 @@ struct Params {
   int max_query_len;
   int qblocks;                         // 256-row query blocks of the longest chunk
   int total_items;                     // qblocks * num_seqs * num_kv_heads
-  int box_rows;                        // rows per TMA copy: min(block_size, kKeys)
+  int box_rows;                        // rows per TMA copy: min(block_size, 64)
   float q_scale;                       // scale * log2(e)
 };
 
@@ -94,9 +97,9 @@ struct Item {
   int kvh, qb, qs, C, L;
 };
 
-// What an item reads: keys of each query tile (the causal range of its last
-// row), of the whole item, and the lowest query tile that reads the last key
-// tile (it zeroes that tile's V rows past the last key).
+// What an item reads: key tiles of each query tile (the causal range of its
+// last row), keys and key tiles of the whole item, and the lowest query tile
+// that reads the last key tile (it zeroes that tile's V rows past the last key).
 struct Shape {
   int nt[kQTiles];
   int kv_end, n_tiles, zt;
@@ -123,21 +126,22 @@ __device__ __forceinline__ Shape item_shape(const Item& it, int G) {
 // 128-byte rows with the 128-byte swizzle (16-byte chunk c of the row at
 // position n sits at c ^ (n % 8)), 8-row groups 1024 bytes apart:
 //  Q, per query tile: D/64 column blocks of 128 rows (A of S, K-major);
-//  each stage: K then V, each D/64 line blocks of 64 key rows (B of S,
-//  K-major; B of P V, MN-major with the next 64 columns one line block on);
-//  (P stays in tensor memory.) Then the barriers and two item slots.
+//  a ring of slots, each holding a K tile or a V tile: D/64 line blocks of
+//  128 key rows (K: B of S, K-major; V: B of P V, MN-major with the next 64
+//  columns one line block on); (P stays in tensor memory.) Then the
+//  barriers and two item slots.
 template <int D>
 struct Layout {
   static constexpr int NH = D / 64;
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kLineBytes = kKeys * 128;          // one line block of a K or V tile
-  static constexpr int kTileBytes = NH * kLineBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kOffStages = kQTiles * kQBytes;
-  static constexpr int kOffBars = kOffStages + kStages * kStageBytes;
-  // stage_full[S], stage_empty[S], item_full[2], item_empty[2], q_full, q_free,
-  // per query tile s_full[2], p_full[2], pv_done[2], o_free; drain, tail
-  static constexpr int kNumBars = 2 * kStages + 4 + 2 + 7 * kQTiles + 2;
+  static constexpr int kSlotBytes = NH * kLineBytes;      // one K or V tile
+  static constexpr int kSlots = D == 128 ? 5 : 8;
+  static constexpr int kOffSlots = kQTiles * kQBytes;
+  static constexpr int kOffBars = kOffSlots + kSlots * kSlotBytes;
+  // slot_full[S], slot_empty[S], item_full[2], item_empty[2], q_full, q_free,
+  // per query tile s_full, p_full, pv_done, o_free; drain, tail
+  static constexpr int kNumBars = 2 * kSlots + 4 + 2 + 4 * kQTiles + 2;
   static constexpr int kOffItems = kOffBars + kNumBars * 8;
   static constexpr int kOffTmem = kOffItems + 2 * static_cast<int>(sizeof(Item));
   static constexpr int kSmem = 1024 + kOffTmem + 16;
@@ -175,8 +179,9 @@ __device__ __forceinline__ void store_row(void* out, int out_dtype, int64_t base
 // names the parity of the phase it needs; no barrier can run two phases ahead
 // of a waiter, because each producer's next phase needs the waiter's
 // progress:
-//  * stage_full / stage_empty: per K/V tile of the CTA (g, counted over all
-//    items); item_full / item_empty: per item, two slots;
+//  * slot_full / slot_empty: per K or V tile of the CTA (g, counted over all
+//    items: K of key tile j in slot g, its V in slot g + 1); item_full /
+//    item_empty: per item, two slots;
 //  * q_full (256 arrivals: every softmax thread wrote its query row) and
 //    q_free (the item's S products are done): once per item;
 //  * s_full / p_full / pv_done of query tile t: per key tile that t reads,
@@ -189,20 +194,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const Params p) {
   using Lay = Layout<D>;
   constexpr int NH = Lay::NH;
+  constexpr int S = Lay::kSlots;
   constexpr bool kBF16 = std::is_same<T, BF16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* qtiles = smem;
-  uint8_t* stages = smem + Lay::kOffStages;
-  uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
-  uint64_t* stage_empty = stage_full + kStages;
-  uint64_t* item_full = stage_empty + kStages;
+  uint8_t* slots = smem + Lay::kOffSlots;
+  uint64_t* slot_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
+  uint64_t* slot_empty = slot_full + S;
+  uint64_t* item_full = slot_empty + S;
   uint64_t* item_empty = item_full + 2;
   uint64_t* q_full = item_empty + 2;
   uint64_t* q_free = q_full + 1;
-  uint64_t* tbars = q_free + 1;                 // per query tile: s_full[2], p_full[2], pv_done[2], o_free
-  uint64_t* drain = tbars + 7 * kQTiles;
+  uint64_t* tbars = q_free + 1;                 // per query tile: s_full, p_full, pv_done, o_free
+  uint64_t* drain = tbars + 4 * kQTiles;
   uint64_t* tail = drain + 1;
   Item* items = reinterpret_cast<Item*>(smem + Lay::kOffItems);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffTmem);
@@ -213,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = p.block_size;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&stage_full[i], 1);
-      mbar_init(&stage_empty[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&slot_full[i], 1);
+      mbar_init(&slot_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&item_full[i], 1);
@@ -224,12 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, kQTiles * kRows);
     mbar_init(q_free, 1);
     for (int t = 0; t < kQTiles; ++t) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&tbars[7 * t + i], 1);              // s_full
-        mbar_init(&tbars[7 * t + 2 + i], kRows);      // p_full
-        mbar_init(&tbars[7 * t + 4 + i], 1);          // pv_done
-      }
-      mbar_init(&tbars[7 * t + 6], kRows);            // o_free
+      mbar_init(&tbars[4 * t], 1);              // s_full
+      mbar_init(&tbars[4 * t + 1], kRows);      // p_full
+      mbar_init(&tbars[4 * t + 2], 1);          // pv_done
+      mbar_init(&tbars[4 * t + 3], kRows);      // o_free
     }
     mbar_init(drain, 1);
     mbar_init(tail, kRows);
@@ -243,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- items, copies
-    // Lane l copies line (l / 2) % NH of K (l even) or V (l odd) for the
-    // tile's copy l / (2 NH); it reads that copy's block id before the wait
-    // for the stage, so the read overlaps the wait.
+    // Lane l copies line l % NH of the tile's copy l / NH (R rows of one
+    // block); it reads that copy's block id before the waits for the slots,
+    // and issues the copy into the K slot and then into the V slot.
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
@@ -253,15 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t policy = l2_evict_first_policy();
     const int R = p.box_rows;
     const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
-    const int my_c = lane / (2 * NH);
-    const int my_h = (lane >> 1) % NH;
-    const CUtensorMap* my_map = (lane & 1) ? &tm_v : &tm_k;
-    const uint32_t my_off =
-        (lane & 1) * Lay::kTileBytes + my_h * Lay::kLineBytes + my_c * copy_bytes;
+    const int my_c = lane / NH;
+    const int my_h = lane % NH;
+    const uint32_t my_off = my_h * Lay::kLineBytes + my_c * copy_bytes;
     const int per_qb = p.num_seqs * p.num_kv_heads;
     const int tok_per_item = kQTiles * (kRows / G);
     const int max_ctx = p.max_blocks_per_seq * B;
-    int g = 0;                                  // K/V tiles issued
+    int g = 0;                                  // slots filled
     int k = 0;                                  // items published
     bool ok = true;
     for (int claim = 0; ok; ++claim) {
@@ -303,59 +305,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.seq < 0) break;
       const Shape sh = item_shape(it, G);
       const int32_t* row = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
-      for (int j = 0; j < sh.n_tiles; ++j, ++g) {
-        const int st = g % kStages;
+      for (int j = 0; ok && j < sh.n_tiles; ++j) {
         const int t0 = j * kKeys;
         const int copies = (min(kKeys, sh.kv_end - t0) + R - 1) / R;   // copies of R rows cover the keys
         const bool mine = my_c < copies;
         const int tk = t0 + my_c * R;                      // first key of the lane's copy
         int32_t id = mine ? __ldg(row + tk / B) : 0;
-        if (g >= kStages &&
-            !__all_sync(0xffffffffu, mbar_wait(&stage_empty[st], ((g / kStages) & 1) ^ 1))) {
-          ok = false;
-          break;
+        if (mine && (id < 0 || id >= p.num_blocks)) {
+          flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+          id = 0;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&stage_full[st], 2u * NH * copies * copy_bytes);
-        __syncwarp();
-        if (mine) {
-          if (id < 0 || id >= p.num_blocks) {
-            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;
+        for (int kv = 0; kv < 2; ++kv, ++g) {
+          const int st = g % S;
+          if (g >= S &&
+              !__all_sync(0xffffffffu, mbar_wait(&slot_empty[st], ((g / S) & 1) ^ 1))) {
+            ok = false;
+            break;
           }
-          tma_load_4d(stages + st * Lay::kStageBytes + my_off, my_map, &stage_full[st], 0,
-                      id * B + tk % B, it.kvh, my_h, policy);
+          if (lane == 0) mbar_arrive_expect_tx(&slot_full[st], NH * copies * copy_bytes);
+          __syncwarp();
+          if (mine)
+            tma_load_4d(slots + st * Lay::kSlotBytes + my_off, kv ? &tm_v : &tm_k, &slot_full[st], 0,
+                        id * B + tk % B, it.kvh, my_h, policy);
         }
       }
     }
     if (!ok && lane == 0) {
       flag_error(p.err, PKV_DEVERR_TIMEOUT);
-      // let the copies in flight (the last kStages tiles issued) land
-      for (int i = max(0, g - kStages); i < g; ++i)
-        mbar_wait(&stage_full[i % kStages], (i / kStages) & 1);
+      // let the copies in flight (the last S slots filled) land
+      for (int i = max(0, g - S); i < g; ++i) mbar_wait(&slot_full[i % S], (i / S) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t kIdescS = mma_idesc_f16(kBF16, kRows, kKeys, false);
       constexpr uint32_t kIdescO = mma_idesc_f16(kBF16, kRows, D, true);
-      // Descriptors are built once; a k-step or another buffer only moves the
+      // Descriptors are built once; a k-step or another slot only moves the
       // start address (bits 0-13, in 16-byte units), so it is an addition.
       const uint64_t dq0 = smem_desc_sw128(qtiles, 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(stages, 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(stages + Lay::kTileBytes, Lay::kLineBytes, 1024);
-      int g = 0;                                // K/V tiles consumed
+      const uint64_t dk0 = smem_desc_sw128(slots, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(slots, Lay::kLineBytes, 1024);
+      int g = 0;                                // slots consumed
       int gt[kQTiles] = {0, 0};                 // key tiles each query tile has read
       int no[kQTiles] = {0, 0};                 // items in which each query tile read keys
       bool ok = true;
-      // S of query tile t for its key tile gi (counted over items), into score
-      // buffer gi % 2, once the P V product two tiles back has read the P there
-      auto issue_s = [&](int t, int gi, int stage) -> bool {
-        const int b = gi & 1;
-        if (gi >= 2 && !mbar_wait(&tbars[7 * t + 4 + b], ((gi - 2) >> 1) & 1)) return false;
+      auto slot_landed = [&](int gg) -> bool {
+        if (!mbar_wait(&slot_full[gg % S], (gg / S) & 1)) return false;
         tc_fence_after();
+        return true;
+      };
+      // S of query tile t from the K tile in slot gg, into its score columns
+      auto issue_s = [&](int t, int gg) {
         const uint64_t dq = dq0 + (t * Lay::kQBytes >> 4);
-        const uint64_t dk = dk0 + (stage * Lay::kStageBytes >> 4);
-        const uint32_t d = tbase + 256 * t + b * kKeys;
+        const uint64_t dk = dk0 + ((gg % S) * Lay::kSlotBytes >> 4);
+        const uint32_t d = tbase + 256 * t;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           // 64-element column block ks / 4, 32 bytes per k-step inside it
@@ -363,21 +366,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ko = ((ks >> 2) * Lay::kLineBytes + (ks & 3) * 32) >> 4;
           tc_mma_f16(d, dq + qo, dk + ko, kIdescS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&tbars[7 * t + b]);                       // s_full
-        return true;
+        tc_commit(&tbars[4 * t]);                           // s_full
       };
-      // O of query tile t (+)= P V for its key tile gi; P (16-bit, two per
-      // column) is in the first 32 columns of score buffer gi % 2, 8 columns
-      // per k-step; an item's first P V overwrites O
-      auto issue_pv = [&](int t, int gi, int stage, bool first) -> bool {
-        const int b = gi & 1;
-        if (!mbar_wait(&tbars[7 * t + 2 + b], (gi >> 1) & 1)) return false;   // p_full
-        tc_fence_after();
+      // O of query tile t (+)= P V with the V tile in slot gg; P (16-bit, two
+      // per column) is in the first 64 score columns, 8 columns per k-step;
+      // an item's first P V overwrites O
+      auto issue_pv = [&](int t, int gg, bool first) {
         // V as B, MN-major: 16 keys are two 8-row groups; the next 64 columns
         // of D are one line block (kLineBytes) on
-        const uint64_t dv = dv0 + (stage * Lay::kStageBytes >> 4);
-        const uint32_t a = tbase + 256 * t + b * kKeys;
-        const uint32_t d = tbase + 256 * t + 128;
+        const uint64_t dv = dv0 + ((gg % S) * Lay::kSlotBytes >> 4);
+        const uint32_t a = tbase + 256 * t;
+        const uint32_t d = a + 128;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           tc_mma_f16_ts(d, a + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO,
@@ -387,8 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kKeys / 16; ++kk)
             tc_mma_f16_ts(d, a + kKeys / 2 + kk * 8, dv + ((kk * 16 * 128) >> 4), kIdescO, 1u);
         }
-        tc_commit(&tbars[7 * t + 4 + b]);                   // pv_done
-        return true;
+        tc_commit(&tbars[4 * t + 2]);                       // pv_done
       };
       for (int k = 0; ok; ++k) {
         const int slot = k & 1;
@@ -405,31 +403,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // S of both query tiles for key tile j of this item
-        auto issue_s_all = [&](int j) -> bool {
-          const int gg = g + j;
-          if (!mbar_wait(&stage_full[gg % kStages], (gg / kStages) & 1)) return false;
-          for (int t = 0; t < kQTiles; ++t)
-            if (j < sh.nt[t] && !issue_s(t, gt[t] + j, gg % kStages)) return false;
-          if (j == sh.n_tiles - 1) tc_commit(q_free);       // the item's S products are issued
-          return true;
-        };
-        ok = issue_s_all(0);
+        // S of the first key tile; the S columns are free: every softmax
+        // thread read back its tile's output (after the tile's last P V)
+        // before it wrote this item's query rows
+        if (!slot_landed(g)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < kQTiles; ++t)
+          if (sh.nt[t] > 0) issue_s(t, g);
+        tc_commit(&slot_empty[g % S]);                     // K tile 0 read
+        if (sh.n_tiles == 1) tc_commit(q_free);            // the item's S products are issued
         for (int j = 0; ok && j < sh.n_tiles; ++j) {
-          if (j + 1 < sh.n_tiles) ok = issue_s_all(j + 1);
+          const int gk = g + 2 * j;                        // K of tile j; its V in gk + 1
+          if (!slot_landed(gk + 1)) {
+            ok = false;
+            break;
+          }
+          bool k_next = false;
           for (int t = 0; ok && t < kQTiles; ++t) {
             if (j >= sh.nt[t]) continue;
-            // the item's first P V overwrites O: the softmax threads have read
-            // back the last item in which this query tile read keys
-            if (j == 0 && no[t] >= 1 && !mbar_wait(&tbars[7 * t + 6], (no[t] - 1) & 1)) {
+            const int gi = gt[t] + j;
+            if (!mbar_wait(&tbars[4 * t + 1], gi & 1)) {   // p_full: P of tile j written
               ok = false;
               break;
             }
-            ok = issue_pv(t, gt[t] + j, (g + j) % kStages, j == 0);
+            // the item's first P V overwrites O: the softmax threads have read
+            // back the last item in which this query tile read keys
+            if (j == 0 && no[t] >= 1 && !mbar_wait(&tbars[4 * t + 3], (no[t] - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, gk + 1, j == 0);
+            if (j + 1 < sh.nt[t]) {
+              // the next S overwrites the P this P V reads; products issued
+              // by one thread run in issue order, so it follows at once
+              if (!k_next && !slot_landed(gk + 2)) {
+                ok = false;
+                break;
+              }
+              k_next = true;
+              tc_fence_after();
+              issue_s(t, gk + 2);
+            }
           }
-          if (ok) tc_commit(&stage_empty[(g + j) % kStages]);   // K and V of the tile are read
+          if (!ok) break;
+          tc_commit(&slot_empty[(gk + 1) % S]);            // V tile j read
+          if (k_next) {
+            tc_commit(&slot_empty[(gk + 2) % S]);          // K tile j + 1 read
+            if (j + 2 == sh.n_tiles) tc_commit(q_free);    // the item's S products are issued
+          }
         }
-        g += sh.n_tiles;
+        g += 2 * sh.n_tiles;
         for (int t = 0; t < kQTiles; ++t) {
           gt[t] += sh.nt[t];
           no[t] += sh.nt[t] > 0 ? 1 : 0;
@@ -445,14 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - kSoftmaxWarp0) >> 2;             // query tile
     const int r = ((warp - kSoftmaxWarp0) & 3) * 32 + lane;   // row of the tile = TMEM lane
     const uint32_t tl = tbase + 256 * t + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
-    uint64_t* s_full = &tbars[7 * t];
-    uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = s_full + 4;
-    uint64_t* o_free = s_full + 6;
+    uint64_t* s_full = &tbars[4 * t];
+    uint64_t* p_full = s_full + 1;
+    uint64_t* pv_done = s_full + 2;
+    uint64_t* o_free = s_full + 3;
     uint8_t* qtile = qtiles + t * Lay::kQBytes;
     const int tok_per_qt = kRows / G;
     int gt = 0;                                            // key tiles this query tile read, over all items
-    int gall = 0;                                          // key tiles of the CTA, over all items
+    int gall = 0;                                          // slots of the CTA, over all items
     int ntail = 0;                                         // items whose last key tile was partial
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -492,35 +518,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_my; ++j) {
         const int gi = gt + j;
-        const int b = gi & 1;
         // tcgen05.ld/st are warp-collective: every wait result is made warp-uniform
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (gi >> 1) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full, gi & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float s[kKeys];
-#pragma unroll
-        for (int h = 0; h < kKeys / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(tl + b * kKeys + h * 32, raw);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[h * 32 + i] = __uint_as_float(raw[i]);
-        }
-        // causal mask (also hides keys past the context and rows past the chunk);
-        // the row maximum is taken on unscaled scores (the scale is positive)
+        // the row's 128 scores in one load; the causal mask (also hides keys
+        // past the context and rows past the chunk) only on tiles that cross
+        // the row's causal edge; the row maximum is taken on unscaled scores
+        // (the scale is positive)
         const int key0 = j * kKeys;
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (live && key0 + kKeys - 1 <= pos) {              // every key of the tile is visible
+        uint32_t sc[kKeys];
+        tmem_ld128(tl, sc);
+        if (!(live && key0 + kKeys - 1 <= pos)) {
 #pragma unroll
-          for (int i = 0; i < kKeys; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < kKeys; ++i) {
-            s[i] = (live && key0 + i <= pos) ? s[i] : -INFINITY;
-            mx[i & 3] = fmaxf(mx[i & 3], s[i]);
-          }
+          for (int i = 0; i < kKeys; ++i)
+            if (!(live && key0 + i <= pos)) sc[i] = __float_as_uint(-INFINITY);
         }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sc[i]));
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.q_scale;
         const bool need = mt > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {                 // the whole warp takes this branch
@@ -528,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j > 0) {
             // the output rows hold earlier tiles: rescale them once their P V is
             // done (factor 1 on rows that keep their max or hold nothing yet)
-            if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(gi - 1) & 1], ((gi - 1) >> 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gi - 1) & 1))) {
               ok = false;
               break;
             }
@@ -547,30 +565,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mn;
         }
         // p = 2^(scale s - m): a masked score is -inf and gives 0 (m is finite
-        // on a live row from its first tile on; a row past the chunk writes 0)
+        // on a live row from its first tile on; a row past the chunk writes 0);
+        // P goes over the scores as 16-bit pairs in one store; bf16 P also
+        // keeps its rounding error (p - hi) in the next 64 columns, read by a
+        // second P V
         const float nm = live ? -m : 0.f;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        // P as 16-bit pairs over the first 32 columns of the scores; bf16 P also
-        // keeps its rounding error (p - hi) in the next 32, read by a second P V
-        uint32_t pk[kKeys / 2], pl[kKeys / 2];
+        uint32_t pk[kKeys / 2];
 #pragma unroll
         for (int i = 0; i < kKeys; i += 2) {
-          const float e0 = live ? ex2(fmaf(s[i], p.q_scale, nm)) : 0.f;
-          const float e1 = live ? ex2(fmaf(s[i + 1], p.q_scale, nm)) : 0.f;
+          const float e0 = live ? ex2(fmaf(__uint_as_float(sc[i]), p.q_scale, nm)) : 0.f;
+          const float e1 = live ? ex2(fmaf(__uint_as_float(sc[i + 1]), p.q_scale, nm)) : 0.f;
           ls[(i >> 1) & 3] += e0 + e1;
           pk[i >> 1] = T::pack(e0, e1);
           if constexpr (kBF16) {
             const float2 h = T::to_float2(pk[i >> 1]);
-            pl[i >> 1] = T::pack(e0 - h.x, e1 - h.y);
+            sc[i >> 1] = T::pack(e0 - h.x, e1 - h.y);        // sc[0 .. i] are no longer needed
           }
         }
+        tmem_st64(tl, pk);
+        if constexpr (kBF16) {
+          uint32_t pl[kKeys / 2];
+#pragma unroll
+          for (int i = 0; i < kKeys / 2; ++i) pl[i] = sc[i];
+          tmem_st64(tl + kKeys / 2, pl);
+        }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tmem_st32(tl + b * kKeys, pk);                        // over the scores of this tile
-        if constexpr (kBF16) tmem_st32(tl + b * kKeys + kKeys / 2, pl);
         if (j == sh.n_tiles - 1 && partial_end) {
           if (t == sh.zt) {
-            // V rows past the last key may hold anything (0 x NaN is NaN): zero them
-            uint8_t* vt = stages + ((gall + j) % kStages) * Lay::kStageBytes + Lay::kTileBytes;
+            // V rows past the last key may hold anything (0 x NaN is NaN): zero
+            // them, once the tile's V copies have landed
+            const int gv = gall + 2 * j + 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&slot_full[gv % S], (gv / S) & 1))) {
+              ok = false;
+              break;
+            }
+            uint8_t* vt = slots + (gv % S) * Lay::kSlotBytes;
             const int valid = sh.kv_end - key0;
             for (int idx = r; idx < NH * kKeys; idx += kRows) {
               const int kr = idx % kKeys, h = idx / kKeys;
@@ -588,23 +618,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&p_full[b]);
+        mbar_arrive(p_full);
       }
       if (!ok) break;
       gt += n_my;
       if (n_my > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gt - 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
         float o[D];
+        {
+          uint32_t raw[D];
+          if constexpr (D == 128) tmem_ld128(tl + 128, raw);
+          else tmem_ld64(tl + 128, raw);
 #pragma unroll
-        for (int h = 0; h < D / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(tl + 128 + h * 32, raw);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[h * 32 + i] = __uint_as_float(raw[i]);
+          for (int i = 0; i < D; ++i) o[i] = __uint_as_float(raw[i]);
         }
         tc_fence_before();
         mbar_arrive(o_free);                                 // the output columns may be reused
@@ -616,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (static_cast<int64_t>(it.qs + tok) * p.num_heads + head) * D, o, D);
         }
       }
-      gall += sh.n_tiles;
+      gall += 2 * sh.n_tiles;
       if (partial_end) ++ntail;
     }
     if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -689,7 +719,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_EINVAL;
 
-  const int box_rows = std::min(block_size, prefill::kKeys);
+  const int box_rows = std::min(block_size, 64);
   CUtensorMap tk, tv;
   const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
   if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, kLineSwizzled) ||

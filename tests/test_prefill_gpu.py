@@ -10,7 +10,7 @@ import torch
 import paged_kv_cache_118_gb300 as pk
 from oracle.pipeline import build_decode_state, pool_demand
 from oracle.prefill import paged_attention_prefill
-from parity import TORCH_DTYPE, assert_close, dev, gpu_decode_state
+from parity import TORCH_DTYPE, assert_close, dev, gpu_decode_state, record_max_err
 from workloads import decode_batch, free_order, normal_bits, poison_bits
 
 pytestmark = pytest.mark.gpu
@@ -59,7 +59,9 @@ def _run(case, seed=0):
                                        max(chunks), B, float(batch.scale), workspace=ws,
                                        err_flag=cache.err)
         torch.cuda.synchronize()
-        assert_close(out, want, dt)
+        err = assert_close(out, want, dt)
+        record_max_err(f"prefill {dt} lens={lens} chunks={chunks} H={H}/{Hkv} d={D} B={B} "
+                       f"({'fp32' if od == torch.float32 else dt} out)", err)
         if od == torch.float32:
             # the same call again, bit for bit, whichever CTA claims which item
             again = torch.empty_like(out)
