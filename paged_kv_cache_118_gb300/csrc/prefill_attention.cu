@@ -60,7 +60,8 @@ namespace prefill {
 constexpr int kRows = 128;             // query rows of one query tile: the TMEM lanes
 constexpr int kQTiles = 2;             // query tiles per item, sharing every K/V tile
 constexpr int kKeys = 128;             // keys per tile
-constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: items, copies; warp 1: MMA; 4 warps per query tile
+constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: items, copies; warp 1: MMA; warps 2-3: Q; 4 warps per query tile
+constexpr int kQLoaders = 64;                   // warps 2 and 3
 constexpr int kSoftmaxWarp0 = 4;
 // per query tile t, from column 256 t: S (P over it) [0, 128), O [128, 128 + D)
 constexpr uint32_t kTmemCols = 256 * kQTiles;
@@ -225,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], kQTiles * kRows + 1);   // the softmax threads and the MMA thread
+      mbar_init(&item_empty[i], kQTiles * kRows + 1 + kQLoaders);   // softmax, MMA and Q threads
     }
-    mbar_init(q_full, kQTiles * kRows);
+    mbar_init(q_full, kQLoaders);
     mbar_init(q_free, 1);
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&tbars[4 * t], 1);              // s_full
@@ -403,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // S of the first key tile; the S columns are free: every softmax
-        // thread read back its tile's output (after the tile's last P V)
-        // before it wrote this item's query rows
+        // S of the first key tile: it follows the previous item's last P V
+        // of each query tile (which read P there), and that P V's softmax
+        // threads are done with the scores
         if (!slot_landed(g)) {
           ok = false;
           break;
@@ -466,7 +467,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain);
       if (!mbar_wait(drain, 0)) flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp >= kSoftmaxWarp0) {
+  } else if (warp < kSoftmaxWarp0) {
+    // ---------------------------------------------------------- query rows
+    // Warps 2 and 3 copy each item's 256 query rows into the A layout of S
+    // (zeros past the chunk) as soon as the previous item's S products are
+    // done, while the softmax threads still finish that item.
+    const int qt = threadIdx.x - 64;
+    const int tok_per_qt = kRows / G;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&item_full[slot], (k >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const Item it = items[slot];
+      mbar_arrive(&item_empty[slot]);
+      if (it.seq < 0) break;
+      if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(q_free, (k - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      // 16-byte chunk c of row rr of query tile t; the row's token and head
+      for (int idx = qt; idx < kQTiles * kRows * (D / 8); idx += kQLoaders) {
+        const int c = idx % (D / 8), rt = idx / (D / 8);
+        const int t = rt / kRows, rr = rt % kRows;
+        const int tok = it.qb * kQTiles * tok_per_qt + t * tok_per_qt + rr / G;
+        const int head = it.kvh * G + rr % G;
+        const bool live = tok < it.C;
+        const uint16_t* src =
+            live ? p.q + (static_cast<int64_t>(it.qs + tok) * p.num_heads + head) * D + c * 8 : p.q;
+        cp_async16(qtiles + t * Lay::kQBytes + (c >> 3) * kRows * 128 + rr * 128 +
+                       (((c & 7) ^ (rr & 7)) << 4),
+                   src, live ? 16u : 0u);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+  } else {
     // ---------------------------------------------------------- softmax
     const int t = (warp - kSoftmaxWarp0) >> 2;             // query tile
     const int r = ((warp - kSoftmaxWarp0) & 3) * 32 + lane;   // row of the tile = TMEM lane
@@ -475,7 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 1;
     uint64_t* pv_done = s_full + 2;
     uint64_t* o_free = s_full + 3;
-    uint8_t* qtile = qtiles + t * Lay::kQBytes;
     const int tok_per_qt = kRows / G;
     int gt = 0;                                            // key tiles this query tile read, over all items
     int gall = 0;                                          // slots of the CTA, over all items
@@ -496,24 +535,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = it.kvh * G + r % G;
       const bool live = tok < it.C;
       const int pos = it.L - it.C + tok;
-      // this row of Q into the A layout of S (zeros past the chunk), once the
-      // previous item's S products have read the tile
-      if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(q_free, (k - 1) & 1))) {
-        ok = false;
-        break;
-      }
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<int64_t>(it.qs + (live ? tok : 0)) * p.num_heads + head) * D);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const int h = c >> 3, cc = c & 7;
-          uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(qtile + h * kRows * 128 + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(q_full);
-      }
       const bool partial_end = sh.kv_end % kKeys != 0;     // the item's last key tile is partial
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n_my; ++j) {
