@@ -945,9 +945,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--op", choices=["decode", "swap", "blockmgr", "prefill"], default="decode",
+    ap.add_argument("--op", choices=["decode", "swap", "blockmgr", "prefill", "tiny"],
+                    default="decode",
                     help="decode: the headline measurement; swap: swap_blocks bandwidth; "
-                         "blockmgr: host costs of the block manager")
+                         "blockmgr: host costs of the block manager; prefill: chunked-prefill "
+                         "attention; tiny: decode-call latency of the tiny batch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -964,6 +966,10 @@ def main():
     if args.op == "blockmgr":
         if rank == 0:
             print(json.dumps(run_blockmgr(args)), flush=True)
+        return
+    if args.op == "tiny":
+        if rank == 0:
+            print(json.dumps(run_tiny(args)), flush=True)
         return
 
     if args.impl == "reference":
