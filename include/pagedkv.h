@@ -196,7 +196,8 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, int out_dtype, const vo
  *   out, q        device, [total_queries][num_heads][head_size] (out_dtype / kv_dtype)
  *   caches, tables, context_lens  as for pkv_paged_attention_decode
  *   query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
- *   max_query_len host int >= every C (sizes the grid)
+ *   max_query_len host int >= every C (sizes the work list)
+ *   total_queries host int, rows of q and out
  *   head_size 64 or 128; block_size a power of two from 8 to 256;
  *   128 % (num_heads / num_kv_heads) == 0; scale > 0
  *   workspace     device, >= pkv_prefill_workspace_size() bytes, 16-byte
@@ -207,9 +208,10 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, int out_dtype, const vo
  * Work: one item per 256 query rows (chunk tokens x the KV head's query
  * heads), KV head and sequence; at most one CTA per SM takes items, those
  * with the most keys first.
- * Device checks: 0 <= C <= min(L, max_query_len) and L <= max_blocks_per_seq *
- * block_size, else the sequence is skipped (its rows untouched) and
- * PKV_DEVERR_CONTEXT set; bad block ids as for decode.
+ * Device checks: 0 <= C <= min(L, max_query_len), L <= max_blocks_per_seq *
+ * block_size and query_start[s] + C <= total_queries, else the sequence is
+ * skipped (its rows untouched) and PKV_DEVERR_CONTEXT set; bad block ids as
+ * for decode.
  * Errors: PKV_EINVAL (also a missing, short or unaligned workspace),
  * PKV_ECUDA.
  * ------------------------------------------------------------------------ */
@@ -220,8 +222,8 @@ pkv_status pkv_paged_attention_prefill(void* out, int out_dtype, const void* q,
                                        const int32_t* query_start, int num_seqs, int num_heads,
                                        int num_kv_heads, int head_size, int num_blocks,
                                        int block_size, int max_blocks_per_seq, int max_query_len,
-                                       float scale, void* workspace, size_t workspace_bytes,
-                                       int32_t* err_flag, void* stream);
+                                       int total_queries, float scale, void* workspace,
+                                       size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* ------------------------------------------------------------------------
  * reshape_and_cache: write new tokens' keys and values into their slots.

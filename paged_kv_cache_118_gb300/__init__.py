@@ -48,7 +48,7 @@ SIGNATURES = {
     "pkv_prefill_workspace_size": (_c_sz, []),
     "pkv_paged_attention_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _vp,
                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                             _c_int, _c_int, _c_f, _vp, _c_sz, _vp, _vp]),
+                                             _c_int, _c_int, _c_int, _c_f, _vp, _c_sz, _vp, _vp]),
     "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _vp, _vp]),
     "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_sz, _vp]),
@@ -334,8 +334,8 @@ def pkv_paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: tor
     st = lib.pkv_paged_attention_prefill(
         _ptr(out), _DTYPE[out.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache), _DTYPE[q.dtype],
         _ptr(block_tables), _ptr(context_lens), _ptr(query_start), context_lens.shape[0], H,
-        Hkv, D, nb, block_size, block_tables.shape[1], int(max_query_len), float(scale),
-        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream))
+        Hkv, D, nb, block_size, block_tables.shape[1], int(max_query_len), q.shape[0],
+        float(scale), _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(stream))
     _check(st, "pkv_paged_attention_prefill")
 
 

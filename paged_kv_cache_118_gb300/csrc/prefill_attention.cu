@@ -85,6 +85,7 @@ struct Params {
   int block_size;
   int max_blocks_per_seq;
   int max_query_len;
+  int total_queries;                   // rows of q and out
   int qblocks;                         // 256-row query blocks of the longest chunk
   int total_items;                     // qblocks * num_seqs * num_kv_heads
   int box_rows;                        // rows per TMA copy: min(block_size, 64)
@@ -286,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qs = __shfl_sync(0xffffffffu, v, 0);
         const int C = __shfl_sync(0xffffffffu, v, 1) - qs;
         const int L = __shfl_sync(0xffffffffu, v, 2);
-        if (C < 0 || C > p.max_query_len || C > L || L > max_ctx) {
+        if (C < 0 || C > p.max_query_len || C > L || L > max_ctx || qs < 0 ||
+            qs > p.total_queries - C) {
           if (lane == 0 && qb == 0 && kvh == 0 && C != 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
           continue;
         }
@@ -711,8 +713,8 @@ extern "C" pkv_status pkv_paged_attention_prefill(
     void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
     int kv_dtype, const int32_t* block_tables, const int32_t* context_lens,
     const int32_t* query_start, int num_seqs, int num_heads, int num_kv_heads, int head_size,
-    int num_blocks, int block_size, int max_blocks_per_seq, int max_query_len, float scale,
-    void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream) {
+    int num_blocks, int block_size, int max_blocks_per_seq, int max_query_len, int total_queries,
+    float scale, void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream) {
   if (num_seqs < 0 || num_seqs > 65535) return PKV_EINVAL;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
@@ -728,7 +730,8 @@ extern "C" pkv_status pkv_paged_attention_prefill(
   if (prefill::kRows % group != 0) return PKV_EINVAL;
   if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0)
     return PKV_EINVAL;
-  if (num_blocks < 1 || max_blocks_per_seq < 1 || max_query_len < 1) return PKV_EINVAL;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || max_query_len < 1 || total_queries < 0)
+    return PKV_EINVAL;
   if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PKV_EINVAL;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT32_MAX / 2) return PKV_EINVAL;
   // work items: 256-row query blocks x sequences x KV heads, counted in an int
@@ -763,6 +766,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(
   p.block_size = block_size;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_query_len = max_query_len;
+  p.total_queries = total_queries;
   p.qblocks = static_cast<int>(qblocks);
   p.total_items = static_cast<int>(items);
   p.box_rows = box_rows;

@@ -125,12 +125,13 @@ def test_reshape_and_cache_host_validation():
 
 def _prefill_status(**over):
     a = dict(out=16, out_dtype=0, q=16, k=16, v=16, kv_dtype=0, bt=16, cl=16, qs=16, S=2, H=8,
-             Hkv=8, D=128, nb=8, B=16, mb=4, mq=64, scale=0.125, ws=16, ws_bytes=16, err=None)
+             Hkv=8, D=128, nb=8, B=16, mb=4, mq=64, tq=64, scale=0.125, ws=16, ws_bytes=16,
+             err=None)
     a.update(over)
     return pk.lib.pkv_paged_attention_prefill(a["out"], a["out_dtype"], a["q"], a["k"], a["v"],
                                               a["kv_dtype"], a["bt"], a["cl"], a["qs"], a["S"],
                                               a["H"], a["Hkv"], a["D"], a["nb"], a["B"], a["mb"],
-                                              a["mq"], a["scale"], a["ws"], a["ws_bytes"],
+                                              a["mq"], a["tq"], a["scale"], a["ws"], a["ws_bytes"],
                                               a["err"], None)
 
 
@@ -138,7 +139,7 @@ def _prefill_status(**over):
     dict(q=None), dict(qs=None), dict(kv_dtype=2), dict(out_dtype=7), dict(D=96), dict(B=4),
     dict(B=12), dict(B=512), dict(H=24, Hkv=8), dict(H=6, Hkv=4), dict(mq=0), dict(S=-1),
     dict(scale=0.0), dict(scale=-0.125), dict(scale=float("inf")), dict(out=24),
-    dict(ws=None), dict(ws=24), dict(ws_bytes=8)])
+    dict(ws=None), dict(ws=24), dict(ws_bytes=8), dict(tq=-1)])
 def test_prefill_rejects_bad_arguments_on_host(over):
     """Host checks: head size 64/128, block sizes 8..256 (powers of two), a
     query-head group that divides the 128 rows of a query tile, a positive

@@ -91,3 +91,20 @@ def test_bad_chunk_is_reported_and_skipped():
     assert cache.err.item() & pk.PKV_DEVERR_CONTEXT
     assert torch.all(out[10:] == 0) and torch.all(torch.isfinite(out[:10]))
     assert not torch.all(out[:10] == 0)
+
+
+def test_rows_past_the_end_of_q_are_reported_and_skipped():
+    """A chunk whose rows would run past the end of q (query_start[s] + C >
+    the rows of q) is skipped and reported; the other sequences are computed."""
+    batch = decode_batch("p", (40, 100), 4, 4, 64, 16, "f16", seed=3)
+    n = pool_demand(batch.context_lens, 16) + 2
+    cache, tables, ctx = gpu_decode_state(batch, n, free_order(n, 1))
+    starts = torch.tensor([0, 10, 70], dtype=torch.int32, device="cuda")   # 70 > 65 rows
+    q = torch.randn(65, 4, 64, dtype=torch.float16, device="cuda")
+    out = torch.zeros_like(q)
+    pk.pkv_paged_attention_prefill(out, q, cache.k_cache, cache.v_cache, tables, ctx, starts,
+                                   60, 16, 0.125, err_flag=cache.err)
+    torch.cuda.synchronize()
+    assert cache.err.item() & pk.PKV_DEVERR_CONTEXT
+    assert torch.all(out[10:] == 0) and torch.all(torch.isfinite(out[:10]))
+    assert not torch.all(out[:10] == 0)
