@@ -588,18 +588,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mn;
         }
         // p = 2^(scale s - m): a masked score is -inf and gives 0 (m is finite
-        // on a live row from its first tile on; a row past the chunk writes 0);
-        // P goes over the scores as 16-bit pairs in one store; bf16 P also
-        // keeps its rounding error (p - hi) in the next 64 columns, read by a
-        // second P V
+        // on a live row from its first tile on; a row past the chunk has only
+        // -inf scores and nm = 0, so it writes 0 without a select); P goes
+        // over the scores as 16-bit pairs in one store; bf16 P also keeps its
+        // rounding error (p - hi) in the next 64 columns, read by a second
+        // P V. This loop is bound by instruction issue, so the scale, the
+        // shift and the row sum run as packed f32x2 pairs.
         const float nm = live ? -m : 0.f;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const f32x2 sc2 = pack2(p.q_scale, p.q_scale), nm2 = pack2(nm, nm);
+        f32x2 ls2[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
         uint32_t pk[kKeys / 2];
 #pragma unroll
         for (int i = 0; i < kKeys; i += 2) {
-          const float e0 = live ? ex2(fmaf(__uint_as_float(sc[i]), p.q_scale, nm)) : 0.f;
-          const float e1 = live ? ex2(fmaf(__uint_as_float(sc[i + 1]), p.q_scale, nm)) : 0.f;
-          ls[(i >> 1) & 3] += e0 + e1;
+          float x0, x1;
+          unpack2(fma2(pack2_bits(sc[i], sc[i + 1]), sc2, nm2), x0, x1);
+          const float e0 = ex2(x0);
+          const float e1 = ex2(x1);
+          ls2[(i >> 1) & 1] = add2(ls2[(i >> 1) & 1], pack2(e0, e1));
           pk[i >> 1] = T::pack(e0, e1);
           if constexpr (kBF16) {
             const float2 h = T::to_float2(pk[i >> 1]);
@@ -613,7 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < kKeys / 2; ++i) pl[i] = sc[i];
           tmem_st64(tl + kKeys / 2, pl);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        float l0, l1;
+        unpack2(add2(ls2[0], ls2[1]), l0, l1);
+        l += l0 + l1;
         if (j == sh.n_tiles - 1 && partial_end) {
           if (t == sh.zt) {
             // V rows past the last key may hold anything (0 x NaN is NaN): zero
