@@ -658,32 +658,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         // p = 2^(scale s - m) on this copy's keys, 0 on the others' (a slice
         // with no key yet keeps m = -inf and gives 0)
         const float nm = m == -INFINITY ? 0.f : -m;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const f32x2 sc2 = pack2(p.q_scale, p.q_scale), nm2 = pack2(nm, nm), neg1 = pack2(-1.f, -1.f);
+        f32x2 ls2[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
         uint32_t vh[KC / 2], vl[KC / 2];
 #pragma unroll
         for (int e = 0; e < KC; e += 2) {
-          const float e0 = ex2(fmaf(s[e], p.q_scale, nm));
-          const float e1 = ex2(fmaf(s[e + 1], p.q_scale, nm));
-          ls[(e >> 1) & 3] += e0 + e1;
+          float x0, x1;
+          unpack2(fma2(pack2(s[e], s[e + 1]), sc2, nm2), x0, x1);
+          const float e0 = ex2(x0);
+          const float e1 = ex2(x1);
+          const f32x2 ee = pack2(e0, e1);
+          ls2[(e >> 1) & 1] = add2(ls2[(e >> 1) & 1], ee);
           vh[e >> 1] = T::pack(e0, e1);
           if constexpr (kBF16) {
-            const float2 h = T::to_float2(vh[e >> 1]);
-            vl[e >> 1] = T::pack(e0 - h.x, e1 - h.y);
+            float d0, d1;
+            unpack2(fma2(T::to_pair(vh[e >> 1]), neg1, ee), d0, d1);
+            vl[e >> 1] = T::pack(d0, d1);
           }
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        {
+          float l0, l1;
+          unpack2(add2(ls2[0], ls2[1]), l0, l1);
+          l += l0 + l1;
+        }
         // P as 16-bit pairs over the first 32 columns of the scores; bf16 P also
         // keeps its rounding error (p - hi) in the next 32, read by a second P V
-        uint32_t pk[kKeys / 2], pl[kKeys / 2];
+        if constexpr (C == 2) {
+          // this copy's 16 columns, and zeros over the other copy's
+          uint32_t zero[KC / 2];
 #pragma unroll
-        for (int cc = 0; cc < C; ++cc)
-#pragma unroll
-          for (int e = 0; e < KC / 2; ++e) {
-            pk[cc * KC / 2 + e] = cp == cc ? vh[e] : 0u;
-            if constexpr (kBF16) pl[cc * KC / 2 + e] = cp == cc ? vl[e] : 0u;
+          for (int e = 0; e < KC / 2; ++e) zero[e] = 0u;
+          tmem_st16_issue(tl + b * kKeys + cp * (KC / 2), vh);
+          tmem_st16_issue(tl + b * kKeys + (1 - cp) * (KC / 2), zero);
+          if constexpr (kBF16) {
+            tmem_st16_issue(tl + b * kKeys + kKeys / 2 + cp * (KC / 2), vl);
+            tmem_st16_issue(tl + b * kKeys + kKeys / 2 + (1 - cp) * (KC / 2), zero);
           }
-        tmem_st32(tl + b * kKeys, pk);                      // over the scores of this tile
-        if constexpr (kBF16) tmem_st32(tl + b * kKeys + kKeys / 2, pl);
+          tmem_wait_st();
+        } else {
+          uint32_t pk[kKeys / 2], pl[kKeys / 2];
+#pragma unroll
+          for (int cc = 0; cc < C; ++cc)
+#pragma unroll
+            for (int e = 0; e < KC / 2; ++e) {
+              pk[cc * KC / 2 + e] = cp == cc ? vh[e] : 0u;
+              if constexpr (kBF16) pl[cc * KC / 2 + e] = cp == cc ? vl[e] : 0u;
+            }
+          tmem_st32(tl + b * kKeys, pk);                    // over the scores of this tile
+          if constexpr (kBF16) tmem_st32(tl + b * kKeys + kKeys / 2, pl);
+        }
         if (tile_valid < kKeys) {
           // V rows past the last key may hold anything (0 x NaN is NaN): zero them
           uint8_t* vt = stages + (g % kStages) * Lay::kStageBytes + Lay::kTileBytes;
