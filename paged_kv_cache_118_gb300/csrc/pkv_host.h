@@ -38,6 +38,13 @@ bool encode_cache_map(CUtensorMap* tm, const void* base, int D, int num_kv_heads
 // line of box_rows consecutive rows per copy.
 bool encode_query_map(CUtensorMap* tm, const void* base, int D, int64_t rows, int box_rows);
 
+// TMA map of packed queries [tokens][num_heads][D] (16-bit elements) as (64
+// elements, D/64 lines, head, token) with the box 64 x 1 x group x 128/group
+// and the 128-byte swizzle: one line of 128 rows (token-major, head-minor) of
+// one KV head's query group per copy; tokens past the end read as zeros.
+bool encode_token_query_map(CUtensorMap* tm, const void* base, int D, int num_heads,
+                            int64_t tokens, int group);
+
 struct DecodeTcArgs {
   float* part_acc;
   float2* part_ml;

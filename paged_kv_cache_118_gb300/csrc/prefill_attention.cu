@@ -24,13 +24,13 @@
 //    buffer and the D-column output) and issues, from one thread,
 //    S = Q K^T (M = 128, N = 128, K = D) and O += P V (M = 128, N = D,
 //    K = 128, P read from tensor memory), each followed by a commit to an
-//    mbarrier; a query tile's next S follows its P V, so one tile's
-//    softmax runs while the other tile's products are computed. A product
-//    issue costs one thread tens of cycles whatever its size, so the
-//    products are made as wide as tensor memory allows;
+//    mbarrier; a query tile's next S follows its P V. A product issue
+//    costs one thread tens of cycles whatever its size, so the products
+//    are made as wide as tensor memory allows;
+//  * one thread of warp 2 loads each item's query rows by TMA once the
+//    previous item's S products are done;
 //  * a softmax warpgroup per query tile, one thread per query row (its TMEM
-//    lane): it writes the row's query into shared memory once the previous
-//    item's S products are done; it reads the row's 128 scores from tensor
+//    lane): it reads the row's 128 scores from tensor
 //    memory in one load (a tensor-memory round trip costs hundreds of
 //    cycles under load, so a tile takes one load and one store), runs a
 //    base-2 online softmax with lazy rescale (the output row is rescaled in
@@ -60,8 +60,7 @@ namespace prefill {
 constexpr int kRows = 128;             // query rows of one query tile: the TMEM lanes
 constexpr int kQTiles = 2;             // query tiles per item, sharing every K/V tile
 constexpr int kKeys = 128;             // keys per tile
-constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: items, copies; warp 1: MMA; warps 2-3: Q; 4 warps per query tile
-constexpr int kQLoaders = 64;                   // warps 2 and 3
+constexpr int kThreads = 128 + kQTiles * 128;   // warp 0: items, K/V; warp 1: MMA; warp 2: Q; 4 warps per query tile
 constexpr int kSoftmaxWarp0 = 4;
 // per query tile t, from column 256 t: S (P over it) [0, 128), O [128, 128 + D)
 constexpr uint32_t kTmemCols = 256 * kQTiles;
@@ -193,7 +192,7 @@ __device__ __forceinline__ void store_row(void* out, int out_dtype, int64_t base
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tm_q, const Params p) {
   using Lay = Layout<D>;
   constexpr int NH = Lay::NH;
   constexpr int S = Lay::kSlots;
@@ -227,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], kQTiles * kRows + 1 + kQLoaders);   // softmax, MMA and Q threads
+      mbar_init(&item_empty[i], kQTiles * kRows + 2);   // the softmax, MMA and query threads
     }
-    mbar_init(q_full, kQLoaders);
+    mbar_init(q_full, 1);
     mbar_init(q_free, 1);
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&tbars[4 * t], 1);              // s_full
@@ -469,46 +468,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain);
       if (!mbar_wait(drain, 0)) flag_error(p.err, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp < kSoftmaxWarp0) {
+  } else if (warp == 2) {
     // ---------------------------------------------------------- query rows
-    // Warps 2 and 3 copy each item's 256 query rows into the A layout of S
-    // (zeros past the chunk) as soon as the previous item's S products are
-    // done, while the softmax threads still finish that item.
-    const int qt = threadIdx.x - 64;
-    const int tok_per_qt = kRows / G;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int slot = k & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&item_full[slot], (k >> 1) & 1))) {
-        ok = false;
-        break;
+    // One thread copies each item's 256 query rows into the A layout of S by
+    // TMA (four boxes at d = 128: two query tiles x two 64-element lines) as
+    // soon as the previous item's S products are done, while the softmax
+    // threads still finish that item. Rows past the chunk read the next
+    // tokens' queries (or zeros past the last token): they are masked out.
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      const uint64_t policy = l2_evict_first_policy();
+      const int tok_per_qt = kRows / G;
+      bool ok = true;
+      int issued = 0;                                       // items whose query rows were loaded
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait(&item_full[slot], (k >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const Item it = items[slot];
+        mbar_arrive(&item_empty[slot]);
+        if (it.seq < 0) break;
+        if (k >= 1 && !mbar_wait(q_free, (k - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        ++issued;
+        mbar_arrive_expect_tx(q_full, kQTiles * Lay::kQBytes);
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t)
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            tma_load_4d(qtiles + t * Lay::kQBytes + h * kRows * 128, &tm_q, q_full, 0, h, it.kvh * G,
+                        it.qs + it.qb * kQTiles * tok_per_qt + t * tok_per_qt, policy);
       }
-      const Item it = items[slot];
-      mbar_arrive(&item_empty[slot]);
-      if (it.seq < 0) break;
-      if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(q_free, (k - 1) & 1))) {
-        ok = false;
-        break;
+      if (!ok) {
+        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+        // let the last copy in flight land before the CTA leaves
+        if (issued > 0) mbar_wait(q_full, (issued - 1) & 1);
       }
-      // 16-byte chunk c of row rr of query tile t; the row's token and head
-      for (int idx = qt; idx < kQTiles * kRows * (D / 8); idx += kQLoaders) {
-        const int c = idx % (D / 8), rt = idx / (D / 8);
-        const int t = rt / kRows, rr = rt % kRows;
-        const int tok = it.qb * kQTiles * tok_per_qt + t * tok_per_qt + rr / G;
-        const int head = it.kvh * G + rr % G;
-        const bool live = tok < it.C;
-        const uint16_t* src =
-            live ? p.q + (static_cast<int64_t>(it.qs + tok) * p.num_heads + head) * D + c * 8 : p.q;
-        cp_async16(qtiles + t * Lay::kQBytes + (c >> 3) * kRows * 128 + rr * 128 +
-                       (((c & 7) ^ (rr & 7)) << 4),
-                   src, live ? 16u : 0u);
-      }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      mbar_arrive(q_full);
     }
-    if (!ok) flag_error(p.err, PKV_DEVERR_TIMEOUT);
-  } else {
+  } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- softmax
     const int t = (warp - kSoftmaxWarp0) >> 2;             // query tile
     const int r = ((warp - kSoftmaxWarp0) & 3) * 32 + lane;   // row of the tile = TMEM lane
@@ -690,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, typename T>
-static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Params& p,
-                          cudaStream_t s) {
+static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                          const Params& p, cudaStream_t s) {
   auto kern = prefill_kernel<D, T>;
   // one CTA per SM: it holds all 512 tensor-memory columns, so shared memory is
   // requested past half an SM even where the layout needs less (d = 64)
@@ -705,7 +706,7 @@ static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Pa
   e = cudaMemsetAsync(p.counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.total_items, sms);           // persistent: one CTA per SM at most
-  kern<<<grid, kThreads, kSmemLaunch, s>>>(tk, tv, p);
+  kern<<<grid, kThreads, kSmemLaunch, s>>>(tk, tv, tq, p);
   return cudaGetLastError();
 }
 
@@ -751,10 +752,12 @@ extern "C" pkv_status pkv_paged_attention_prefill(
     return PKV_EINVAL;
 
   const int box_rows = std::min(block_size, 64);
-  CUtensorMap tk, tv;
+  if (total_queries == 0) return PKV_OK;                  // no chunk has a row
+  CUtensorMap tk, tv, tq;
   const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
   if (!encode_cache_map(&tk, k_cache, head_size, num_kv_heads, slots, box_rows, kLineSwizzled) ||
-      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, kLineSwizzled))
+      !encode_cache_map(&tv, v_cache, head_size, num_kv_heads, slots, box_rows, kLineSwizzled) ||
+      !encode_token_query_map(&tq, q, head_size, num_heads, total_queries, group))
     return PKV_ECUDA;
   prefill::Params p{};
   p.out = out;
@@ -781,10 +784,10 @@ extern "C" pkv_status pkv_paged_attention_prefill(
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (head_size == 128)
-    e = kv_dtype == PKV_F16 ? prefill::launch<128, F16>(tk, tv, p, s)
-                            : prefill::launch<128, BF16>(tk, tv, p, s);
+    e = kv_dtype == PKV_F16 ? prefill::launch<128, F16>(tk, tv, tq, p, s)
+                            : prefill::launch<128, BF16>(tk, tv, tq, p, s);
   else
-    e = kv_dtype == PKV_F16 ? prefill::launch<64, F16>(tk, tv, p, s)
-                            : prefill::launch<64, BF16>(tk, tv, p, s);
+    e = kv_dtype == PKV_F16 ? prefill::launch<64, F16>(tk, tv, tq, p, s)
+                            : prefill::launch<64, BF16>(tk, tv, tq, p, s);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

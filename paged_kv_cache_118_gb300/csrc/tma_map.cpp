@@ -121,4 +121,25 @@ bool encode_query_map(CUtensorMap* tm, const void* base, int D, int64_t rows, in
   return true;
 }
 
+bool encode_token_query_map(CUtensorMap* tm, const void* base, int D, int num_heads,
+                            int64_t tokens, int group) {
+  const MapKey key{base, tokens, D, num_heads, group, -2};
+  if (cached_map(key, tm)) return true;
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(num_heads),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(num_heads) * D * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  remember_map(key, *tm);
+  return true;
+}
+
 }  // namespace pkv
