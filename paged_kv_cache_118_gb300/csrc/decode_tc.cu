@@ -733,16 +733,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t prow = (static_cast<int64_t>(info.seq) * p.num_heads + info.kvh * G + hr) *
                                p.max_parts + info.part;
       if constexpr (C == 1) {
+        uint32_t raw[D];                                    // one tensor-memory round trip
+        if constexpr (D == 128) tmem_ld128(to, raw);
+        else tmem_ld64(to, raw);
+        float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D);
 #pragma unroll
-        for (int h = 0; h < D / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(to + h * 32, raw);
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + h * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(raw[4 * e]), __uint_as_float(raw[4 * e + 1]),
-                                 __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
-        }
+        for (int e = 0; e < D / 4; ++e)
+          dst[e] = make_float4(__uint_as_float(raw[4 * e]), __uint_as_float(raw[4 * e + 1]),
+                               __uint_as_float(raw[4 * e + 2]), __uint_as_float(raw[4 * e + 3]));
         p.part_ml[prow] = make_float2(m, l);
       } else if constexpr (C == 2) {
         // Copy c merges and writes the half [c D/2, (c + 1) D/2) of the head's
@@ -752,12 +750,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         float* out_row = merge + (cp * G + hr) * Lay::kMergeStride;
+        {
+          uint32_t raw[Lay::kHalf];                        // one tensor-memory round trip
+          if constexpr (Lay::kHalf == 64) tmem_ld64(to + (1 - cp) * Lay::kHalf, raw);
+          else tmem_ld32(to + (1 - cp) * Lay::kHalf, raw);
 #pragma unroll
-        for (int h = 0; h < Lay::kHalf / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(to + (1 - cp) * Lay::kHalf + h * 32, raw);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) out_row[h * 32 + e] = __uint_as_float(raw[e]);
+          for (int e = 0; e < Lay::kHalf; ++e) out_row[e] = __uint_as_float(raw[e]);
         }
         mrg_ml[cp * G + hr] = make_float2(m, l);
         mbar_arrive(mrg_full);
@@ -771,17 +769,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float fm = m == -INFINITY ? 0.f : ex2(m - M);
         const float fo = mo.x == -INFINITY ? 0.f : ex2(mo.x - M);
         if (cp == 0) p.part_ml[prow] = make_float2(M, fmaf(mo.y, fo, l * fm));
+        {
+          uint32_t raw[Lay::kHalf];
+          if constexpr (Lay::kHalf == 64) tmem_ld64(to + cp * Lay::kHalf, raw);
+          else tmem_ld32(to + cp * Lay::kHalf, raw);
+          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + cp * Lay::kHalf);
 #pragma unroll
-        for (int h = 0; h < Lay::kHalf / 32; ++h) {
-          uint32_t raw[32];
-          tmem_ld32(to + cp * Lay::kHalf + h * 32, raw);
-          float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * D + cp * Lay::kHalf + h * 32);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < Lay::kHalf / 4; ++j) {
             float o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              o[i] = fmaf(in_row[h * 32 + 4 * j + i], fo, __uint_as_float(raw[4 * j + i]) * fm);
+              o[i] = fmaf(in_row[4 * j + i], fo, __uint_as_float(raw[4 * j + i]) * fm);
             dst[j] = make_float4(o[0], o[1], o[2], o[3]);
           }
         }
