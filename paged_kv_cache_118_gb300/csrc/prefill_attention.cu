@@ -152,7 +152,31 @@ struct Layout {
 template <typename T>
 __device__ __forceinline__ void store_row(void* out, int out_dtype, int64_t base, const float* v,
                                           int n) {
-  // n values of one output row, 16 bytes at a time
+  // n values of one output row, 32 bytes per store where the output is
+  // 32-byte aligned (the ABI asks for 16), else 16 bytes per store
+  if ((reinterpret_cast<uintptr_t>(out) & 31) == 0) {
+    if (out_dtype == PKV_F32) {
+      float* d = static_cast<float*>(out) + base;
+      for (int i = 0; i < n / 8; ++i)
+        asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d + 8 * i),
+                     "f"(v[8 * i]), "f"(v[8 * i + 1]), "f"(v[8 * i + 2]), "f"(v[8 * i + 3]),
+                     "f"(v[8 * i + 4]), "f"(v[8 * i + 5]), "f"(v[8 * i + 6]), "f"(v[8 * i + 7])
+                     : "memory");
+    } else {
+      uint16_t* d = static_cast<uint16_t*>(out) + base;
+      for (int i = 0; i < n / 16; ++i) {
+        uint32_t w[8];
+        for (int j = 0; j < 8; ++j)
+          w[j] = out_dtype == PKV_F16 ? F16::pack(v[16 * i + 2 * j], v[16 * i + 2 * j + 1])
+                                      : BF16::pack(v[16 * i + 2 * j], v[16 * i + 2 * j + 1]);
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d + 16 * i),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                     "r"(w[7])
+                     : "memory");
+      }
+    }
+    return;
+  }
   if (out_dtype == PKV_F32) {
     float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
     for (int i = 0; i < n / 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);

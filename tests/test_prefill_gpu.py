@@ -108,3 +108,25 @@ def test_rows_past_the_end_of_q_are_reported_and_skipped():
     assert cache.err.item() & pk.PKV_DEVERR_CONTEXT
     assert torch.all(out[10:] == 0) and torch.all(torch.isfinite(out[:10]))
     assert not torch.all(out[:10] == 0)
+
+
+@pytest.mark.parametrize("od", [torch.float16, torch.float32])
+def test_output_aligned_to_16_bytes_only(od):
+    """An output 16-byte but not 32-byte aligned takes the 16-byte stores: the
+    same values, bit for bit, as a 32-byte aligned output."""
+    batch = decode_batch("p", (300, 129), 8, 2, 128, 16, "f16", seed=5)
+    n = pool_demand(batch.context_lens, 16) + 2
+    cache, tables, ctx = gpu_decode_state(batch, n, free_order(n, 2))
+    starts = torch.tensor([0, 100, 229], dtype=torch.int32, device="cuda")
+    q = torch.randn(229, 8, 128, dtype=torch.float16, device="cuda")
+    aligned = torch.empty(q.shape, dtype=od, device="cuda")
+    pad = 16 // aligned.element_size()
+    big = torch.empty(aligned.numel() + pad, dtype=od, device="cuda")
+    shifted = big[pad:].view(q.shape)
+    assert shifted.data_ptr() % 16 == 0 and shifted.data_ptr() % 32 != 0
+    for out in (aligned, shifted):
+        pk.pkv_paged_attention_prefill(out, q, cache.k_cache, cache.v_cache, tables, ctx, starts,
+                                       129, 16, float(batch.scale), err_flag=cache.err)
+    torch.cuda.synchronize()
+    assert cache.err.item() == 0
+    assert torch.equal(aligned, shifted)
