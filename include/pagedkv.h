@@ -105,7 +105,9 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, 
  * enough units to keep every SM busy (each unit then carries twice the keys
  * per merge): units = num_seqs * num_kv_heads * ceil(max context / 1024) at
  * least 1024 for query groups of 2 to 16 heads per KV head (block_size >= 8),
- * at least 256 for groups of 32, 64 or 128 heads (the tensor-memory path);
+ * at least 256 for groups of 32, 64 or 128 heads (the tensor-memory path),
+ * where 2048 is taken instead when num_seqs * num_kv_heads * ceil(max
+ * context / 2048) is at least 256 and 2048 / block_size is at most 254;
  * else 512, or 1024 when the tables can hold 32768 tokens or more (long
  * contexts then produce half as many partials). Never fails. */
 int pkv_decode_partition_tokens(int num_seqs, int num_heads, int num_kv_heads, int head_size,

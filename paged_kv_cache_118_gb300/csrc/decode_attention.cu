@@ -1455,7 +1455,10 @@ using namespace pkv;
 // for one merge, one partial and one claim. Measured, fraction of the HBM copy
 // rate: 0.82 against 0.80 on the 256-beam shared-prefix batch, 0.99 against
 // 0.95 on the long-context one, 0.42 against 0.38 with 64 query heads on one KV
-// head. Otherwise 512, or 1024 when the tables can hold 32K tokens or more.
+// head. On the tcgen05 path 2048 when even 2048-token units are that many
+// (and a partition's blocks fit its id buffer): 0.44 against 0.42 with 64
+// query heads on one KV head, back to back. Otherwise 512, or 1024 when the
+// tables can hold 32K tokens or more.
 constexpr int64_t kBigPartitionUnits = 1024;
 constexpr int64_t kBigPartitionUnitsTc = 256;
 static int effective_partition(int partition_tokens, int num_seqs, int num_heads,
@@ -1465,8 +1468,12 @@ static int effective_partition(int partition_tokens, int num_seqs, int num_heads
   const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * block_size;
   const int group = num_kv_heads >= 1 ? num_heads / num_kv_heads : 1;
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 1023) / 1024);
-  if (group >= 2 && decode_tc_supported(group, head_size, block_size, 1024))
+  if (group >= 2 && decode_tc_supported(group, head_size, block_size, 1024)) {
+    const int64_t units2 = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 2047) / 2048);
+    if (units2 >= kBigPartitionUnitsTc && decode_tc_supported(group, head_size, block_size, 2048))
+      return 2048;
     return units >= kBigPartitionUnitsTc ? 1024 : (max_ctx >= 32768 ? 1024 : 512);
+  }
   const bool warp_tensor = group >= 2 && block_size >= 8 &&
                            !decode_tc_supported(group, head_size, block_size, 512);
   if (warp_tensor && units >= kBigPartitionUnits) return 1024;

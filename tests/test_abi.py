@@ -37,12 +37,16 @@ def test_status_strings_and_version():
 def _default_partition(S, H, Hkv, D, mb, B):
     """The default partition as the header states it: 1024 tokens when
     S * Hkv * ceil(max/1024) reaches 1024 for query groups of 2 to 16 heads per
-    KV head (B >= 8), or 256 for groups of 32/64/128 (the tensor-memory path);
-    else 512, or 1024 for tables of 32768 tokens or more."""
+    KV head (B >= 8), or 256 for groups of 32/64/128 (the tensor-memory path,
+    which takes 2048 when S * Hkv * ceil(max/2048) reaches 256 and a partition
+    holds at most 254 blocks); else 512, or 1024 for tables of 32768 tokens or
+    more."""
     group = H // Hkv
     units = S * Hkv * -(-(mb * B) // 1024)
     tc = group >= 32 and 128 % group == 0 and D in (64, 128) and B >= 8 and 1024 // B + 2 <= 256
     if tc:
+        if S * Hkv * -(-(mb * B) // 2048) >= 256 and 2048 // B + 2 <= 256:
+            return 2048
         return 1024 if units >= 256 or mb * B >= 32768 else 512
     warp_tensor = 2 <= group and B >= 8
     if warp_tensor and units >= 1024:
@@ -58,7 +62,8 @@ def test_workspace_size_formula():
                                     (8, 32, 8, 128, 8192, 16, 0), (64, 40, 40, 128, 128, 16, 0),
                                     (256, 32, 8, 128, 98, 16, 0), (16, 32, 8, 128, 98, 16, 0),
                                     (128, 64, 1, 128, 256, 16, 0), (256, 32, 8, 128, 98, 4, 0),
-                                    (16, 128, 4, 64, 40, 32, 0), (16, 32, 1, 128, 40, 16, 1024)]:
+                                    (16, 128, 4, 64, 40, 32, 0), (16, 32, 1, 128, 40, 16, 1024),
+                                    (128, 64, 1, 128, 512, 8, 0), (96, 64, 1, 128, 256, 16, 0)]:
         eff = pt or _default_partition(S, H, Hkv, D, mb, B)
         assert pk.pkv_decode_partition_tokens(S, H, Hkv, D, mb, B, pt) == eff
         parts = -(-(mb * B) // eff)
@@ -66,11 +71,16 @@ def test_workspace_size_formula():
         assert (pk.pkv_decode_workspace_size(S, H, Hkv, D, mb, B, pt)
                 == rows * D * 4 + -(-rows * 8 // 16) * 16 + 16)
     # the shared-prefix batch (256 beams, 32/8 heads) takes 1024-token partitions,
-    # the same heads over 16 sequences 512, MHA 512, 64 heads on one KV head 1024
+    # the same heads over 16 sequences 512, MHA 512; 64 heads on one KV head
+    # 2048 over 128 sequences of up to 4096 tokens (1024 with 8-row blocks, whose
+    # 2048-token partitions would hold 256 blocks; 1024 over 96 sequences), 512
+    # over 16
     assert pk.pkv_decode_partition_tokens(256, 32, 8, 128, 98, 16, 0) == 1024
     assert pk.pkv_decode_partition_tokens(16, 32, 8, 128, 98, 16, 0) == 512
     assert pk.pkv_decode_partition_tokens(64, 40, 40, 128, 128, 16, 0) == 512
-    assert pk.pkv_decode_partition_tokens(128, 64, 1, 128, 256, 16, 0) == 1024
+    assert pk.pkv_decode_partition_tokens(128, 64, 1, 128, 256, 16, 0) == 2048
+    assert pk.pkv_decode_partition_tokens(128, 64, 1, 128, 512, 8, 0) == 1024
+    assert pk.pkv_decode_partition_tokens(96, 64, 1, 128, 256, 16, 0) == 1024
     assert pk.pkv_decode_partition_tokens(16, 64, 1, 128, 256, 16, 0) == 512
     assert pk.pkv_decode_workspace_size(4, 8, 0, 128, 10, 16, 0) == 0
 
