@@ -30,16 +30,16 @@
 //  * one thread of warp 2 loads each item's query rows by TMA once the
 //    previous item's S products are done;
 //  * a softmax warpgroup per query tile, one thread per query row (its TMEM
-//    lane): it reads the row's 128 scores from tensor
-//    memory in one load (a tensor-memory round trip costs hundreds of
-//    cycles under load, so a tile takes one load and one store), runs a
+//    lane): it reads the row's 128 scores from tensor memory in one load (a
+//    tensor-memory round trip costs hundreds of cycles under load, so a tile
+//    takes one load and one store), runs a
 //    base-2 online softmax with lazy rescale (the output row is rescaled in
 //    place only when the running maximum grows by more than 2^8) and writes
 //    P back over the scores as 16-bit pairs, where the P V product reads it;
 //    the output row is divided by the row sum at the item's end and the
 //    output columns are handed back to the MMA.
-// Every wait is bounded; a chunk or context length out of range is skipped
-// and reported.
+// Every wait is bounded; a chunk or context length out of range, or a chunk
+// whose rows would pass the end of q, is skipped and reported.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,7 +47,6 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 #include <type_traits>
 
 #include "pagedkv.h"
