@@ -21,9 +21,12 @@
 //    the empty ones. Warp 0 then takes units: its CTA's index first, then
 //    claims from a global counter. Per unit it reads the partition's block ids (one per lane),
 //    loads the G query rows by TMA into a staging buffer and streams
-//    the partition's 64-key K/V tiles into a ring of 4 to 6 stages (as many
-//    as shared memory holds beside the rest), one TMA copy per
-//    physical block and 128-byte line, issued by several lanes at once;
+//    the partition's 64-key K tiles into a ring of 4 to 6 stages (as many
+//    as shared memory holds beside the rest), while warp 2 follows the same
+//    units and streams their V tiles into the same stages: one TMA copy per
+//    physical block and 128-byte line, each warp's lanes issuing a tile's
+//    copies at once (one warp issuing all of them was the stream's limit
+//    below 16-row blocks);
 //  * one thread of warp 1 owns the 512 tensor-memory columns (two 64-column
 //    score buffers, two D-column output buffers and two query buffers, one of
 //    each per unit in flight), copies each unit's query rows from the staging
@@ -61,7 +64,7 @@ constexpr int kRows = 128;             // product rows: 128 / G copies of the gr
 constexpr int kKeys = 64;              // keys per tile
 constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;     // shared memory one CTA may ask for
-constexpr int kThreads = 256;          // warp 0: claims and copies; warp 1: MMA; warps 4-7: softmax
+constexpr int kThreads = 256;          // warp 0: claims, K copies; 1: MMA; 2: V copies; 4-7: softmax
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kMaxIds = 256;           // block ids of one unit, read ahead of its copies
 constexpr int kCompactMaxSeqs = 1024;  // batches up to this size get a compact work list
@@ -124,7 +127,7 @@ struct Layout {
   // q_full, q_free, s_full[2], p_full[2], pv_done[2], o_free[2], drain,
   // mrg_full, mrg_free, never (one that nothing completes: the test hook's)
   static constexpr int kTailBytes = (2 * kMaxStages + 2 * 8 + 4) * 8 +
-                                    2 * static_cast<int>(sizeof(UnitInfo)) + kMaxIds * 4 +
+                                    2 * static_cast<int>(sizeof(UnitInfo)) + 2 * kMaxIds * 4 +
                                     (kCompactMaxSeqs + 4) * 4 + kCompactMaxSeqs * 2 +
                                     kCompactMaxSeqs * 4 + 16;
   static constexpr int kFit =
@@ -135,7 +138,7 @@ struct Layout {
   static constexpr int kNumBars = 2 * kStages + 2 * 8 + 4;
   static constexpr int kOffUnits = kOffBars + kNumBars * 8;
   static constexpr int kOffIds = kOffUnits + 2 * static_cast<int>(sizeof(UnitInfo));
-  static constexpr int kOffPref = kOffIds + kMaxIds * 4;     // whole partitions per sequence
+  static constexpr int kOffPref = kOffIds + 2 * kMaxIds * 4;  // whole partitions per sequence
   static constexpr int kOffOrder = kOffPref + (kCompactMaxSeqs + 4) * 4;  // partial ones, largest first
   static constexpr int kOffLens = kOffOrder + kCompactMaxSeqs * 2;
   static constexpr int kOffTmem = kOffLens + kCompactMaxSeqs * 4;
@@ -302,12 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&stage_full[i], 1);
+      mbar_init(&stage_full[i], 2);                 // the K and the V copy warps
       mbar_init(&stage_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&unit_full[i], 1);
-      mbar_init(&unit_empty[i], kRows + 1);          // the softmax threads and the MMA thread
+      mbar_init(&unit_empty[i], kRows + 2);          // softmax threads, MMA thread, V copy warp
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kRows);
       mbar_init(&pv_done[i], 1);
@@ -333,119 +336,143 @@ __global__ void __launch_bounds__(kThreads, 1)
     build_list(p, max_ctx, reinterpret_cast<int*>(qstage), pref, porder, lens, whole_units,
                partial_units);
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     // ---------------------------------------------------------- claims, copies
+    // Warp 0 takes the units (claims, block ids, query rows) and copies each
+    // tile's K; warp 2 follows the published units and copies the tiles' V.
+    // Each lane issues one copy (one physical block, one 128-byte line), and
+    // each warp's lane 0 arrives on the stage with the bytes of its own copies.
+    const bool leader = warp == 0;
     if (lane == 0) {
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_q);
+      prefetch_tmap(leader ? &tm_k : &tm_v);
+      if (leader) prefetch_tmap(&tm_q);
     }
     const uint64_t policy = l2_evict_first_policy();
     const int R = p.box_rows;
     const uint32_t copy_bytes = static_cast<uint32_t>(R) * 128;
     const int Hkv = p.num_kv_heads;
     const int total = compact ? (whole_units + partial_units) * Hkv : p.total_units;
+    // lane l copies line l % NH of the tile's copy l / NH
+    const int my_c = lane / NH;
+    const int my_h = lane % NH;
+    const CUtensorMap* my_map = leader ? &tm_k : &tm_v;
+    const uint32_t my_off =
+        (leader ? 0u : static_cast<uint32_t>(Lay::kTileBytes)) + my_h * Lay::kLineBytes +
+        my_c * copy_bytes;
     int g = 0;                                             // tiles issued
-    int k = 0;                                             // units published
+    int k = 0;                                             // units published / followed
     int last_issued[kStages];
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_issued[i] = -1;
     bool ok = true;
     for (int claim = 0; ok; ++claim) {
-      // the CTA's own index first (no round trip), then the shared counter
-      int u = blockIdx.x;
-      if (claim > 0) {
-        if (lane == 0) u = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
-      }
+      const int slot = k & 1;
+      int32_t* uids = ids + slot * kMaxIds;                // this unit's block ids
       UnitInfo info{-1, 0, 0, 0};
       int t_begin = 0, t_end = 0;
-      if (u < total) {
-        int seq, kvh, part, L;
-        if (compact) {
-          const int w = u / Hkv;
-          kvh = u - w * Hkv;
-          if (w >= whole_units) {                          // a partial last partition
-            seq = porder[w - whole_units];
-            L = lens[seq];
-            part = L / PT;
-          } else {
-            int lo = 0, hi = p.num_seqs;                   // largest lo with pref[lo] <= w
-            while (hi - lo > 1) {
-              const int mid = (lo + hi) >> 1;
-              if (pref[mid] <= w) lo = mid; else hi = mid;
+      if (leader) {
+        // the CTA's own index first (no round trip), then the shared counter
+        int u = blockIdx.x;
+        if (claim > 0) {
+          if (lane == 0) u = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
+          u = __shfl_sync(0xffffffffu, u, 0);
+        }
+        if (u < total) {
+          int seq, kvh, part, L;
+          if (compact) {
+            const int w = u / Hkv;
+            kvh = u - w * Hkv;
+            if (w >= whole_units) {                        // a partial last partition
+              seq = porder[w - whole_units];
+              L = lens[seq];
+              part = L / PT;
+            } else {
+              int lo = 0, hi = p.num_seqs;                 // largest lo with pref[lo] <= w
+              while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (pref[mid] <= w) lo = mid; else hi = mid;
+              }
+              seq = lo;
+              L = lens[lo];
+              part = w - pref[lo];
             }
-            seq = lo;
-            L = lens[lo];
-            part = w - pref[lo];
+          } else {
+            const int per_part = p.num_seqs * Hkv;
+            part = u / per_part;
+            const int rem = u - part * per_part;
+            seq = rem / Hkv;
+            kvh = rem - seq * Hkv;
+            L = __ldg(p.context_lens + seq);
+            if (L < 1 || L > max_ctx) {
+              if (lane == 0 && part == 0 && kvh == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
+              continue;
+            }
+            if (part * PT >= L) continue;                  // this sequence has no such partition
           }
-        } else {
-          const int per_part = p.num_seqs * Hkv;
-          part = u / per_part;
-          const int rem = u - part * per_part;
-          seq = rem / Hkv;
-          kvh = rem - seq * Hkv;
-          L = __ldg(p.context_lens + seq);
-          if (L < 1 || L > max_ctx) {
-            if (lane == 0 && part == 0 && kvh == 0) flag_error(p.err, PKV_DEVERR_CONTEXT);
-            continue;
-          }
-          if (part * PT >= L) continue;                    // this sequence has no such partition
+          t_begin = part * PT;
+          t_end = min(L, t_begin + PT);
+          info = UnitInfo{seq, kvh, part, L};
         }
-        t_begin = part * PT;
-        t_end = min(L, t_begin + PT);
-        info = UnitInfo{seq, kvh, part, L};
-      }
-      const int b0 = t_begin / B;
-      if (info.seq >= 0) {
-        // lane 0 read the previous unit's ids before the __syncwarp that ends
-        // the loop
-        const int32_t* row =
-            p.block_tables + static_cast<int64_t>(info.seq) * p.max_blocks_per_seq;
-        const int nb = (t_end - 1) / B - b0 + 1;
-        for (int i = lane; i < nb; i += 32) {
-          int32_t id = __ldg(row + b0 + i);
-          if (id < 0 || id >= p.num_blocks) {
-            flag_error(p.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;
-          }
-          ids[i] = id;
+        // the slot's unit two back has been read by all its consumers, and its
+        // block ids by warp 2 (its last arrival)
+        bool w_ok = true;
+        if (lane == 0 && k >= 2) w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1, p.wait_ns);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
         }
-      }
-      __syncwarp();
-      const int slot = k & 1;
-      bool w_ok = true;
-      if (lane == 0 && k >= 2) w_ok = mbar_wait(&unit_empty[slot], ((k >> 1) & 1) ^ 1, p.wait_ns);
-      // the staging buffer, once the previous unit's rows are in tensor memory
-      if (lane == 0 && k >= 1 && info.seq >= 0) w_ok = w_ok && mbar_wait(q_free, (k - 1) & 1, p.wait_ns);
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        units[slot] = info;
         if (info.seq >= 0) {
-          // the group's query rows, once per copy
-          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(NH) * kRows * 128);
-          const int row0 = info.seq * p.num_heads + info.kvh * G;
-#pragma unroll
-          for (int c = 0; c < C; ++c)
-#pragma unroll
-            for (int h = 0; h < NH; ++h)
-              tma_load_3d(qstage + h * kRows * 128 + c * G * 128, &tm_q, q_full, 0, h, row0,
-                          policy);
+          const int b0 = t_begin / B;
+          const int32_t* row =
+              p.block_tables + static_cast<int64_t>(info.seq) * p.max_blocks_per_seq;
+          const int nb = (t_end - 1) / B - b0 + 1;
+          for (int i = lane; i < nb; i += 32) {
+            int32_t id = __ldg(row + b0 + i);
+            if (id < 0 || id >= p.num_blocks) {
+              flag_error(p.err, PKV_DEVERR_BLOCK_ID);
+              id = 0;
+            }
+            uids[i] = id;
+          }
         }
-        mbar_arrive(&unit_full[slot]);
+        __threadfence_block();
+        __syncwarp();
+        // the staging buffer, once the previous unit's rows are in tensor memory
+        if (lane == 0 && k >= 1 && info.seq >= 0) w_ok = mbar_wait(q_free, (k - 1) & 1, p.wait_ns);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          units[slot] = info;
+          if (info.seq >= 0) {
+            // the group's query rows, once per copy
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(NH) * kRows * 128);
+            const int row0 = info.seq * p.num_heads + info.kvh * G;
+#pragma unroll
+            for (int c = 0; c < C; ++c)
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+                tma_load_3d(qstage + h * kRows * 128 + c * G * 128, &tm_q, q_full, 0, h, row0,
+                            policy);
+          }
+          // the release orders the ids' stores before warp 2's reads
+          mbar_arrive(&unit_full[slot]);
+        }
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(&unit_full[slot], (k >> 1) & 1, p.wait_ns))) {
+          ok = false;
+          break;
+        }
+        info = units[slot];
+        if (info.seq >= 0) {
+          t_begin = info.part * PT;
+          t_end = min(info.len, t_begin + PT);
+        }
       }
       ++k;
       if (info.seq < 0) break;
-      // lane l copies line (l / 2) % NH of K (l even) or V (l odd) for the
-      // tile's copy l / (2 NH)
-      const int my_c = lane / (2 * NH);
-      const int my_h = (lane >> 1) % NH;
-      const CUtensorMap* my_map = (lane & 1) ? &tm_v : &tm_k;
-      const uint32_t my_off =
-          (lane & 1) * Lay::kTileBytes + my_h * Lay::kLineBytes + my_c * copy_bytes;
+      const int b0 = t_begin / B;
       const int n_tiles = (t_end - t_begin + kKeys - 1) / kKeys;
       for (int i = 0; i < n_tiles; ++i, ++g) {
         const int st = g % kStages;
@@ -458,18 +485,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t0 = t_begin + i * kKeys;
         const int copies = (min(kKeys, t_end - t0) + R - 1) / R;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&stage_full[st], 2u * NH * copies * copy_bytes);
+          mbar_arrive_expect_tx(&stage_full[st], static_cast<uint32_t>(NH) * copies * copy_bytes);
           last_issued[st] = g;
         }
         __syncwarp();
         if (my_c < copies) {
           const int tk = t0 + my_c * R;
-          const int z = ids[tk / B - b0] * B + tk % B;
+          const int z = uids[tk / B - b0] * B + tk % B;
           tma_load_4d(stages + st * Lay::kStageBytes + my_off, my_map, &stage_full[st], 0, z,
                       info.kvh, my_h, policy);
         }
       }
       __syncwarp();
+      // warp 2 is done with the unit's block ids
+      if (ok && !leader && lane == 0) mbar_arrive(&unit_empty[slot]);
     }
     if (!ok && lane == 0) {
       flag_error(p.err, PKV_DEVERR_TIMEOUT);
