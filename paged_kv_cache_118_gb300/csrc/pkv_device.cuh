@@ -249,14 +249,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
-// Prefetch one box of a 3-D tensor into L2 (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // 4-D tiled TMA load global -> shared, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, uint64_t* bar,
                                             int c0, int c1, int c2, int c3, uint64_t policy) {
@@ -283,11 +275,6 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Named barrier among the first `threads` threads of the CTA.
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ---- packed fp32 pairs (the f32x2 arithmetic of sm_100 and later) --------
